@@ -1,0 +1,20 @@
+"""Seeded synthetic workloads for paged decode attention.
+
+This module only draws random structure (context lengths, physical block
+placement, sharing groups) and random values.  It holds none of the method's
+arithmetic: no attention, no slot arithmetic, no softmax.  Both the oracle
+tests and the CUDA path take their inputs from here, so neither depends on
+the other for data.
+"""
+
+from .synth import (  # noqa: F401
+    CONFIGS,
+    SAMPLING,
+    DecodeConfig,
+    DecodeCase,
+    SamplingConfig,
+    SamplingCase,
+    make_decode_case,
+    make_sampling_case,
+    make_values,
+)
