@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Paged decode attention benchmark on GB300.
+
+One step = the whole decode hot path for one batch: append each sequence's
+newest K/V at its slot (pa_append_kv), copy-on-write copies if the step has
+any (pa_copy_blocks), and paged decode attention (pa_decode).  The workload is
+the Llama-3-70B-shaped decode layer (batch 256, 64 query / 8 KV heads,
+head_dim 128, block 16, context U[1024, 8192], bf16, pool 1.1x, seeded random
+block placement built by the host BlockManager).  Inputs are synthetic and
+seeded; the KV stream of one step (~4.8 GB) is far larger than L2, so no L2
+flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  ``value`` is effective HBM GB/s: algorithmic
+bytes of all ranks' steps / max-over-ranks device time.  ``--impl reference``
+times the CPU fp64 oracle (the reference arm of this build) on a bounded
+sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: effective HBM GB/s (% of GB300 peak), tokens/s"
+WORKLOAD = "llama3_70b_b256"
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic per decode launch (bytes read + written), keyed by a hash
+# of the decode kernel's source; a stale entry reports null.
+TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode_kernel.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_254_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- accounting
+def decode_bytes(ctx, Hq, Hkv, d, B, elem=2) -> int:
+    """Bytes the method must move for one decode call: every cached K and V
+    element once, Q and O once, the block-table entries in use and the
+    context lengths."""
+    ctx = [int(c) for c in ctx]
+    kv = sum(ctx) * Hkv * d * elem * 2
+    qo = 2 * len(ctx) * Hq * d * elem
+    tables = sum(-(-c // B) for c in ctx) * 4
+    return kv + qo + tables + 4 * len(ctx)
+
+
+def append_bytes(T, Hkv, d, elem=2) -> int:
+    """K and V rows read and written, plus the int64 slots."""
+    return 2 * T * Hkv * d * elem * 2 + 8 * T
+
+
+def copy_bytes(n, Hkv, B, d, elem=2) -> int:
+    return 2 * n * Hkv * B * d * elem * 2
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- workload
+def build_step(cfg, device, seed):
+    """Device tensors of one decode step, with the block tables and slot
+    mapping made by the host BlockManager (random placement, seeded)."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_254_gb300 import BlockManager
+    from workloads import make_decode_case
+
+    case = make_decode_case(cfg, device=device, seed=seed, values=True)
+    B = cfg.block_size
+    bm = BlockManager(case.num_blocks, B, seed=seed + 17)
+    N = len(case.context_lens)
+    for s in range(N):
+        if bm.add_sequence(s, int(case.context_lens[s]) - 1) is None:
+            raise RuntimeError("pool too small")
+    snap = bm.snapshot()
+    t0 = time.perf_counter()
+    slots = bm.append_slots(list(range(N)))          # the newest token of every sequence
+    host_ms = (time.perf_counter() - t0) * 1e3
+    copies = bm.take_copies()
+    tables = bm.block_tables(list(range(N)), cfg.max_blocks_per_seq)
+    ctx = bm.context_lens(list(range(N)))
+    assert np.array_equal(ctx, case.context_lens)
+    st = bm.stats()
+    del snap
+    return {
+        "case": case,
+        "q": case.q, "k_pool": case.k_pool, "v_pool": case.v_pool,
+        "k_new": case.k_new, "v_new": case.v_new,
+        "tables_h": tables, "ctx_h": ctx, "slots_h": slots.astype(np.int64), "copies_h": copies,
+        "tables": torch.from_numpy(tables).to(device), "ctx": torch.from_numpy(ctx).to(device),
+        "slots": torch.from_numpy(slots.astype(np.int64)).to(device),
+        "copies": torch.from_numpy(copies).to(device),
+        "host_block_manager_ms": host_ms, "bm_stats": st,
+    }
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def cpu_worker(args):
+    """Time the fp64 oracle on the first sequences of the workload (host
+    cores, single-threaded BLAS) and print one JSON object."""
+    import numpy as np
+
+    from oracle.attention import decode_ref
+    from workloads import CONFIGS, make_decode_case
+
+    cfg = CONFIGS[args.config]
+    n_gen = min(cfg.num_seqs, 48)
+    case = make_decode_case(cfg, device="cpu", seed=args.seed, num_seqs=n_gen)
+    Hq, Hkv, d, B = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    done, ctx_done = 0, []
+    t0 = time.perf_counter()
+    while done < n_gen and time.perf_counter() - t0 < args.cpu_seconds:
+        rows = [(done, h) for h in range(Hq)]
+        decode_ref(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, case.scale, rows=rows)
+        ctx_done.append(int(case.context_lens[done]))
+        done += 1
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B) + append_bytes(done, Hkv, d)
+    print(json.dumps({
+        "value": nbytes / dt / 1e9, "unit": "GB/s", "tokens_per_s": done / dt, "seconds": dt,
+        "sample": f"first {done} of {cfg.num_seqs} sequences of {cfg.name} (all {Hq} query heads, "
+                  f"{sum(ctx_done)} cached tokens), fp64 oracle",
+        "cores": 1,
+    }))
+
+
+def run_cpu_baseline(args) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--config", args.config,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    if args.seed is not None:
+        cmd += ["--seed", str(args.seed)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": out["value"], "unit": "GB/s", "cores": out["cores"], "kind": "oracle",
+            "sample": out["sample"], "tokens_per_s": out["tokens_per_s"]}
+
+
+def reference_arm(args):
+    world, rank, local = dist_env()
+    if world > 1 and rank != 0:
+        return
+    from workloads import CONFIGS
+    cfg = CONFIGS[args.config]
+    vals = []
+    sample = None
+    tok = []
+    per = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        a = argparse.Namespace(**vars(args))
+        a.cpu_seconds = per
+        res = run_cpu_baseline(a)
+        if i >= args.warmup and res["value"] is not None:
+            vals.append(res["value"])
+            tok.append(res["tokens_per_s"])
+            sample = res["sample"]
+    value = statistics.median(vals) if vals else None
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "tokens_per_s": statistics.median(tok) if tok else None,
+        "config": {"workload": cfg.name, "description": cfg.description},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step, about {per:.0f} s of: {sample}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU arm
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_254_gb300 as pa
+    from paged_kv_cache_254_gb300 import _build
+    from workloads import CONFIGS
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    _build.build()
+
+    cfg = CONFIGS[args.config]
+    seed = (cfg.seed if args.seed is None else args.seed) + 1000 * rank
+    st = build_step(cfg, device, seed)
+    Hq, Hkv, d, B = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    N = len(st["ctx_h"])
+    stream = torch.cuda.current_stream(device)
+    out = torch.empty_like(st["q"])
+    ws = pa.workspace_for(st["q"], st["k_pool"], st["tables"])
+    n_copies = int(st["copies"].shape[0])
+
+    def step(q, k_new, v_new, slots, tables, ctx, ev=None):
+        launches = 0
+        if n_copies:
+            pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
+            launches += 1
+        pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["case"].scale, out=out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        return launches + 2
+
+    dev_args = (st["q"], st["k_new"], st["v_new"], st["slots"], st["tables"], st["ctx"])
+    for _ in range(args.warmup):
+        step(*dev_args)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if local == 0:
+        clocks.start()
+        time.sleep(0.05)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    t_start.record(stream)
+    for i in range(args.steps):
+        launches += step(*dev_args, ev=evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if local == 0 else None
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    max_ms = max_over_ranks(total_ms, dist, device)
+
+    # ---- end to end through the public API from pinned host buffers ----
+    host = {k: t.detach().cpu().pin_memory() for k, t in zip(("q", "k_new", "v_new"), dev_args[:3])}
+    host["slots"] = torch.from_numpy(st["slots_h"]).pin_memory()
+    host["tables"] = torch.from_numpy(st["tables_h"]).pin_memory()
+    host["ctx"] = torch.from_numpy(st["ctx_h"]).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k in ("q", "k_new", "v_new", "slots", "tables", "ctx"):
+            dbuf[k].copy_(host[k], non_blocking=True)
+        step(dbuf["q"], dbuf["k_new"], dbuf["v_new"], dbuf["slots"], dbuf["tables"], dbuf["ctx"])
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, device)
+
+    # ---- numbers ----
+    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B)
+    step_bytes = dbytes + append_bytes(N, Hkv, d) + copy_bytes(n_copies, Hkv, B, d)
+    value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
+    tokens = world * args.steps * N / (max_ms * 1e-3)
+    e2e_value = world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = float(peak) if peak else FALLBACK_HBM_GBS
+    dec_avg_ms = statistics.mean(decode_ms)
+    achieved = dbytes / (dec_avg_ms * 1e-3) / 1e9
+    khash = kernel_hash()
+    traffic = TRAFFIC.get(khash)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = run_cpu_baseline(args)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, random block placement)",
+        "config": {"workload": cfg.name, "description": cfg.description, "num_seqs": N, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": d, "block_size": B, "num_blocks": st["case"].num_blocks,
+                   "mean_context": float(np.mean(st["ctx_h"])), "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(tokens, 1),
+        "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_decode_kernel", "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "kernel_hash": khash},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "host_block_manager_ms": round(st["host_block_manager_ms"], 3),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.cpu_worker:
+        cpu_worker(args)
+    elif args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

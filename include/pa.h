@@ -1,0 +1,163 @@
+/*
+ * pa.h -- C ABI of libpa: paged KV-cache decode attention for sm_103a (GB300).
+ *
+ * The KV cache is a pool of fixed-size physical blocks; a sequence reaches its
+ * tokens through a block table (logical block i = floor(t / B), offset
+ * j = t mod B).  Sources: "vLLM & High-Throughput Serving ..." (thewebvale.com),
+ * section 2 "PagedAttention: Virtual Memory Virtualization ...", block-table
+ * formula; "AI Inference Serving at Scale ..." (ontq.xyz), section 3
+ * "PagedAttention: Virtual Memory and Paging for GPU Tensors".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor argument is a DEVICE pointer to contiguous row-major memory
+ *    owned by the caller.  The library allocates nothing and keeps no
+ *    per-call state between calls (it caches per-device launch properties).
+ *  - 16-bit element pointers (q, pools, out, new K/V) must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work on `stream` and return; the caller synchronises.
+ *  - Host-side argument checks run before any launch; a failing check returns
+ *    its status and enqueues nothing.
+ *  - Bad data found on the device (a block id outside [0, num_blocks), a
+ *    context length outside [0, max_blocks_per_seq * block_size], a slot past
+ *    the pool, a bad copy pair) never traps: the kernel ORs a PA_DEVERR_* bit
+ *    into `*err_word` (if err_word is not NULL), skips the bad access, and
+ *    writes NaN to the affected decode rows.  pa_read_error() turns the word
+ *    into a status.
+ *
+ * Pool layout: k_pool and v_pool are [num_blocks][num_kv_heads][block_size]
+ * [head_dim]; one (block, kv head) chunk is block_size * head_dim contiguous
+ * elements.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, misaligned pointer, Hq % Hkv != 0 */
+    PA_ERR_UNSUPPORTED = 2,   /* a shape outside the compiled set (see pa_decode) */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    PA_ERR_OUT_OF_RANGE = 4,  /* device found a bad block id, context length, slot or copy pair */
+    PA_ERR_TIMEOUT = 5,       /* a device-side wait ran past its limit; the kernel gave up */
+    PA_ERR_WORKSPACE = 6      /* workspace missing or smaller than pa_decode_workspace_bytes() */
+} pa_status;
+
+typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits ORed into *err_word by the kernels. */
+#define PA_DEVERR_BLOCK_ID  1u   /* block table entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT   2u   /* context length < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEVERR_SLOT      4u   /* slot >= num_blocks * block_size */
+#define PA_DEVERR_COPY_PAIR 8u   /* copy pair id outside [0, num_blocks) */
+#define PA_DEVERR_TIMEOUT   16u  /* a bounded wait expired */
+
+typedef struct pa_shape {
+    int32_t num_seqs;            /* N: sequences in the batch (>= 0) */
+    int32_t num_q_heads;         /* Hq */
+    int32_t num_kv_heads;        /* Hkv; query head h reads KV head h / (Hq / Hkv) */
+    int32_t head_dim;            /* d */
+    int32_t block_size;          /* B: tokens per physical block */
+    int32_t num_blocks;          /* NB: blocks in the pool */
+    int32_t max_blocks_per_seq;  /* MB: columns of the block table */
+    int32_t dtype;               /* pa_dtype of q, pools, out and new K/V */
+} pa_shape;
+
+/*
+ * Bytes of scratch that pa_decode needs for `shape` on the CURRENT device.
+ * The workspace holds the per-(sequence, KV head) arrival counters and the
+ * partial softmax states of sequences whose keys are split across thread
+ * blocks.  It must be zero-filled once before its first use; every completed
+ * pa_decode call leaves the counter region zero again, so the same buffer can
+ * be reused by later calls on the same stream.  Calls that may run at the same
+ * time must use different workspaces.  Returns 0 if the shape is invalid or
+ * unsupported.
+ */
+size_t pa_decode_workspace_bytes(const pa_shape* shape);
+
+/*
+ * Paged decode attention ("How LLM Inference Engines Work ..." by
+ * letsbuildsolutions.com, section "PagedAttention: Virtual Memory for KV
+ * Caches": the kernel gathers K and V from non-adjacent blocks; ontq section 8:
+ * the result equals un-paged attention; ontq section 6: grouped-query heads).
+ *
+ * For each sequence b and query head h, with g = Hq / Hkv, kh = h / g and
+ * n = context_lens[b]:
+ *     s_t  = scale * <q[b,h,:], K_pool[table[b][t/B], kh, t%B, :]>,  t < n
+ *     out[b,h,:] = sum_t softmax(s)_t * V_pool[table[b][t/B], kh, t%B, :]
+ * accumulated in fp32 and rounded once to the output dtype.  n == 0 gives a
+ * zero row.  Table entries past ceil(n / B) and pool slots past position n-1
+ * are never read.
+ *
+ *   q             [N][Hq][d]            query of the newest token
+ *   k_pool,v_pool [NB][Hkv][B][d]       the cache
+ *   block_tables  int32 [N][MB]         physical block ids in logical order
+ *   context_lens  int32 [N]             tokens cached per sequence (incl. the newest)
+ *   scale         fp32 softmax scale (typically 1/sqrt(d))
+ *   out           [N][Hq][d]            result, same dtype as q
+ *   workspace     see pa_decode_workspace_bytes
+ *   err_word      device uint32, may be NULL
+ *
+ * Supported: dtype fp16 or bf16; d in {64, 128}; B in {16, 32};
+ * g in {1, 2, 4, 8, 16}; NB * Hkv * B < 2^31.  Others: PA_ERR_UNSUPPORTED.
+ * Results are deterministic for a given device and input, and bitwise
+ * independent of where the blocks sit in the pool.
+ */
+pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                    void* stream);
+
+/*
+ * Append new tokens' keys and values to the cache (ontq section 3, on-demand
+ * allocation; thewebvale section 2, block table).  For i < num_tokens with
+ * slot = slot_mapping[i] >= 0:
+ *     k_pool[slot / B][kh][slot % B][:] = k_new[i][kh][:]   for every kh (same for V)
+ * A negative slot skips the row.  Bit-exact copy.  Two live rows with the same
+ * slot in one call race (the block manager never emits that).
+ *
+ *   k_new, v_new  [num_tokens][Hkv][d]
+ *   slot_mapping  int64 [num_tokens]
+ * Uses shape->num_kv_heads, head_dim, block_size, num_blocks, dtype.
+ */
+pa_status pa_append_kv(const pa_shape* shape, int32_t num_tokens, const void* k_new,
+                       const void* v_new, const int64_t* slot_mapping, void* k_pool,
+                       void* v_pool, uint32_t* err_word, void* stream);
+
+/*
+ * Copy-on-write block copies (ontq section 3, "Copy-on-Write Memory
+ * Sharing": only the diverged block is copied; thewebvale section 2).  For each
+ * pair (src, dst) = (pairs[2i], pairs[2i+1]), i < num_pairs, the whole block
+ * (every KV head and slot, K and V) of src is copied to dst.  Bit-exact.  A dst
+ * must not appear twice or as a src in the same call (the block manager
+ * always copies into a freshly taken block); src == dst is a no-op.
+ *
+ *   src_dst_pairs int32 [num_pairs][2] (device)
+ */
+pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs,
+                         void* k_pool, void* v_pool, uint32_t* err_word, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word and map it to a status:
+ * PA_ERR_TIMEOUT if the timeout bit is set, else PA_ERR_OUT_OF_RANGE if any
+ * other bit is set, else PA_OK.  The word is left unchanged.
+ */
+pa_status pa_read_error(const uint32_t* err_word, void* stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

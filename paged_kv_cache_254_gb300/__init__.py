@@ -1,0 +1,24 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a).
+
+* ``pa_decode``, ``pa_append_kv``, ``pa_copy_blocks``, ``pa_read_error`` --
+  thin bindings of the C ABI in ``include/pa.h`` (libpa.so, CUDA kernels).
+* ``BlockManager`` -- host bookkeeping that builds block tables, slot
+  mappings and copy-on-write copy lists.
+
+The CUDA library is loaded on first use; without it every entry point raises.
+"""
+
+from ._lib import PagedAttentionError  # noqa: F401
+from .block_manager import BlockManager  # noqa: F401
+from .ops import (  # noqa: F401
+    make_shape,
+    new_error_word,
+    pa_append_kv,
+    pa_copy_blocks,
+    pa_decode,
+    pa_decode_workspace_bytes,
+    pa_read_error,
+    workspace_for,
+)
+
+__version__ = "0.1.0"

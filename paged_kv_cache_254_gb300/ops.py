@@ -1,0 +1,160 @@
+"""Python entry points with the C ABI's names: torch tensors in, kernels run.
+
+PyTorch supplies device memory and streams only.  Each function checks that
+its tensors sit on one CUDA device with the expected dtype and layout, then
+calls the matching ``pa_*`` function of libpa.so on the current stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float16: _lib.PA_FP16, torch.bfloat16: _lib.PA_BF16}
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device, stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+               dtype) -> _lib.PaShape:
+    return _lib.PaShape(int(num_seqs), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                        int(num_blocks), int(max_blocks_per_seq), _DTYPES[dtype])
+
+
+def _pool_shape(k_pool, num_seqs=0, num_q_heads=1, max_blocks=1) -> _lib.PaShape:
+    NB, Hkv, B, d = k_pool.shape
+    return make_shape(num_seqs, num_q_heads, Hkv, d, B, NB, max_blocks, k_pool.dtype)
+
+
+def pa_decode_workspace_bytes(q, k_pool, block_tables) -> int:
+    N, Hq, _ = q.shape
+    shape = _pool_shape(k_pool, N, Hq, block_tables.shape[1])
+    with torch.cuda.device(q.device):
+        return int(_lib.load().pa_decode_workspace_bytes(ctypes.byref(shape)))
+
+
+_ws_lock = threading.Lock()
+_ws_cache = {}
+
+
+def workspace_for(q, k_pool, block_tables, stream=None) -> torch.Tensor:
+    """A zero-filled workspace kept per (device, stream) and grown on demand.
+    pa_decode leaves its counters at zero, so the buffer is reused as is."""
+    need = pa_decode_workspace_bytes(q, k_pool, block_tables)
+    if need == 0:
+        return torch.empty(0, dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    key = (q.device.index, s.cuda_stream)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=q.device)
+            _ws_cache[key] = ws
+        return ws
+
+
+def new_error_word(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def pa_decode(q, k_pool, v_pool, block_tables, context_lens, scale, out=None, workspace=None, err=None,
+              stream=None):
+    """out[N, Hq, d] = paged decode attention of q over the pools (see include/pa.h)."""
+    _need_cuda("q", q)
+    _need_cuda("k_pool", k_pool, q.dtype)
+    _need_cuda("v_pool", v_pool, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if q.dtype not in _DTYPES:
+        raise TypeError("q must be float16 or bfloat16")
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or q.dim() != 3:
+        raise ValueError("q [N, Hq, d], k_pool and v_pool [NB, Hkv, B, d]")
+    N, Hq, d = q.shape
+    if k_pool.shape[3] != d or block_tables.dim() != 2 or block_tables.shape[0] != N or context_lens.shape != (N,):
+        raise ValueError("shape mismatch between q, pools, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = workspace_for(q, k_pool, block_tables, stream)
+    else:
+        _need_cuda("workspace", workspace)
+    if err is not None:
+        _need_cuda("err", err, torch.int32)
+    shape = _pool_shape(k_pool, N, Hq, block_tables.shape[1])
+    with torch.cuda.device(q.device):
+        st = _lib.load().pa_decode(ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                   _ptr(context_lens), ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                                   ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(err),
+                                   _stream(q.device, stream))
+    _lib.check(st, "pa_decode")
+    return out
+
+
+def pa_append_kv(k_new, v_new, slot_mapping, k_pool, v_pool, err=None, stream=None):
+    """Write k_new/v_new [T, Hkv, d] into the pools at slot_mapping [T] (int64; < 0 skips)."""
+    _need_cuda("k_pool", k_pool)
+    _need_cuda("v_pool", v_pool, k_pool.dtype)
+    _need_cuda("k_new", k_new, k_pool.dtype)
+    _need_cuda("v_new", v_new, k_pool.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    T = slot_mapping.shape[0]
+    if k_new.shape != (T,) + tuple(k_pool.shape[1:2]) + tuple(k_pool.shape[3:]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new, v_new must be [T, Hkv, d]")
+    if err is not None:
+        _need_cuda("err", err, torch.int32)
+    shape = _pool_shape(k_pool)
+    with torch.cuda.device(k_pool.device):
+        st = _lib.load().pa_append_kv(ctypes.byref(shape), ctypes.c_int32(T), _ptr(k_new), _ptr(v_new),
+                                      _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool), _ptr(err),
+                                      _stream(k_pool.device, stream))
+    _lib.check(st, "pa_append_kv")
+
+
+def pa_copy_blocks(src_dst_pairs, k_pool, v_pool, err=None, stream=None):
+    """Copy whole blocks src -> dst for each row of src_dst_pairs [n, 2] (int32)."""
+    _need_cuda("k_pool", k_pool)
+    _need_cuda("v_pool", v_pool, k_pool.dtype)
+    _need_cuda("src_dst_pairs", src_dst_pairs, torch.int32)
+    if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+    if err is not None:
+        _need_cuda("err", err, torch.int32)
+    shape = _pool_shape(k_pool)
+    with torch.cuda.device(k_pool.device):
+        st = _lib.load().pa_copy_blocks(ctypes.byref(shape), _ptr(src_dst_pairs),
+                                        ctypes.c_int32(src_dst_pairs.shape[0]), _ptr(k_pool), _ptr(v_pool),
+                                        _ptr(err), _stream(k_pool.device, stream))
+    _lib.check(st, "pa_copy_blocks")
+
+
+def pa_read_error(err, stream=None) -> int:
+    """Synchronise the stream and return the status the error word maps to."""
+    _need_cuda("err", err, torch.int32)
+    with torch.cuda.device(err.device):
+        return int(_lib.load().pa_read_error(_ptr(err), _stream(err.device, stream)))

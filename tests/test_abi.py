@@ -1,0 +1,106 @@
+"""The C ABI library builds, loads and exports what include/pa.h declares;
+host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_254_gb300 import _build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = header_functions()
+    assert set(declared) == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_version() == 100
+    for code in range(7):
+        assert lib.pa_status_string(code).decode() not in ("", "unknown status")
+    assert lib.pa_status_string(99).decode() == "unknown status"
+
+
+def shape(**kw):
+    base = dict(num_seqs=4, num_q_heads=8, num_kv_heads=8, head_dim=64, block_size=16, num_blocks=64,
+                max_blocks_per_seq=7, dtype=_lib.PA_FP16)
+    base.update(kw)
+    return _lib.PaShape(*[base[f] for f, _ in _lib.PaShape._fields_])
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: checks fail before any launch
+NULL = ctypes.c_void_p(0)
+
+
+def decode_status(lib, s, q=FAKE, scale=0.125, ws=FAKE, ws_bytes=1 << 30):
+    return lib.pa_decode(ctypes.byref(s), q, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(scale), FAKE, ws,
+                         ctypes.c_size_t(ws_bytes), NULL, NULL)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_q_heads=12, num_kv_heads=8), 1),      # Hq % Hkv != 0
+    (dict(num_kv_heads=0), 1),
+    (dict(num_seqs=-1), 1),
+    (dict(dtype=7), 1),
+    (dict(head_dim=96), 2),
+    (dict(block_size=8), 2),
+    (dict(num_q_heads=24, num_kv_heads=8), 2),      # group of 3
+    (dict(num_q_heads=64, num_kv_heads=2), 2),      # group of 32
+    (dict(num_blocks=1 << 26, num_kv_heads=8, num_q_heads=8), 2),   # pool rows >= 2^31
+])
+def test_decode_rejects_bad_shapes(lib, kw, status):
+    assert decode_status(lib, shape(**kw)) == status
+
+
+def test_decode_rejects_null_and_misaligned(lib):
+    s = shape()
+    assert decode_status(lib, s, q=NULL) == 1
+    assert decode_status(lib, s, q=ctypes.c_void_p((1 << 20) + 2)) == 1
+    assert decode_status(lib, s, scale=float("nan")) == 1
+    assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), FAKE, FAKE, 0, NULL, NULL) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert decode_status(lib, shape(num_seqs=0)) == 0
+
+
+def test_append_and_copy_checks(lib):
+    s = shape()
+    assert lib.pa_append_kv(ctypes.byref(s), -1, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_append_kv(ctypes.byref(s), 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL) == 0
+    assert lib.pa_append_kv(ctypes.byref(s), 3, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_copy_blocks(ctypes.byref(s), FAKE, -2, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_copy_blocks(ctypes.byref(s), NULL, 0, NULL, NULL, NULL, NULL) == 0
+    assert lib.pa_copy_blocks(ctypes.byref(s), NULL, 4, FAKE, FAKE, NULL, NULL) == 1
+    bad = shape(dtype=3)
+    assert lib.pa_copy_blocks(ctypes.byref(bad), FAKE, 1, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_read_error(NULL, NULL) == 1
+
+
+def test_workspace_query_rejects_bad_shape(lib):
+    assert lib.pa_decode_workspace_bytes(ctypes.byref(shape(head_dim=80))) == 0
+    assert lib.pa_decode_workspace_bytes(None) == 0
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "library_path", lambda: "/nonexistent/libpa.so")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.load()

@@ -103,9 +103,20 @@ def _torch_gen(seed: int, device) -> torch.Generator:
 
 
 def make_values(shape, dtype: str, gen: torch.Generator, device) -> torch.Tensor:
-    """Standard-normal values in the storage dtype (drawn in fp32, rounded once)."""
-    t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
-    return t.to(DTYPES[dtype])
+    """Standard-normal values in the storage dtype (drawn in fp32, rounded
+    once), generated in slices along the first dimension so large pools do
+    not need an fp32 copy of their own size."""
+    out = torch.empty(shape, dtype=DTYPES[dtype], device=device)
+    if out.numel() == 0:
+        return out
+    rows = out.shape[0]
+    per_row = out.numel() // rows
+    step = max(1, (1 << 27) // max(per_row, 1))
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        out[r0:r1] = torch.randn((r1 - r0,) + tuple(out.shape[1:]), generator=gen, device=device,
+                                 dtype=torch.float32)
+    return out
 
 
 def _context_lens(cfg: DecodeConfig, rng: np.random.Generator) -> np.ndarray:
