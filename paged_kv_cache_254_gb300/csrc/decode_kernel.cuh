@@ -94,7 +94,7 @@ struct DecodeTraits {
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
-    static_assert(STAGES >= 2, "ring");
+    static_assert(STAGES >= 2 && STAGES % NC == 0, "ring stages are owned by consumer warps");
 };
 
 // Shared CTA bookkeeping written by warp 0 before the roles split.
@@ -375,7 +375,12 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 for (int e = 0; e < 4; ++e) o[mt][r][e] = 0.f;
         int poisoned = 0;
 
-        for (int j = warp; j < len; j += NC) {
+        // Block k of the CTA range (k = gi - lo) goes to warp k % NC.  With
+        // STAGES a multiple of NC every ring stage is owned by one warp, which
+        // consumes its fills strictly in order (no mbarrier phase aliasing).
+        int j0 = warp - (int)((it.gi - lo) % NC);
+        if (j0 < 0) j0 += NC;
+        for (int j = j0; j < len; j += NC) {
             const long long k = it.gi + j - lo;
             const int st = (int)(k % S);
             const uint32_t par = (uint32_t)((k / S) & 1);
@@ -447,14 +452,21 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     }
                 }
             // P^T fragments (B operand of O^T += V^T P^T): k = tokens, n = heads.
-            uint32_t pb[Tr::KT][Tr::NR][2];
+            // P is carried as hi + lo, two 16-bit parts (hi = round(p),
+            // lo = round(p - hi)), so the product keeps ~16 bits of p instead
+            // of the 8 a single bf16 would leave.
+            uint32_t pb[Tr::KT][Tr::NR][2], pl[Tr::KT][Tr::NR][2];
 #pragma unroll
             for (int kt = 0; kt < Tr::KT; ++kt)
 #pragma unroll
-                for (int r = 0; r < Tr::NR; ++r) {
-                    pb[kt][r][0] = pack2<Tr::BF16>(sacc[2 * kt][2 * r], sacc[2 * kt][2 * r + 1]);
-                    pb[kt][r][1] = pack2<Tr::BF16>(sacc[2 * kt + 1][2 * r], sacc[2 * kt + 1][2 * r + 1]);
-                }
+                for (int r = 0; r < Tr::NR; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float x0 = sacc[2 * kt + h][2 * r], x1 = sacc[2 * kt + h][2 * r + 1];
+                        const uint32_t hi = pack2<Tr::BF16>(x0, x1);
+                        pb[kt][r][h] = hi;
+                        pl[kt][r][h] = pack2<Tr::BF16>(x0 - lo_of<Tr::BF16>(hi), x1 - hi_of<Tr::BF16>(hi));
+                    }
 
             // Rows past the context in a partly filled block may hold anything
             // (even NaN); zero them so 0 * V stays 0 in the PV product.
@@ -495,8 +507,10 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     const int chunk = 2 * mt + ((lane >> 3) & 1);
                     ldsm_x4_t(vb + swz<Tr>(row, chunk), a0, a1, a2, a3);
 #pragma unroll
-                    for (int r = 0; r < Tr::NR; ++r)
+                    for (int r = 0; r < Tr::NR; ++r) {
                         mma16816<Tr::BF16>(o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
+                        mma16816<Tr::BF16>(o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
+                    }
                 }
             if (valid < BS) fence_proxy_async_smem();
             __syncwarp();

@@ -129,6 +129,29 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// The two halves of a packed 16-bit pair, widened exactly to fp32.
+template <bool BF16>
+__device__ __forceinline__ float lo_of(uint32_t v) {
+    if constexpr (BF16) {
+        return __uint_as_float(v << 16);
+    } else {
+        float f;
+        asm("{\n\t.reg .f16 h;\n\tmov.b32 {h, _}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));
+        return f;
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float hi_of(uint32_t v) {
+    if constexpr (BF16) {
+        return __uint_as_float(v & 0xffff0000u);
+    } else {
+        float f;
+        asm("{\n\t.reg .f16 h;\n\tmov.b32 {_, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));
+        return f;
+    }
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
 }

@@ -54,7 +54,7 @@ class DecodeConfig:
 
     @property
     def max_blocks_per_seq(self) -> int:
-        return -(-self.max_context_len // self.block_size)
+        return max(1, -(-self.max_context_len // self.block_size))
 
 
 CONFIGS = {
