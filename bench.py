@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="truncate the batch (small profiling captures); the JSON line says so")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -173,7 +175,7 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 
 # --------------------------------------------------------------------------- workload
-def build_step(cfg, device, seed):
+def build_step(cfg, device, seed, num_seqs=None):
     """Device tensors of one decode step, with the block tables and slot
     mapping made by the host BlockManager (random placement, seeded)."""
     import numpy as np
@@ -182,7 +184,7 @@ def build_step(cfg, device, seed):
     from paged_kv_cache_254_gb300 import BlockManager
     from workloads import make_decode_case
 
-    case = make_decode_case(cfg, device=device, seed=seed, values=True)
+    case = make_decode_case(cfg, device=device, seed=seed, values=True, num_seqs=num_seqs)
     B = cfg.block_size
     bm = BlockManager(case.num_blocks, B, seed=seed + 17)
     N = len(case.context_lens)
@@ -310,7 +312,7 @@ def gpu_arm(args):
 
     cfg = CONFIGS[args.config]
     seed = (cfg.seed if args.seed is None else args.seed) + 1000 * rank
-    st = build_step(cfg, device, seed)
+    st = build_step(cfg, device, seed, args.num_seqs)
     Hq, Hkv, d, B = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     N = len(st["ctx_h"])
     stream = torch.cuda.current_stream(device)
@@ -416,7 +418,8 @@ def gpu_arm(args):
                    "num_kv_heads": Hkv, "head_dim": d, "block_size": B, "num_blocks": st["case"].num_blocks,
                    "mean_context": float(np.mean(st["ctx_h"])), "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "truncated_batch": args.num_seqs},
         "tokens_per_s": round(tokens, 1),
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

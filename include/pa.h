@@ -73,11 +73,11 @@ typedef struct pa_shape {
  * Bytes of scratch that pa_decode needs for `shape` on the CURRENT device.
  * The workspace holds the per-(sequence, KV head) arrival counters and the
  * partial softmax states of sequences whose keys are split across thread
- * blocks.  It must be zero-filled once before its first use; every completed
- * pa_decode call leaves the counter region zero again, so the same buffer can
- * be reused by later calls on the same stream.  Calls that may run at the same
- * time must use different workspaces.  Returns 0 if the shape is invalid or
- * unsupported.
+ * blocks.  It needs no initialisation: pa_decode clears the counter region on
+ * `stream` (cudaMemsetAsync) before its kernel.  The same buffer can serve any
+ * later call on the same stream, whatever its shape; calls that may run at the
+ * same time must use different workspaces.  Returns 0 if the shape is invalid
+ * or unsupported.
  */
 size_t pa_decode_workspace_bytes(const pa_shape* shape);
 

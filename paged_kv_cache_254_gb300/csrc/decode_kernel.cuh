@@ -15,8 +15,9 @@
 // range as "segments" (the part of one pair that falls in the range).  A pair
 // that lies inside one CTA is finished there; a pair cut by range boundaries
 // leaves a partial softmax state (m, l, unnormalised o) per piece in the
-// workspace, and the last CTA to finish a piece of that pair (arrival counter)
-// merges them with the log-sum-exp rule in CTA order and resets the counter.
+// workspace, and the last CTA to finish a piece of that pair (arrival counter,
+// zeroed by the host before the launch) merges them with the log-sum-exp rule
+// in CTA order.
 // Everything about the split depends on context lengths only, never on block
 // ids, so results are bitwise independent of block placement.
 //
@@ -51,7 +52,7 @@ struct DecodeParams {
     const int32_t* block_tables;  // [N][MB]
     const int32_t* context_lens;  // [N]
     uint16_t* out;                // [N][Hq][D]
-    int32_t* counters;            // [N * Hkv], zero between calls
+    int32_t* counters;            // [N * Hkv], zeroed before each launch
     float* partials;              // [gridDim.x][2][G][D + 2]
     uint32_t* err;                // may be null
     int32_t N, Hq, Hkv, NB, MB;
@@ -615,7 +616,6 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     }
                     orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L);
                 }
-                if (tid == 0) p.counters[pair] = 0;
             }
         }
         named_bar_sync(1, NC * 32);

@@ -177,6 +177,9 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     L.p.timeout_ns = kTimeoutNs;
     L.stream = static_cast<cudaStream_t>(stream);
     L.grid = ctas;
+    // Arrival counters start at zero for every call (the region may hold
+    // another shape's partial states from an earlier call).
+    if (cudaMemsetAsync(workspace, 0, counters_bytes(shape), L.stream) != cudaSuccess) return PA_ERR_CUDA;
     return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -60,8 +60,8 @@ _ws_cache = {}
 
 
 def workspace_for(q, k_pool, block_tables, stream=None) -> torch.Tensor:
-    """A zero-filled workspace kept per (device, stream) and grown on demand.
-    pa_decode leaves its counters at zero, so the buffer is reused as is."""
+    """A workspace kept per (device, stream) and grown on demand; pa_decode
+    clears its counter region itself, so the buffer is reused as is."""
     need = pa_decode_workspace_bytes(q, k_pool, block_tables)
     if need == 0:
         return torch.empty(0, dtype=torch.uint8, device=q.device)
