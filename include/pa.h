@@ -144,6 +144,33 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
                          void* k_pool, void* v_pool, uint32_t* err_word, void* stream);
 
 /*
+ * Paged decode attention without caller-provided scratch -- no counterpart on
+ * the pages; it exists for callers that cannot allocate device memory (a host
+ * framework that has reserved the device's memory for its own pool, a plugin
+ * host that passes only inputs and outputs, a serving loop that must not call
+ * cudaMalloc/cudaFree because they may synchronise the device).
+ *
+ * Same arguments and results as pa_decode, minus the workspace: the scratch is
+ * a static device buffer of PA_NOALLOC_SCRATCH_BYTES inside the library, held
+ * on every GPU that loads it until the process exits.  This call allocates
+ * nothing.
+ *  - Shapes whose pa_decode_workspace_bytes() exceeds PA_NOALLOC_SCRATCH_BYTES
+ *    are rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the buffer's address on that device
+ *    (with it current); make that first call before any stream capture.
+ *  - Every call on a device shares the one buffer and it keeps the last call's
+ *    contents (the call clears the part that must start at zero).  Calls that
+ *    overlap on the GPU -- on different streams, or unordered from different
+ *    threads -- race on it and give wrong results; order them on one stream.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+pa_status pa_decode_noalloc(const pa_shape* shape, const void* q, const void* k_pool,
+                            const void* v_pool, const int32_t* block_tables,
+                            const int32_t* context_lens, float scale, void* out,
+                            uint32_t* err_word, void* stream);
+
+/*
  * Synchronise `stream`, read the device error word and map it to a status:
  * PA_ERR_TIMEOUT if the timeout bit is set, else PA_ERR_OUT_OF_RANGE if any
  * other bit is set, else PA_OK.  The word is left unchanged.

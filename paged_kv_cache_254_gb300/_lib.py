@@ -24,7 +24,8 @@ DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT =
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
-           "pa_status_string", "pa_version")
+           "pa_status_string", "pa_version", "pa_decode_noalloc")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class PaShape(ctypes.Structure):
@@ -83,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_version.argtypes = []
         lib.pa_version.restype = I32
+        lib.pa_decode_noalloc.argtypes = [SP, P, P, P, P, P, ctypes.c_float, P, P, P]
+        lib.pa_decode_noalloc.restype = I32
         _lib = lib
         return lib
 
