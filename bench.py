@@ -41,7 +41,9 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic per decode launch (bytes read + written), keyed by a hash
 # of the decode kernel's source; a stale entry reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    ("b01e7ef0750b7170", "llama3_70b_b256"): 4_838_000_000,   # 4.83 GB read + 7.94 MB written
+}
 
 
 def kernel_hash() -> str:
@@ -175,41 +177,77 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 
 # --------------------------------------------------------------------------- workload
-def build_step(cfg, device, seed, num_seqs=None):
-    """Device tensors of one decode step, with the block tables and slot
-    mapping made by the host BlockManager (random placement, seeded)."""
+def unique_decode_bytes(tables, ctx, Hq, Hkv, d, B, elem=2) -> int:
+    """Like decode_bytes, but each physical block's valid tokens count once
+    however many sequences share it (the shared-prompt workload)."""
+    filled = {}
+    for row, n in zip(tables, ctx):
+        n = int(n)
+        for i in range(-(-n // B)):
+            b = int(row[i])
+            filled[b] = max(filled.get(b, 0), min(B, n - i * B))
+    kv = sum(filled.values()) * Hkv * d * elem * 2
+    qo = 2 * len(ctx) * Hq * d * elem
+    return kv + qo + sum(-(-int(c) // B) for c in ctx) * 4 + 4 * len(ctx)
+
+
+def make_workload(name, device, seed, num_seqs=None) -> dict:
+    """Device tensors of one decode step.  Block tables, lengths, slot mapping
+    and copy list come from the host BlockManager (seeded random placement);
+    values from the seeded workload generators."""
     import numpy as np
     import torch
 
     from paged_kv_cache_254_gb300 import BlockManager
-    from workloads import make_decode_case
+    from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case
 
-    case = make_decode_case(cfg, device=device, seed=seed, values=True, num_seqs=num_seqs)
-    B = cfg.block_size
-    bm = BlockManager(case.num_blocks, B, seed=seed + 17)
-    N = len(case.context_lens)
-    for s in range(N):
-        if bm.add_sequence(s, int(case.context_lens[s]) - 1) is None:
-            raise RuntimeError("pool too small")
-    snap = bm.snapshot()
-    t0 = time.perf_counter()
-    slots = bm.append_slots(list(range(N)))          # the newest token of every sequence
-    host_ms = (time.perf_counter() - t0) * 1e3
+    if name == SAMPLING.name:
+        cfg = SAMPLING
+        seed = cfg.seed if seed is None else seed
+        case = make_sampling_case(cfg, device=device, seed=seed)
+        B, S = cfg.block_size, cfg.samples
+        G = case.prompt_blocks.shape[0]
+        bm = BlockManager(case.num_blocks, B, seed=seed + 17)
+        for g in range(G):
+            if bm.add_sequence((g, 0), cfg.prompt_len) is None:
+                raise RuntimeError("pool too small")
+            for j in range(1, S):
+                bm.fork((g, 0), (g, j))
+        seqs = [(g, j) for g in range(G) for j in range(S)]
+        reqs = [(sq, int(case.tails[i]) + 1) for i, sq in enumerate(seqs)]
+        t0 = time.perf_counter()
+        slots = bm.append_slots(reqs)                # each sample's tail and new token
+        host_ms = (time.perf_counter() - t0) * 1e3
+        max_blocks = cfg.max_blocks_per_seq
+        desc, Hq, Hkv, d = cfg.description, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    else:
+        cfg = CONFIGS[name]
+        seed = cfg.seed if seed is None else seed
+        case = make_decode_case(cfg, device=device, seed=seed, values=True, num_seqs=num_seqs)
+        B = cfg.block_size
+        bm = BlockManager(case.num_blocks, B, seed=seed + 17)
+        seqs = list(range(len(case.context_lens)))
+        for s in seqs:
+            if bm.add_sequence(s, int(case.context_lens[s]) - 1) is None:
+                raise RuntimeError("pool too small")
+        t0 = time.perf_counter()
+        slots = bm.append_slots(seqs)                # the newest token of every sequence
+        host_ms = (time.perf_counter() - t0) * 1e3
+        max_blocks = cfg.max_blocks_per_seq
+        desc, Hq, Hkv, d = cfg.description, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
     copies = bm.take_copies()
-    tables = bm.block_tables(list(range(N)), cfg.max_blocks_per_seq)
-    ctx = bm.context_lens(list(range(N)))
-    assert np.array_equal(ctx, case.context_lens)
-    st = bm.stats()
-    del snap
+    tables = bm.block_tables(seqs, max_blocks)
+    ctx = bm.context_lens(seqs)
+    slots = slots.astype(np.int64)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     return {
-        "case": case,
-        "q": case.q, "k_pool": case.k_pool, "v_pool": case.v_pool,
-        "k_new": case.k_new, "v_new": case.v_new,
-        "tables_h": tables, "ctx_h": ctx, "slots_h": slots.astype(np.int64), "copies_h": copies,
-        "tables": torch.from_numpy(tables).to(device), "ctx": torch.from_numpy(ctx).to(device),
-        "slots": torch.from_numpy(slots.astype(np.int64)).to(device),
-        "copies": torch.from_numpy(copies).to(device),
-        "host_block_manager_ms": host_ms, "bm_stats": st,
+        "name": name, "description": desc, "Hq": Hq, "Hkv": Hkv, "d": d, "B": B,
+        "num_blocks": case.num_blocks, "scale": case.scale,
+        "q": case.q, "k_pool": case.k_pool, "v_pool": case.v_pool, "k_new": case.k_new, "v_new": case.v_new,
+        "tables_h": tables, "ctx_h": ctx, "slots_h": slots, "copies_h": copies,
+        "tables": to(tables), "ctx": to(ctx), "slots": to(slots), "copies": to(copies),
+        "host_block_manager_ms": host_ms, "bm_stats": bm.stats(),
+        "shared": name == SAMPLING.name,
     }
 
 
@@ -217,27 +255,36 @@ def build_step(cfg, device, seed, num_seqs=None):
 def cpu_worker(args):
     """Time the fp64 oracle on the first sequences of the workload (host
     cores, single-threaded BLAS) and print one JSON object."""
-    import numpy as np
-
     from oracle.attention import decode_ref
-    from workloads import CONFIGS, make_decode_case
+    from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case, sampling_tables
 
-    cfg = CONFIGS[args.config]
-    n_gen = min(cfg.num_seqs, 48)
-    case = make_decode_case(cfg, device="cpu", seed=args.seed, num_seqs=n_gen)
-    Hq, Hkv, d, B = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
-    done, ctx_done = 0, []
+    if args.config == SAMPLING.name:
+        cfg = SAMPLING
+        case = make_sampling_case(cfg, device="cpu", seed=args.seed, groups=8)
+        tables, ctx_all = sampling_tables(case)
+        n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    else:
+        cfg = CONFIGS[args.config]
+        case = make_decode_case(cfg, device="cpu", seed=args.seed, num_seqs=min(cfg.num_seqs, 48))
+        tables, ctx_all = case.block_tables, case.context_lens
+        n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    n_gen = len(ctx_all)
+    done = 0
     t0 = time.perf_counter()
     while done < n_gen and time.perf_counter() - t0 < args.cpu_seconds:
         rows = [(done, h) for h in range(Hq)]
-        decode_ref(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, case.scale, rows=rows)
-        ctx_done.append(int(case.context_lens[done]))
+        decode_ref(case.q, case.k_pool, case.v_pool, tables, ctx_all, case.scale, rows=rows)
         done += 1
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B) + append_bytes(done, Hkv, d)
+    ctx_done = [int(c) for c in ctx_all[:done]]
+    if args.config == SAMPLING.name:
+        nbytes = unique_decode_bytes(tables[:done], ctx_done, Hq, Hkv, d, B)
+    else:
+        nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B)
+    nbytes += append_bytes(done, Hkv, d)
     print(json.dumps({
         "value": nbytes / dt / 1e9, "unit": "GB/s", "tokens_per_s": done / dt, "seconds": dt,
-        "sample": f"first {done} of {cfg.num_seqs} sequences of {cfg.name} (all {Hq} query heads, "
+        "sample": f"first {done} of {n_total} sequences of {cfg.name} (all {Hq} query heads, "
                   f"{sum(ctx_done)} cached tokens), fp64 oracle",
         "cores": 1,
     }))
@@ -266,8 +313,8 @@ def reference_arm(args):
     world, rank, local = dist_env()
     if world > 1 and rank != 0:
         return
-    from workloads import CONFIGS
-    cfg = CONFIGS[args.config]
+    from workloads import CONFIGS, SAMPLING
+    cfg = SAMPLING if args.config == SAMPLING.name else CONFIGS[args.config]
     vals = []
     sample = None
     tok = []
@@ -302,19 +349,17 @@ def gpu_arm(args):
 
     import paged_kv_cache_254_gb300 as pa
     from paged_kv_cache_254_gb300 import _build
-    from workloads import CONFIGS
-
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
     _build.build()
 
-    cfg = CONFIGS[args.config]
-    seed = (cfg.seed if args.seed is None else args.seed) + 1000 * rank
-    st = build_step(cfg, device, seed, args.num_seqs)
-    Hq, Hkv, d, B = cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    seed = None if args.seed is None and rank == 0 else (args.seed or 0) + 1000 * rank
+    st = make_workload(args.config, device, seed, args.num_seqs)
+    Hq, Hkv, d, B = st["Hq"], st["Hkv"], st["d"], st["B"]
     N = len(st["ctx_h"])
+    T = int(st["slots_h"].shape[0])
     stream = torch.cuda.current_stream(device)
     out = torch.empty_like(st["q"])
     ws = pa.workspace_for(st["q"], st["k_pool"], st["tables"])
@@ -328,7 +373,7 @@ def gpu_arm(args):
         pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
             ev[0].record(stream)
-        pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["case"].scale, out=out, workspace=ws)
+        pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], out=out, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
         return launches + 2
@@ -391,7 +436,9 @@ def gpu_arm(args):
 
     # ---- numbers ----
     dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B)
-    step_bytes = dbytes + append_bytes(N, Hkv, d) + copy_bytes(n_copies, Hkv, B, d)
+    ubytes = unique_decode_bytes(st["tables_h"], st["ctx_h"], Hq, Hkv, d, B) if st["shared"] else dbytes
+    extra = append_bytes(T, Hkv, d) + copy_bytes(n_copies, Hkv, B, d)
+    step_bytes = ubytes + extra
     value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
     tokens = world * args.steps * N / (max_ms * 1e-3)
     e2e_value = world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9
@@ -400,32 +447,36 @@ def gpu_arm(args):
     peak_src = "measured" if peak else "fallback"
     peak = float(peak) if peak else FALLBACK_HBM_GBS
     dec_avg_ms = statistics.mean(decode_ms)
-    achieved = dbytes / (dec_avg_ms * 1e-3) / 1e9
+    achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = TRAFFIC.get(khash)
+    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None else None
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = run_cpu_baseline(args)
+    cfg_out = {"workload": st["name"], "description": st["description"], "num_seqs": N, "num_q_heads": Hq,
+               "num_kv_heads": Hkv, "head_dim": d, "block_size": B, "num_blocks": st["num_blocks"],
+               "mean_context": float(np.mean(st["ctx_h"])), "appended_tokens": T, "cow_copies": n_copies,
+               "bytes_per_step": step_bytes,
+               "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
+               "parallelism": f"replicas x{world}", "truncated_batch": args.num_seqs}
+    if st["shared"]:
+        cfg_out["bytes_note"] = ("value counts each shared physical block once (unique bytes); "
+                                 "logical_gbs counts every sequence's reads")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) values, random block placement)",
-        "config": {"workload": cfg.name, "description": cfg.description, "num_seqs": N, "num_q_heads": Hq,
-                   "num_kv_heads": Hkv, "head_dim": d, "block_size": B, "num_blocks": st["case"].num_blocks,
-                   "mean_context": float(np.mean(st["ctx_h"])), "bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
-                   "parallelism": f"replicas x{world}",
-                   "truncated_batch": args.num_seqs},
+        "config": cfg_out,
         "tokens_per_s": round(tokens, 1),
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "pa_decode_kernel", "peak_source": f"{peak_src} hbm_gbs",
-                     "algorithmic_bytes_per_launch": dbytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
@@ -434,6 +485,8 @@ def gpu_arm(args):
         "host_block_manager_ms": round(st["host_block_manager_ms"], 3),
         "cpu_baseline": cpu,
     }
+    if st["shared"]:
+        line["logical_gbs"] = round(world * args.steps * (dbytes + extra) / (max_ms * 1e-3) / 1e9, 2)
     print(json.dumps(line))
 
 

@@ -112,3 +112,31 @@ def test_restore_round_trip():
     bm2 = BlockManager.restore(bm.snapshot())
     assert bm2.snapshot() == bm.snapshot()
     assert bm2.append_slots(["x"]).tolist() == bm.append_slots(["x"]).tolist()
+
+
+def test_parallel_sampling_flow_matches_reference_at_full_size():
+    """The shared-prompt workload driven through both managers: 64 prompts of
+    2032 tokens (block 32), 7 forks each, then every sample's tail and new
+    token in one request list."""
+    from workloads import SAMPLING, make_sampling_case
+    case = make_sampling_case(SAMPLING, values=False)
+    cfg = SAMPLING
+    order = [int(b) for b in np.random.Generator(np.random.PCG64(5)).permutation(case.num_blocks)]
+    bm = BlockManager(case.num_blocks, cfg.block_size, free_order=order)
+    ref = RefBlockManager(cfg.block_size, order)
+    for g in range(cfg.groups):
+        assert bm.add_sequence((g, 0), cfg.prompt_len).tolist() == ref.add_sequence((g, 0), cfg.prompt_len)
+        for j in range(1, cfg.samples):
+            bm.fork((g, 0), (g, j))
+            ref.fork((g, 0), (g, j))
+    reqs = [((g, j), int(case.tails[g * cfg.samples + j]) + 1) for g in range(cfg.groups)
+            for j in range(cfg.samples)]
+    assert bm.append_slots(reqs).tolist() == ref.append_tokens(reqs)
+    copies = bm.take_copies()
+    assert copies.tolist() == [list(c) for c in ref.take_copies()]
+    assert copies.shape == (cfg.groups * (cfg.samples - 1), 2)
+    same_state(bm, ref)
+    for g in range(cfg.groups):
+        rows = [bm.table((g, j)) for j in range(cfg.samples)]
+        assert all(r[:63] == rows[0][:63] for r in rows)            # 63 full prompt blocks shared
+        assert len({r[63] for r in rows}) == cfg.samples               # the half-full one: 7 copies + original

@@ -8,7 +8,7 @@ import torch
 from oracle.attention import decode_ref
 from oracle.kv_ops import append_ref, bits, copy_ref, slot_of
 from tests.gpu_util import assert_close, dev_case, from_bits, need_gpu
-from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case, make_values
+from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case, make_values, sampling_tables
 
 pytestmark = pytest.mark.gpu
 
@@ -110,23 +110,6 @@ def test_decode_step_with_append():
     ref = decode_ref(case.q, from_bits(want_k, dt), from_bits(want_v, dt), case.block_tables, case.context_lens,
                      case.scale)
     assert_close(out, ref, what="append + decode")
-
-
-def sampling_tables(case):
-    """Post-divergence block tables from the generated sharing structure."""
-    cfg = case.cfg
-    nS = case.prompt_blocks.shape[0] * cfg.samples
-    mb = cfg.max_blocks_per_seq
-    tables = np.full((nS, mb), -1, dtype=np.int32)
-    for i in range(nS):
-        grp = i // cfg.samples
-        row = list(case.prompt_blocks[grp])
-        if case.private_last[i] >= 0:
-            row[-1] = int(case.private_last[i])
-        row += [int(b) for b in case.tail_blocks[i]]
-        tables[i, :len(row)] = row
-    ctx = (cfg.prompt_len + case.tails.astype(np.int64) + 1).astype(np.int32)
-    return tables, ctx
 
 
 @pytest.mark.parametrize("groups", [3, None])

@@ -17,4 +17,5 @@ from .synth import (  # noqa: F401
     make_decode_case,
     make_sampling_case,
     make_values,
+    sampling_tables,
 )

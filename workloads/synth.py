@@ -301,3 +301,20 @@ def make_sampling_case(cfg: SamplingConfig = SAMPLING, device="cpu", seed: Optio
         case.k_new = make_values((T, hkv, d), cfg.dtype, g, device)
         case.v_new = make_values((T, hkv, d), cfg.dtype, g, device)
     return case
+
+
+def sampling_tables(case: SamplingCase):
+    """Block tables and lengths of every sample after the divergent step:
+    the group's prompt blocks (the last one replaced by the sample's private
+    copy where it has one), then the sample's own tail blocks."""
+    cfg = case.cfg
+    nS = case.prompt_blocks.shape[0] * cfg.samples
+    tables = np.full((nS, cfg.max_blocks_per_seq), -1, dtype=np.int32)
+    for i in range(nS):
+        row = [int(b) for b in case.prompt_blocks[i // cfg.samples]]
+        if case.private_last[i] >= 0:
+            row[-1] = int(case.private_last[i])
+        row += [int(b) for b in case.tail_blocks[i]]
+        tables[i, :len(row)] = row
+    ctx = (cfg.prompt_len + case.tails.astype(np.int64) + 1).astype(np.int32)
+    return tables, ctx
