@@ -156,3 +156,68 @@ def lse_merge_ref(parts) -> np.ndarray:
     L = sum(l * np.exp(m - M) for m, l, _ in parts)
     O = sum(o * np.exp(m - M) for m, _, o in parts)
     return O / L
+
+
+# ---------------------------------------------------------------------------
+# Shared prompt prefixes: sequences of a group point at the same leading
+# blocks (ontq section 3, copy-on-write sharing of prompt blocks;
+# letsbuildsolutions "Production Considerations", prefix caching).
+# ---------------------------------------------------------------------------
+
+def check_prefix_groups(block_tables, context_lens, group_starts, group_prefix_blocks, block_size):
+    """True when every member of each group has the group's shared leading
+    table entries and at least that many full blocks of context."""
+    bt = _i64(block_tables)
+    cl = _i64(context_lens)
+    gs = [int(x) for x in group_starts]
+    for gi, pblk in enumerate(int(x) for x in group_prefix_blocks):
+        for s in range(gs[gi], gs[gi + 1]):
+            if cl[s] < pblk * block_size:
+                return False
+            if any(bt[s, i] != bt[gs[gi], i] for i in range(pblk)):
+                return False
+    return True
+
+
+def decode_shared_prefix_ref(q, k_pool, v_pool, block_tables, context_lens, scale, group_starts,
+                             group_prefix_blocks, rows=None) -> np.ndarray:
+    """Decode attention computed in two parts per row, as a prefix-aware
+    kernel would: the shared prefix keys (read through the group's first
+    member's table) and the row's own remaining keys, each reduced to a
+    partition state and combined by the log-sum-exp rule.  Equal to
+    ``decode_ref`` whenever the groups are consistent."""
+    qf = f64(q)
+    bt = _i64(block_tables)
+    cl = _i64(context_lens)
+    N, Hq, d = qf.shape
+    Hkv, B = k_pool.shape[1], k_pool.shape[2]
+    g = Hq // Hkv
+    prefix_of = np.zeros(N, dtype=np.int64)
+    owner = np.arange(N)
+    gs = [int(x) for x in group_starts]
+    for gi, pblk in enumerate(int(x) for x in group_prefix_blocks):
+        for s in range(gs[gi], gs[gi + 1]):
+            prefix_of[s] = pblk
+            owner[s] = gs[gi]
+    out = np.full((N, Hq, d), np.nan)
+    todo = [(b, h) for b in range(N) for h in range(Hq)] if rows is None else list(rows)
+    cache = {}
+    for b, h in todo:
+        ctx = int(cl[b])
+        if ctx == 0:
+            out[b, h] = 0.0
+            continue
+        kh = h // g
+        npre = int(prefix_of[b]) * B
+        if (b, kh) not in cache:
+            K, V = gather_sequence(k_pool, v_pool, bt[b], ctx, kh, B)
+            if npre:
+                Kp, Vp = gather_sequence(k_pool, v_pool, bt[owner[b]], npre, kh, B)
+                K = np.concatenate([Kp, K[npre:]])
+                V = np.concatenate([Vp, V[npre:]])
+            cache = {(b, kh): (K, V)}
+        K, V = cache[(b, kh)]
+        parts = [partial_ref(qf[b, h], K, V, scale, lo, hi)
+                 for lo, hi in ((0, npre), (npre, ctx)) if hi > lo]
+        out[b, h] = lse_merge_ref(parts)
+    return out

@@ -263,3 +263,53 @@ def test_on_demand_waste_below_one_block():
     waste = sum(sizes.wasted_slots(int(n), 16) for n in lens)
     assert all(sizes.wasted_slots(int(n), 16) < 16 for n in lens)
     assert waste / (waste + lens.sum()) < 0.04
+
+
+def _shared_prefix_case(seed, B=4, groups=((0, 3, 2), (3, 5, 1)), tail_max=9, Hq=4, Hkv=2, d=8):
+    """Sequences grouped as (start, end, shared full blocks); members copy the
+    first member's leading table entries, then own blocks.  One extra
+    sequence sits outside every group."""
+    r = _rng(seed)
+    N = max(e for _, e, _ in groups) + 1
+    ctx = np.zeros(N, dtype=np.int64)
+    tables = np.full((N, 12), -1)
+    nxt = iter(r.permutation(200))
+    for s0, s1, p in groups:
+        shared = [next(nxt) for _ in range(p)]
+        for s in range(s0, s1):
+            ctx[s] = p * B + int(r.integers(0, tail_max))
+            own = [next(nxt) for _ in range(-(-ctx[s] // B) - p)]
+            tables[s, :len(shared) + len(own)] = shared + own
+    ctx[N - 1] = 13
+    tables[N - 1, :4] = [next(nxt) for _ in range(4)]
+    kp = r.standard_normal((200, Hkv, B, d))
+    vp = r.standard_normal((200, Hkv, B, d))
+    q = r.standard_normal((N, Hq, d))
+    starts = [g[0] for g in groups] + [groups[-1][1]]
+    return q, kp, vp, tables, ctx, starts, [g[2] for g in groups]
+
+
+@pytest.mark.parametrize("seed", [20, 22, 23])
+def test_shared_prefix_split_equals_plain_decode(seed):
+    from oracle.attention import check_prefix_groups, decode_shared_prefix_ref
+    q, kp, vp, tables, ctx, starts, pre = _shared_prefix_case(seed)
+    assert check_prefix_groups(tables, ctx, starts, pre, 4)
+    a = decode_shared_prefix_ref(q, kp, vp, tables, ctx, 0.3, starts, pre)
+    b = decode_ref(q, kp, vp, tables, ctx, 0.3)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+def test_shared_prefix_reads_the_first_members_table():
+    # If a member's table disagrees inside the shared prefix the check fails,
+    # and the prefix-aware form follows the group's first member.
+    from oracle.attention import check_prefix_groups, decode_shared_prefix_ref
+    q, kp, vp, tables, ctx, starts, pre = _shared_prefix_case(21)
+    bad = tables.copy()
+    bad[1, 0] = 199
+    assert not check_prefix_groups(bad, ctx, starts, pre, 4)
+    a = decode_shared_prefix_ref(q, kp, vp, bad, ctx, 0.3, starts, pre)
+    b = decode_ref(q, kp, vp, tables, ctx, 0.3)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+    short = ctx.copy()
+    short[3] = 2                                   # shorter than its group's shared block
+    assert not check_prefix_groups(tables, short, starts, pre, 4)
