@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plain-decode", action="store_true",
+                    help="decode shared-prompt batches without the prefix-aware pass")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="truncate the batch (small profiling captures); the JSON line says so")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
@@ -238,6 +240,7 @@ def make_workload(name, device, seed, num_seqs=None) -> dict:
     copies = bm.take_copies()
     tables = bm.block_tables(seqs, max_blocks)
     ctx = bm.context_lens(seqs)
+    gstarts, gprefix = bm.shared_prefix_groups(seqs)
     slots = slots.astype(np.int64)
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     return {
@@ -248,6 +251,7 @@ def make_workload(name, device, seed, num_seqs=None) -> dict:
         "tables": to(tables), "ctx": to(ctx), "slots": to(slots), "copies": to(copies),
         "host_block_manager_ms": host_ms, "bm_stats": bm.stats(),
         "shared": name == SAMPLING.name,
+        "group_starts": to(gstarts), "group_prefix": to(gprefix), "n_groups": int(gprefix.size),
     }
 
 
@@ -368,6 +372,7 @@ def gpu_arm(args):
     out = torch.empty_like(st["q"])
     ws = pa.workspace_for(st["q"], st["k_pool"], st["tables"])
     n_copies = int(st["copies"].shape[0])
+    use_prefix = st["n_groups"] > 0 and not args.plain_decode
 
     def step(q, k_new, v_new, slots, tables, ctx, ev=None):
         launches = 0
@@ -377,7 +382,12 @@ def gpu_arm(args):
         pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
             ev[0].record(stream)
-        pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], out=out, workspace=ws)
+        if use_prefix:
+            pa.pa_decode_shared_prefix(q, st["k_pool"], st["v_pool"], tables, ctx, st["group_starts"],
+                                       st["group_prefix"], st["scale"], out=out)
+            launches += 1
+        else:
+            pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], out=out, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
         return launches + 2
@@ -479,7 +489,8 @@ def gpu_arm(args):
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode_kernel", "peak_source": f"{peak_src} hbm_gbs",
+                     "kernel": "pa_prefix_kernel + pa_decode_kernel" if use_prefix else "pa_decode_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -489,6 +500,8 @@ def gpu_arm(args):
         "host_block_manager_ms": round(st["host_block_manager_ms"], 3),
         "cpu_baseline": cpu,
     }
+    if use_prefix:
+        cfg_out["prefix_groups"] = st["n_groups"]
     if st["shared"]:
         line["logical_gbs"] = round(world * args.steps * (dbytes + extra) / (max_ms * 1e-3) / 1e9, 2)
     print(json.dumps(line))

@@ -57,6 +57,7 @@ typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEVERR_SLOT      4u   /* slot >= num_blocks * block_size */
 #define PA_DEVERR_COPY_PAIR 8u   /* copy pair id outside [0, num_blocks) */
 #define PA_DEVERR_TIMEOUT   16u  /* a bounded wait expired */
+#define PA_DEVERR_GROUP     32u  /* prefix group malformed, or a member does not share the prefix */
 
 typedef struct pa_shape {
     int32_t num_seqs;            /* N: sequences in the batch (>= 0) */
@@ -113,6 +114,39 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
                     const int32_t* block_tables, const int32_t* context_lens, float scale,
                     void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
                     void* stream);
+
+/*
+ * Prefix-aware paged decode: the same results as pa_decode (up to rounding
+ * order), with the leading blocks that a group of sequences shares read once
+ * for the whole group.  Parallel samples of one prompt and requests behind a
+ * common system prompt point at the same physical prompt blocks (ontq
+ * section 3, "Copy-on-Write Memory Sharing"; letsbuildsolutions,
+ * "Production Considerations", prefix caching; thewebvale section 2).
+ *
+ *   num_groups           groups of sequences (0: plain decode)
+ *   group_starts         device int32 [num_groups + 1], ascending: group i is
+ *                        sequences [group_starts[i], group_starts[i + 1])
+ *   group_prefix_blocks  device int32 [num_groups]: every member of group i has
+ *                        the same first group_prefix_blocks[i] table entries
+ *                        and at least that many full blocks of context
+ * Sequences outside every group are decoded as by pa_decode.  The kernel
+ * checks the claim: a member whose table or length breaks it, or a malformed
+ * group description, sets PA_DEVERR_GROUP and the affected rows are NaN (a
+ * malformed group is treated as having no prefix); no access leaves the
+ * tables, pools or workspace.  Two launches on `stream`: the prefix pass
+ * (one (group, KV head) item reads the shared blocks for up to 32 query rows)
+ * and the decode over each sequence's own blocks, which folds the prefix
+ * state in by the log-sum-exp rule.  Workspace: see
+ * pa_decode_shared_prefix_workspace_bytes (no initialisation needed).
+ */
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape);
+
+pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const void* k_pool,
+                                  const void* v_pool, const int32_t* block_tables,
+                                  const int32_t* context_lens, int32_t num_groups,
+                                  const int32_t* group_starts, const int32_t* group_prefix_blocks,
+                                  float scale, void* out, void* workspace, size_t workspace_bytes,
+                                  uint32_t* err_word, void* stream);
 
 /*
  * Append new tokens' keys and values to the cache (ontq section 3, on-demand

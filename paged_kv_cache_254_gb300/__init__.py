@@ -16,6 +16,7 @@ from .ops import (  # noqa: F401
     pa_append_kv,
     pa_copy_blocks,
     pa_decode,
+    pa_decode_shared_prefix,
     pa_decode_workspace_bytes,
     pa_read_error,
     workspace_for,

@@ -20,11 +20,12 @@ STATUS_NAMES = {
     4: "PA_ERR_OUT_OF_RANGE", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE",
 }
 PA_FP16, PA_BF16 = 0, 1
-DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, DEVERR_GROUP = 1, 2, 4, 8, 16, 32
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
-           "pa_status_string", "pa_version", "pa_decode_noalloc")
+           "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
+           "pa_decode_shared_prefix")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -86,6 +87,10 @@ def load() -> ctypes.CDLL:
         lib.pa_version.restype = I32
         lib.pa_decode_noalloc.argtypes = [SP, P, P, P, P, P, ctypes.c_float, P, P, P]
         lib.pa_decode_noalloc.restype = I32
+        lib.pa_decode_shared_prefix_workspace_bytes.argtypes = [SP]
+        lib.pa_decode_shared_prefix_workspace_bytes.restype = SZ
+        lib.pa_decode_shared_prefix.argtypes = [SP, P, P, P, P, P, I32, P, P, ctypes.c_float, P, P, SZ, P, P]
+        lib.pa_decode_shared_prefix.restype = I32
         _lib = lib
         return lib
 

@@ -83,6 +83,47 @@ class BlockManager:
             out[i, :len(b)] = b
         return out
 
+    def shared_prefix_groups(self, seqs: Sequence, min_members: int = 2):
+        """Find runs of consecutive sequences (in batch order) whose tables
+        begin with the same full blocks, for prefix-aware decode.
+
+        Returns (group_starts [G + 1], group_prefix_blocks [G]) as int32
+        arrays: group i is seqs[group_starts[i]:group_starts[i + 1]] and its
+        members share their first group_prefix_blocks[i] blocks, each
+        completely filled in every member.  Gaps between runs become groups
+        with no shared blocks, so the boundaries stay contiguous."""
+        B = self.block_size
+        runs = []
+        i, n = 0, len(seqs)
+        while i < n:
+            first = self._blocks[seqs[i]]
+            j = i + 1
+            while j < n and first and self._blocks[seqs[j]][:1] == first[:1]:
+                j += 1
+            if j - i >= min_members:
+                p = min(self._len[s] for s in seqs[i:j]) // B
+                for s in seqs[i + 1:j]:
+                    b = self._blocks[s]
+                    k = 0
+                    while k < p and b[k] == first[k]:
+                        k += 1
+                    p = k
+                if p > 0:
+                    runs.append((i, j, p))
+            i = j
+        bounds, prefix = [], []
+        for a, b, p in runs:
+            if bounds and bounds[-1] < a:
+                prefix.append(0)
+                bounds.append(a)
+            elif not bounds:
+                bounds.append(a)
+            prefix.append(p)
+            bounds.append(b)
+        if not bounds:
+            bounds = [0]
+        return np.asarray(bounds, dtype=np.int32), np.asarray(prefix, dtype=np.int32)
+
     def context_lens(self, seqs: Sequence) -> np.ndarray:
         return np.array([self._len[s] for s in seqs], dtype=np.int32)
 

@@ -10,40 +10,35 @@
 // (ontq "AI Inference Serving at Scale", section 6, grouped-query attention).
 //
 // Work split.  The (sequence, KV head) pairs are laid end to end, each
-// contributing ceil(ctx / B) blocks; the flattened block list is cut into
-// gridDim.x equal contiguous ranges, one per persistent CTA.  A CTA walks its
-// range as "segments" (the part of one pair that falls in the range).  A pair
-// that lies inside one CTA is finished there; a pair cut by range boundaries
-// leaves a partial softmax state (m, l, unnormalised o) per piece in the
-// workspace, and the last CTA to finish a piece of that pair (arrival counter,
-// zeroed by the host before the launch) merges them with the log-sum-exp rule
-// in CTA order.
+// contributing its blocks; the flattened block list is cut into gridDim.x
+// equal contiguous ranges, one per persistent CTA.  A CTA walks its range as
+// "segments" (the part of one pair that falls in the range).  A pair that lies
+// inside one CTA is finished there; a pair cut by range boundaries leaves a
+// partial softmax state (m, l, unnormalised o) per piece in the workspace, and
+// the last CTA to finish a piece of that pair (arrival counter, zeroed by the
+// host before the launch) merges them with the log-sum-exp rule in CTA order.
 // Everything about the split depends on context lengths only, never on block
 // ids, so results are bitwise independent of block placement.
+//
+// Shared prefixes (optional).  With prefix groups, the first
+// group_prefix_blocks blocks of a member sequence were already reduced by the
+// prefix kernel into a per-row state (the carry); here the pair covers only
+// the sequence's own blocks after the prefix, and the carry joins the final
+// log-sum-exp combination.
 //
 // Inside a CTA.  Warp NC is the producer: it reads block ids from the table
 // (32 at a time, one per lane), and lane 0 issues two-dimensional TMA loads
 // (128-byte swizzle) of each (block, KV head) K chunk and V chunk into a ring
 // of shared-memory stages guarded by full/empty mbarriers.  Warps 0..NC-1 are
-// consumers: within a segment, warp w takes blocks w, w+NC, ...; per block it
-// computes S^T = Q K^T for the whole query-head group with mma.sync
-// (m16n8k16, fp32 accumulate; heads are the M rows, padded to 16), runs the
-// online-softmax update in registers (row max over the lanes of a row by
-// shuffles, exp2 with the scale folded into log2(e)), and accumulates
-// O^T += V^T P^T with mma.sync, feeding the probabilities straight from the
-// score fragments.  At the end of a segment the NC warp states are merged
-// through shared memory.
+// consumers: block k of the CTA range goes to warp k % NC, which folds it in
+// with consume_block() (mma.sync scores, online softmax, PV).  At the end of a
+// segment the NC warp states are merged through shared memory.
 //
 // Every wait is bounded (PA_DEVERR_TIMEOUT); bad block ids and context lengths
 // set error bits and poison the affected rows with NaN instead of trapping.
 #pragma once
 
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cstdint>
-
-#include "ptx.cuh"
-#include "../../include/pa.h"
+#include "decode_common.cuh"
 
 namespace pa {
 
@@ -55,34 +50,32 @@ struct DecodeParams {
     int32_t* counters;            // [N * Hkv], zeroed before each launch
     float* partials;              // [gridDim.x][2][G][D + 2]
     uint32_t* err;                // may be null
+    // shared prefixes (n_groups == 0: none)
+    const int32_t* grp_starts;    // [n_groups + 1], ascending
+    const int32_t* grp_prefix;    // [n_groups] shared leading blocks
+    const float* carry;           // [N][Hq][D + 2] prefix states (o, m, l)
+    int32_t n_groups;
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
     uint64_t timeout_ns;
 };
 
 template <int D_, int BS_, int G_, bool BF16_>
-struct DecodeTraits {
-    static constexpr int D = D_;
-    static constexpr int BS = BS_;
+struct DecodeTraits : Geom<D_, BS_> {
+    using Gm = Geom<D_, BS_>;
     static constexpr int G = G_;
     static constexpr bool BF16 = BF16_;
     static constexpr int NC = 4;                            // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int HALVES = D / 64;                   // 128-byte column boxes per row
-    static constexpr int BOX_BYTES = BS * 128;
-    static constexpr int CHUNK_BYTES = HALVES * BOX_BYTES;  // one (block, head) chunk
-    static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;     // K + V
     static constexpr int RING_TARGET = 64 * 1024;
-    static constexpr int STAGES = (RING_TARGET / STAGE_BYTES) > 16 ? 16 : (RING_TARGET / STAGE_BYTES);
+    static constexpr int STAGES =
+        (RING_TARGET / Gm::STAGE_BYTES) > 16 ? 16 : (RING_TARGET / Gm::STAGE_BYTES);
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
-    static constexpr int NT = BS / 8;                       // 8-token n-tiles of S^T
-    static constexpr int KT = BS / 16;                      // 16-token k-steps of PV
-    static constexpr int KD = D / 16;                       // 16-dim k-steps of QK / m-tiles of PV
-    static constexpr int OSTRIDE = D + 4;                   // padded scratch row (bank spread)
-    static constexpr int PSTRIDE = D + 2;                   // partial row: o[D], m, l
+    static constexpr int OSTRIDE = D_ + 4;                  // padded scratch row (bank spread)
+    static constexpr int PSTRIDE = D_ + 2;                  // state row: o[D], m, l
     // shared memory carve-up, offsets from a 1024-byte aligned base
     static constexpr int RING_OFF = 0;
-    static constexpr int SO_OFF = STAGES * STAGE_BYTES;
+    static constexpr int SO_OFF = STAGES * Gm::STAGE_BYTES;
     static constexpr int SO_BYTES = NC * G * OSTRIDE * 4;
     static constexpr int SM_OFF = SO_OFF + SO_BYTES;        // m per (warp, head)
     static constexpr int SL_OFF = SM_OFF + NC * G * 4;      // l per (warp, head)
@@ -92,8 +85,6 @@ struct DecodeTraits {
     static constexpr int INFO_OFF = BAR_OFF + 2 * STAGES * 8;
     static constexpr int INFO_BYTES = 64;
     static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;  // + alignment slack
-    static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
     static_assert(STAGES >= 2 && STAGES % NC == 0, "ring stages are owned by consumer warps");
 };
@@ -106,23 +97,32 @@ struct CtaInfo {
     int last;
 };
 
-__device__ __forceinline__ int seq_blocks(int ctx, int BS, int MB) {
-    return (ctx > 0 && ctx <= MB * BS) ? (ctx + BS - 1) / BS : 0;
+// First block of sequence s read here: past its group's shared prefix, 0
+// outside every group.
+__device__ __forceinline__ int first_block_of(const DecodeParams& p, int s) {
+    if (p.n_groups == 0 || s < __ldg(p.grp_starts)) return 0;
+    int lo = 0, hi = p.n_groups;   // largest gi < n_groups with starts[gi] <= s
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.grp_starts + mid) <= s) lo = mid; else hi = mid;
+    }
+    // the same validity rule as the prefix kernel's: a malformed group has no prefix
+    const int s0 = __ldg(p.grp_starts + lo), s1 = __ldg(p.grp_starts + lo + 1);
+    const int pb = __ldg(p.grp_prefix + lo);
+    return (s0 >= 0 && s < s1 && s1 <= p.N && pb >= 0 && pb <= p.MB) ? pb : 0;
 }
 
-// Largest CTA index c with floor(c * W / G) <= x.
-__device__ __forceinline__ long long cta_of(long long x, long long W, long long G) {
-    return ((x + 1) * G + W - 1) / W - 1;
-}
-
-__device__ __forceinline__ long long range_lo(long long c, long long W, long long G) {
-    return c * W / G;
+// Blocks of sequence s in this kernel's work list (and its first block).
+__device__ __forceinline__ int pair_blocks(const DecodeParams& p, int s, int BS, int& first) {
+    first = first_block_of(p, s);
+    const int nb = seq_blocks(__ldg(p.context_lens + s), BS, p.MB) - first;
+    return nb > 0 ? nb : 0;
 }
 
 // Position inside the flattened block list, advanced segment by segment.
 struct SegIter {
     long long gi;  // flattened index of the next block
-    int s, kvh, b0, nb;
+    int s, kvh, b0, nb, first;
 };
 
 __device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodeParams& p, int BS) {
@@ -132,35 +132,14 @@ __device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodePa
         it.b0 = 0;
         if (++it.kvh == p.Hkv) {
             it.kvh = 0;
-            int nb = 0;
+            int nb = 0, first = 0;
             while (++it.s < p.N) {
-                nb = seq_blocks(__ldg(p.context_lens + it.s), BS, p.MB);
+                nb = pair_blocks(p, it.s, BS, first);
                 if (nb > 0) break;
             }
             it.nb = nb;
+            it.first = first;
         }
-    }
-}
-
-template <class Tr>
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)((chunk >> 3) * Tr::BOX_BYTES + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void set_err(uint32_t* err, uint32_t bit) {
-    if (err) atomicOr(err, bit);
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint16_t f32_to_16(float x) {
-    if constexpr (BF16) {
-        uint16_t r;
-        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
-        return r;
-    } else {
-        uint16_t r;
-        asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(x));
-        return r;
     }
 }
 
@@ -168,6 +147,7 @@ template <class Tr>
 __global__ void __launch_bounds__(Tr::THREADS, 2)
 pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const DecodeParams p) {
+    using Gm = typename Tr::Gm;
     constexpr int D = Tr::D, BS = Tr::BS, G = Tr::G, NC = Tr::NC, S = Tr::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,7 +180,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // ---- work range of this CTA (warp 0) ----
     if (warp == 0) {
         long long w = 0;
-        for (int s = lane; s < p.N; s += 32) w += seq_blocks(__ldg(p.context_lens + s), BS, p.MB);
+        int first = 0;
+        for (int s = lane; s < p.N; s += 32) w += pair_blocks(p, s, BS, first);
         for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
         const long long W = w * p.Hkv;
         const long long geff = W < (long long)gridDim.x ? W : (long long)gridDim.x;
@@ -212,7 +193,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             long long base = 0;
             for (int sb = 0; sb < p.N; sb += 32) {
                 const int s = sb + lane;
-                const long long v = s < p.N ? (long long)seq_blocks(__ldg(p.context_lens + s), BS, p.MB) * p.Hkv : 0;
+                const long long v = s < p.N ? (long long)pair_blocks(p, s, BS, first) * p.Hkv : 0;
                 long long incl = v;
                 for (int o = 1; o < 32; o <<= 1) {
                     const long long t = __shfl_up_sync(0xffffffffu, incl, o);
@@ -221,10 +202,10 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 const long long total = __shfl_sync(0xffffffffu, incl, 31);
                 if (base + total > lo) {
                     const unsigned m = __ballot_sync(0xffffffffu, base + incl > lo);
-                    const int first = __ffs(m) - 1;
-                    const long long before = base + __shfl_sync(0xffffffffu, incl - v, first);
-                    s0 = sb + first;
-                    const int nb = seq_blocks(__ldg(p.context_lens + s0), BS, p.MB);
+                    const int firstlane = __ffs(m) - 1;
+                    const long long before = base + __shfl_sync(0xffffffffu, incl - v, firstlane);
+                    s0 = sb + firstlane;
+                    const int nb = pair_blocks(p, s0, BS, first);
                     const long long off = lo - before;
                     kvh0 = (int)(off / nb);
                     b0 = (int)(off % nb);
@@ -246,16 +227,26 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
     }
 
-    // ---- rows of sequences with no blocks: zero (ctx == 0) or NaN (bad ctx) ----
+    // ---- rows of sequences with no blocks here: zero (ctx == 0), the prefix
+    //      state alone (every key in a shared prefix), NaN (bad ctx) ----
     if (warp < NC) {
         for (int s = blockIdx.x; s < p.N; s += gridDim.x) {
             const int ctx = __ldg(p.context_lens + s);
-            if (ctx > 0 && ctx <= p.MB * BS) continue;
-            const bool bad = ctx != 0;
+            int first = 0;
+            if (pair_blocks(p, s, BS, first) > 0) continue;
+            const bool bad = ctx < 0 || ctx > p.MB * BS;
             if (bad && threadIdx.x == 0) set_err(p.err, PA_DEVERR_CONTEXT);
-            const uint16_t v = bad ? (Tr::BF16 ? (uint16_t)0x7fc0 : (uint16_t)0x7e00) : (uint16_t)0;
             uint16_t* row = p.out + (size_t)s * p.Hq * D;
-            for (int i = threadIdx.x; i < p.Hq * D; i += NC * 32) row[i] = v;
+            for (int i = threadIdx.x; i < p.Hq * D; i += NC * 32) {
+                uint16_t v = 0;
+                if (bad) {
+                    v = qnan16<Tr::BF16>();
+                } else if (first > 0 && ctx > 0) {
+                    const float* c = p.carry + ((size_t)s * p.Hq + i / D) * Tr::PSTRIDE;
+                    v = f32_to_16<Tr::BF16>(__ldg(c + i % D) / __ldg(c + D + 1));
+                }
+                row[i] = v;
+            }
         }
     }
     __syncthreads();
@@ -268,7 +259,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     it0.s = info->s0;
     it0.kvh = info->kvh0;
     it0.b0 = info->b0;
-    it0.nb = seq_blocks(__ldg(p.context_lens + it0.s), BS, p.MB);
+    it0.nb = pair_blocks(p, it0.s, BS, it0.first);
 
     if (warp == NC) {
         // =========================== producer ===========================
@@ -277,7 +268,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         SegIter it = it0;
         while (it.gi < hi && !aborted) {
             const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
-            const int32_t* trow = p.block_tables + (size_t)it.s * p.MB + it.b0;
+            const int32_t* trow = p.block_tables + (size_t)it.s * p.MB + it.first + it.b0;
             int tcur = lane < len ? __ldg(trow + lane) : 0;
             for (int base = 0; base < len && !aborted; base += 32) {
                 const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
@@ -299,13 +290,13 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                             }
                             stage_poison[st] = bad ? 1 : 0;
                             const uint32_t fb = full0 + 8 * st;
-                            mbar_arrive_expect_tx(fb, Tr::STAGE_BYTES);
+                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
                             const int y = (id * p.Hkv + it.kvh) * BS;
-                            const uint32_t kdst = ring_u32 + st * Tr::STAGE_BYTES;
+                            const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
 #pragma unroll
-                            for (int h = 0; h < Tr::HALVES; ++h) {
-                                tma_load_2d(kdst + h * Tr::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                                tma_load_2d(kdst + Tr::CHUNK_BYTES + h * Tr::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                            for (int h = 0; h < Gm::HALVES; ++h) {
+                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
                             }
                         } else {
                             set_err(p.err, PA_DEVERR_TIMEOUT);
@@ -340,40 +331,16 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int g = lane >> 2;       // fragment row group
     const int t4 = lane & 3;       // fragment column pair
     SegIter it = it0;
+    WarpAcc<D, Tr::NR> acc;
     while (it.gi < hi) {
         const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
         const int ctx = __ldg(p.context_lens + it.s);
 
         // Q fragments (A operand of S^T = Q K^T): rows = heads of the group.
         const uint16_t* qrow = p.q + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
-        uint32_t qa[Tr::KD][4];
-#pragma unroll
-        for (int kk = 0; kk < Tr::KD; ++kk) {
-            const int c = kk * 16 + 2 * t4;
-            qa[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + g * D + c)) : 0u;
-            qa[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + g * D + c + 8)) : 0u;
-            if constexpr (G > 8) {
-                qa[kk][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + (g + 8) * D + c));
-                qa[kk][3] = __ldg(reinterpret_cast<const uint32_t*>(qrow + (g + 8) * D + c + 8));
-            } else {
-                qa[kk][1] = 0u;
-                qa[kk][3] = 0u;
-            }
-        }
-
-        float m_run[Tr::NR], l_run[Tr::NR];
-        float o[Tr::KD][Tr::NR][4];
-#pragma unroll
-        for (int r = 0; r < Tr::NR; ++r) {
-            m_run[r] = -INFINITY;
-            l_run[r] = 0.f;
-        }
-#pragma unroll
-        for (int mt = 0; mt < Tr::KD; ++mt)
-#pragma unroll
-            for (int r = 0; r < Tr::NR; ++r)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[mt][r][e] = 0.f;
+        uint32_t qa[Gm::KD][4];
+        load_q_frags<D>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
+        acc.reset();
         int poisoned = 0;
 
         // Block k of the CTA range (k = gi - lo) goes to warp k % NC.  With
@@ -398,121 +365,14 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 continue;
             }
             poisoned |= stage_poison[st];
-            const int valid = min(BS, ctx - (it.b0 + j) * BS);
-            const uint32_t kb = ring_u32 + st * Tr::STAGE_BYTES;
-            const uint32_t vb = kb + Tr::CHUNK_BYTES;
-
-            // ---- S^T = Q K^T : [16 heads x BS tokens] ----
-            float sacc[Tr::NT][4];
-#pragma unroll
-            for (int nt = 0; nt < Tr::NT; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-#pragma unroll
-                for (int q4 = 0; q4 < Tr::KD / 2; ++q4) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + swz<Tr>(nt * 8 + (lane & 7), q4 * 4 + (lane >> 3)), b0, b1, b2, b3);
-                    mma16816<Tr::BF16>(sacc[nt], qa[2 * q4][0], qa[2 * q4][1], qa[2 * q4][2], qa[2 * q4][3], b0, b1);
-                    mma16816<Tr::BF16>(sacc[nt], qa[2 * q4 + 1][0], qa[2 * q4 + 1][1], qa[2 * q4 + 1][2],
-                                       qa[2 * q4 + 1][3], b2, b3);
-                }
-            }
-
-            // ---- scale, mask tokens past the context, online softmax ----
-            float mx[Tr::NR];
-#pragma unroll
-            for (int r = 0; r < Tr::NR; ++r) mx[r] = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < Tr::NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = nt * 8 + 2 * t4 + (e & 1);
-                    const float v = tok < valid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
-                    sacc[nt][e] = v;
-                    if ((e >> 1) < Tr::NR) mx[e >> 1] = fmaxf(mx[e >> 1], v);
-                }
-            float alpha[Tr::NR];
-#pragma unroll
-            for (int r = 0; r < Tr::NR; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float m_new = fmaxf(m_run[r], mx[r]);
-                alpha[r] = ex2(m_run[r] - m_new);
-                m_run[r] = m_new;
-                l_run[r] *= alpha[r];
-            }
-#pragma unroll
-            for (int nt = 0; nt < Tr::NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = e >> 1;
-                    if (r < Tr::NR) {
-                        const float pe = ex2(sacc[nt][e] - m_run[r]);
-                        sacc[nt][e] = pe;
-                        l_run[r] += pe;
-                    }
-                }
-            // P^T fragments (B operand of O^T += V^T P^T): k = tokens, n = heads.
-            // P is carried as hi + lo, two 16-bit parts (hi = round(p),
-            // lo = round(p - hi)), so the product keeps ~16 bits of p instead
-            // of the 8 a single bf16 would leave.
-            uint32_t pb[Tr::KT][Tr::NR][2], pl[Tr::KT][Tr::NR][2];
-#pragma unroll
-            for (int kt = 0; kt < Tr::KT; ++kt)
-#pragma unroll
-                for (int r = 0; r < Tr::NR; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const float x0 = sacc[2 * kt + h][2 * r], x1 = sacc[2 * kt + h][2 * r + 1];
-                        const uint32_t hi = pack2<Tr::BF16>(x0, x1);
-                        pb[kt][r][h] = hi;
-                        pl[kt][r][h] = pack2<Tr::BF16>(x0 - lo_of<Tr::BF16>(hi), x1 - hi_of<Tr::BF16>(hi));
-                    }
-
-            // Rows past the context in a partly filled block may hold anything
-            // (even NaN); zero them so 0 * V stays 0 in the PV product.
+            const int valid = min(BS, ctx - (it.first + it.b0 + j) * BS);
+            const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
+            const uint32_t vb = kb + Gm::CHUNK_BYTES;
             if (valid < BS) {
-                const int nz = (BS - valid) * Tr::HALVES * 8;   // 16-byte pieces
-                for (int i = lane; i < nz; i += 32) {
-                    const int piece = i & 7;
-                    const int rest = i >> 3;
-                    const int h = rest % Tr::HALVES;
-                    const int row = valid + rest / Tr::HALVES;
-                    const uint32_t a = vb + h * Tr::BOX_BYTES + row * 128 + piece * 16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(a), "r"(0) : "memory");
-                }
+                zero_v_tail<Gm>(vb, valid, lane);
                 __syncwarp();
             }
-
-            // ---- rescale the running O^T by exp2(m_old - m_new) per head ----
-#pragma unroll
-            for (int r = 0; r < Tr::NR; ++r) {
-                const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
-                const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
-#pragma unroll
-                for (int mt = 0; mt < Tr::KD; ++mt) {
-                    o[mt][r][0] *= aa;
-                    o[mt][r][1] *= ab;
-                    o[mt][r][2] *= aa;
-                    o[mt][r][3] *= ab;
-                }
-            }
-
-            // ---- O^T[d x heads] += V^T[d x tokens] P^T[tokens x heads] ----
-#pragma unroll
-            for (int mt = 0; mt < Tr::KD; ++mt)
-#pragma unroll
-                for (int kt = 0; kt < Tr::KT; ++kt) {
-                    uint32_t a0, a1, a2, a3;
-                    const int row = kt * 16 + ((lane >> 4) << 3) + (lane & 7);
-                    const int chunk = 2 * mt + ((lane >> 3) & 1);
-                    ldsm_x4_t(vb + swz<Tr>(row, chunk), a0, a1, a2, a3);
-#pragma unroll
-                    for (int r = 0; r < Tr::NR; ++r) {
-                        mma16816<Tr::BF16>(o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
-                        mma16816<Tr::BF16>(o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
-                    }
-                }
+            consume_block<Gm, Tr::NR, Tr::BF16>(kb, vb, valid, qa, acc, p.scale_log2, lane);
             if (valid < BS) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -521,28 +381,28 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // ---- merge the NC warp states of this segment ----
 #pragma unroll
         for (int r = 0; r < Tr::NR; ++r) {
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-            l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
+            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
         }
         {
             float* mine = so + warp * G * Tr::OSTRIDE;
 #pragma unroll
-            for (int mt = 0; mt < Tr::KD; ++mt)
+            for (int mt = 0; mt < Gm::KD; ++mt)
 #pragma unroll
                 for (int r = 0; r < Tr::NR; ++r)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int head = 8 * r + 2 * t4 + (e & 1);
                         const int dim = 16 * mt + g + 8 * (e >> 1);
-                        if (head < G) mine[head * Tr::OSTRIDE + dim] = o[mt][r][e];
+                        if (head < G) mine[head * Tr::OSTRIDE + dim] = acc.o[mt][r][e];
                     }
             if (t4 == 0) {
 #pragma unroll
                 for (int r = 0; r < Tr::NR; ++r) {
                     const int head = g + 8 * r;
                     if (head < G) {
-                        sm[warp * G + head] = m_run[r];
-                        sl[warp * G + head] = l_run[r];
+                        sm[warp * G + head] = acc.m[r];
+                        sl[warp * G + head] = acc.l[r];
                     }
                 }
             }
@@ -555,11 +415,13 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const long long clast = cta_of(P0 + it.nb - 1, W, geff);
         const bool complete = cfirst == clast;
         const int slot = (it.gi == lo) ? 0 : 1;
+        const bool has_carry = it.first > 0;
         int bad = 0;
 #pragma unroll
         for (int w = 0; w < NC; ++w) bad |= spois[w];
         const float qnan = __int_as_float(0x7fc00000);
         uint16_t* orow = p.out + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
+        const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::PSTRIDE;
         float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * G * Tr::PSTRIDE;
         for (int idx = tid; idx < G * D; idx += NC * 32) {
             const int head = idx / D;
@@ -576,6 +438,10 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             if (bad) O = qnan;
             if (complete) {
+                if (has_carry) {
+                    const float* c = crow + head * Tr::PSTRIDE;
+                    lse_fold(M, L, O, __ldg(c + D), __ldg(c + D + 1), __ldg(c + dim));
+                }
                 orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L);
             } else {
                 prow[head * Tr::PSTRIDE + dim] = O;
@@ -605,14 +471,11 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     for (long long c = cfirst; c <= clast; ++c) {
                         const int sl_c = (c == cfirst && range_lo(c, W, geff) < P0) ? 1 : 0;
                         const float* pr = p.partials + ((size_t)c * 2 + sl_c) * G * Tr::PSTRIDE + head * Tr::PSTRIDE;
-                        const float mc = __ldcg(pr + D);
-                        const float lc = __ldcg(pr + D + 1);
-                        const float oc = __ldcg(pr + dim);
-                        const float Mn = fmaxf(M, mc);
-                        const float fa = ex2(M - Mn), fb = ex2(mc - Mn);
-                        L = L * fa + lc * fb;
-                        O = O * fa + oc * fb;
-                        M = Mn;
+                        lse_fold(M, L, O, __ldcg(pr + D), __ldcg(pr + D + 1), __ldcg(pr + dim));
+                    }
+                    if (has_carry) {
+                        const float* cr = crow + head * Tr::PSTRIDE;
+                        lse_fold(M, L, O, __ldg(cr + D), __ldg(cr + D + 1), __ldg(cr + dim));
                     }
                     orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L);
                 }
@@ -646,29 +509,9 @@ cudaError_t decode_launch(const DecodeLaunch& L) {
 }
 
 template <class Tr>
-int decode_max_ctas(int device) {
-    static int cached[64] = {0};
-    if (device < 0 || device >= 64) return -1;
-    if (cached[device] > 0) return cached[device];
-    int prev = 0;
-    if (cudaGetDevice(&prev) != cudaSuccess) return -1;
-    if (prev != device && cudaSetDevice(device) != cudaSuccess) return -1;
-    int sms = 0, per_sm = 0;
-    cudaError_t e = cudaFuncSetAttribute(pa_decode_kernel<Tr>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Tr::SMEM_BYTES);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_kernel<Tr>, Tr::THREADS,
-                                                          Tr::SMEM_BYTES);
-    if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess || per_sm <= 0) return -1;
-    cached[device] = sms * per_sm;
-    return cached[device];
-}
-
-template <class Tr>
 DecodeKernelInfo decode_info() {
-    return DecodeKernelInfo{&decode_launch<Tr>, &decode_max_ctas<Tr>, Tr::SMEM_BYTES, Tr::STAGES};
+    return DecodeKernelInfo{&decode_launch<Tr>, &persistent_ctas<pa_decode_kernel<Tr>, Tr::THREADS, Tr::SMEM_BYTES>,
+                            Tr::SMEM_BYTES, Tr::STAGES};
 }
 
 // Per-(dtype, head_dim) tables, defined in the instantiation units.

@@ -10,6 +10,7 @@
 #include "../../include/pa.h"
 #include "decode_kernel.cuh"
 #include "kv_ops.cuh"
+#include "prefix_kernel.cuh"
 
 namespace {
 
@@ -122,6 +123,31 @@ int current_sms() {
     return sms;
 }
 
+
+const PrefixKernelInfo& pick_prefix(const pa_shape* s) {
+    static const auto tab = [] {
+        struct T { PrefixKernelInfo t[2][2][2]; } x;
+        prefix_table(x.t);
+        return x;
+    }();
+    return tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of prefix-aware decode: decode counters, prefix counters, carry
+// states, decode partials, prefix partials (offsets in off[0..4]).
+size_t shared_prefix_layout(const pa_shape* s, int dec_ctas, int pre_ctas, size_t (&off)[5]) {
+    const size_t cb = counters_bytes(s);
+    off[0] = 0;
+    off[1] = cb;
+    off[2] = 2 * cb;
+    const size_t carry = align256((size_t)s->num_seqs * s->num_q_heads * (s->head_dim + 2) * sizeof(float));
+    off[3] = off[2] + carry;
+    off[4] = off[3] + align256(partials_bytes(s, dec_ctas));
+    return off[4] + (size_t)pre_ctas * 2 * 32 * (s->head_dim + 2) * sizeof(float);
+}
+
 }  // namespace
 
 extern "C" {
@@ -158,7 +184,7 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     CUtensorMap mk, mv;
     if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
 
-    DecodeLaunch L;
+    DecodeLaunch L{};
     L.tmap_k = &mk;
     L.tmap_v = &mv;
     L.p.q = static_cast<const uint16_t*>(q);
@@ -180,6 +206,104 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     // Arrival counters start at zero for every call (the region may hold
     // another shape's partial states from an earlier call).
     if (cudaMemsetAsync(workspace, 0, counters_bytes(shape), L.stream) != cudaSuccess) return PA_ERR_CUDA;
+    return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape) {
+    const DecodeKernelInfo* k = nullptr;
+    if (pick_decode(shape, &k) != PA_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int dec = k->max_ctas(dev), pre = pick_prefix(shape).max_ctas(dev);
+    if (dec <= 0 || pre <= 0) return 0;
+    size_t off[5];
+    return shared_prefix_layout(shape, dec, pre, off);
+}
+
+pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_tables, const int32_t* context_lens, int32_t num_groups,
+                                  const int32_t* group_starts, const int32_t* group_prefix_blocks, float scale,
+                                  void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                                  void* stream) {
+    const DecodeKernelInfo* k = nullptr;
+    pa_status st = pick_decode(shape, &k);
+    if (st != PA_OK) return st;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || num_groups < 0) return PA_ERR_INVALID_ARG;
+    if (num_groups > 0 && (!group_starts || !group_prefix_blocks || !aligned(group_starts, 4) ||
+                           !aligned(group_prefix_blocks, 4)))
+        return PA_ERR_INVALID_ARG;
+    if (shape->num_seqs == 0) return PA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    const PrefixKernelInfo& pk = pick_prefix(shape);
+    const int dec = k->max_ctas(dev), pre = pk.max_ctas(dev);
+    if (dec <= 0 || pre <= 0) return PA_ERR_CUDA;
+    size_t off[5];
+    const size_t need = shared_prefix_layout(shape, dec, pre, off);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+
+    CUtensorMap mk, mv;
+    if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    const float scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
+    // both arrival-counter regions start at zero for every call
+    if (cudaMemsetAsync(ws, 0, off[2], strm) != cudaSuccess) return PA_ERR_CUDA;
+
+    if (num_groups > 0) {
+        PrefixLaunch P{};
+        P.tmap_k = &mk;
+        P.tmap_v = &mv;
+        P.p.q = static_cast<const uint16_t*>(q);
+        P.p.block_tables = block_tables;
+        P.p.context_lens = context_lens;
+        P.p.grp_starts = group_starts;
+        P.p.grp_prefix = group_prefix_blocks;
+        P.p.carry = reinterpret_cast<float*>(ws + off[2]);
+        P.p.counters = reinterpret_cast<int32_t*>(ws + off[1]);
+        P.p.partials = reinterpret_cast<float*>(ws + off[4]);
+        P.p.err = err_word;
+        P.p.n_groups = num_groups;
+        P.p.G = shape->num_q_heads / shape->num_kv_heads;
+        P.p.N = shape->num_seqs;
+        P.p.Hq = shape->num_q_heads;
+        P.p.Hkv = shape->num_kv_heads;
+        P.p.NB = shape->num_blocks;
+        P.p.MB = shape->max_blocks_per_seq;
+        P.p.scale_log2 = scale_log2;
+        P.p.timeout_ns = kTimeoutNs;
+        P.stream = strm;
+        P.grid = pre;
+        if (pk.launch(P) != cudaSuccess) return PA_ERR_CUDA;
+    }
+
+    DecodeLaunch L{};
+    L.tmap_k = &mk;
+    L.tmap_v = &mv;
+    L.p.q = static_cast<const uint16_t*>(q);
+    L.p.block_tables = block_tables;
+    L.p.context_lens = context_lens;
+    L.p.out = static_cast<uint16_t*>(out);
+    L.p.counters = reinterpret_cast<int32_t*>(ws + off[0]);
+    L.p.partials = reinterpret_cast<float*>(ws + off[3]);
+    L.p.err = err_word;
+    L.p.grp_starts = group_starts;
+    L.p.grp_prefix = group_prefix_blocks;
+    L.p.carry = reinterpret_cast<const float*>(ws + off[2]);
+    L.p.n_groups = num_groups;
+    L.p.N = shape->num_seqs;
+    L.p.Hq = shape->num_q_heads;
+    L.p.Hkv = shape->num_kv_heads;
+    L.p.NB = shape->num_blocks;
+    L.p.MB = shape->max_blocks_per_seq;
+    L.p.scale_log2 = scale_log2;
+    L.p.timeout_ns = kTimeoutNs;
+    L.stream = strm;
+    L.grid = dec;
     return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -1,0 +1,454 @@
+// Prefix pass of prefix-aware decode: sequences that share their leading
+// physical blocks (parallel samples of one prompt, requests with a common
+// system prompt -- ontq "AI Inference Serving at Scale", section 3,
+// copy-on-write sharing; letsbuildsolutions, "Production Considerations",
+// prefix caching) read those blocks once for the whole group.
+//
+// Work items are (group, KV head, row chunk): the query rows of a group are
+// its members x g query heads of that KV head, taken 32 at a time.  An item
+// streams the group's shared blocks (through the first member's table) and
+// leaves, for every row, the softmax state (o unnormalised, m, l) of the
+// prefix keys in `carry`; the decode kernel then covers each member's own
+// blocks and folds the carry in.  Items are cut into equal CTA ranges exactly
+// as in the decode kernel, with the same last-arriver merge for items that
+// straddle a range boundary.
+//
+// Inside a CTA the roles differ from the decode kernel: all NC consumer warps
+// read every block of the ring (the empty barrier counts NC arrivals) and
+// warp w owns rows [8w, 8w + 8) of the chunk, so no warp merge is needed.
+// Shared blocks are full, so no masking is needed.  Each piece also checks
+// that every member's table repeats the first member's over the prefix and
+// that every member holds at least the prefix; a violation sets
+// PA_DEVERR_GROUP and poisons the rows with NaN.
+#pragma once
+
+#include "decode_common.cuh"
+
+namespace pa {
+
+struct PrefixParams {
+    const uint16_t* q;            // [N][Hq][D]
+    const int32_t* block_tables;  // [N][MB]
+    const int32_t* context_lens;  // [N]
+    const int32_t* grp_starts;    // [n_groups + 1]
+    const int32_t* grp_prefix;    // [n_groups]
+    float* carry;                 // [N][Hq][D + 2] (o, m, l) out
+    int32_t* counters;            // [N * Hkv], zeroed before each launch
+    float* partials;              // [gridDim.x][2][32][D + 2]
+    uint32_t* err;
+    int32_t n_groups, G;          // G: query heads per KV head
+    int32_t N, Hq, Hkv, NB, MB;
+    float scale_log2;
+    uint64_t timeout_ns;
+};
+
+template <int D_, int BS_, bool BF16_>
+struct PrefixTraits : Geom<D_, BS_> {
+    using Gm = Geom<D_, BS_>;
+    static constexpr bool BF16 = BF16_;
+    static constexpr int NC = 4;
+    static constexpr int RPW = 8;                 // rows per consumer warp
+    static constexpr int RC = NC * RPW;           // rows per item (chunk)
+    static constexpr int THREADS = (NC + 1) * 32;
+    static constexpr int STAGES = (64 * 1024 / Gm::STAGE_BYTES) > 16 ? 16 : (64 * 1024 / Gm::STAGE_BYTES);
+    static constexpr int PSTRIDE = D_ + 2;
+    static constexpr int BAR_OFF = STAGES * Gm::STAGE_BYTES;
+    static constexpr int PS_OFF = BAR_OFF + 2 * STAGES * 8;
+    static constexpr int INFO_OFF = PS_OFF + STAGES * 4;
+    static constexpr int INFO_BYTES = 64;
+    static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;
+    static_assert(STAGES >= 2, "ring");
+};
+
+struct PrefixInfo {
+    long long lo, hi, W, geff;
+    int g0, kvh0, ch0, b0;
+    int abort, last, bad;
+};
+
+// Members [s0, s1) and shared blocks of group gi, clamped to valid ranges;
+// returns false (and an empty group) when the description is malformed.
+__device__ __forceinline__ bool group_of(const PrefixParams& p, int gi, int& s0, int& s1, int& pb) {
+    s0 = __ldg(p.grp_starts + gi);
+    s1 = __ldg(p.grp_starts + gi + 1);
+    pb = __ldg(p.grp_prefix + gi);
+    const bool ok = s0 >= 0 && s1 >= s0 && s1 <= p.N && pb >= 0 && pb <= p.MB;
+    if (!ok) {
+        s0 = s1 = 0;
+        pb = 0;
+    }
+    return ok;
+}
+
+__device__ __forceinline__ int group_chunks(const PrefixParams& p, int s0, int s1, int RC) {
+    return ((s1 - s0) * p.G + RC - 1) / RC;
+}
+
+// Blocks that group gi contributes to the flattened list.
+__device__ __forceinline__ long long group_work(const PrefixParams& p, int gi, int RC) {
+    int s0, s1, pb;
+    group_of(p, gi, s0, s1, pb);
+    return (long long)p.Hkv * group_chunks(p, s0, s1, RC) * pb;
+}
+
+struct ItemIter {
+    long long gi_flat;   // flattened index of the next block
+    int grp, kvh, ch, b0;
+    int s0, s1, pb, nch;
+};
+
+__device__ __forceinline__ void item_load_group(ItemIter& it, const PrefixParams& p, int RC) {
+    while (it.grp < p.n_groups) {
+        group_of(p, it.grp, it.s0, it.s1, it.pb);
+        it.nch = group_chunks(p, it.s0, it.s1, RC);
+        if (it.pb > 0 && it.nch > 0) return;
+        ++it.grp;
+    }
+}
+
+__device__ __forceinline__ void item_advance(ItemIter& it, int len, const PrefixParams& p, int RC) {
+    it.gi_flat += len;
+    it.b0 += len;
+    if (it.b0 == it.pb) {
+        it.b0 = 0;
+        if (++it.ch == it.nch) {
+            it.ch = 0;
+            if (++it.kvh == p.Hkv) {
+                it.kvh = 0;
+                ++it.grp;
+                item_load_group(it, p, RC);
+            }
+        }
+    }
+}
+
+template <class Tr>
+__global__ void __launch_bounds__(Tr::THREADS, 2)
+pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                 const PrefixParams p) {
+    using Gm = typename Tr::Gm;
+    constexpr int D = Tr::D, BS = Tr::BS, NC = Tr::NC, S = Tr::STAGES, RC = Tr::RC;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring_u32 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::BAR_OFF);
+    volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF);
+    PrefixInfo* info = reinterpret_cast<PrefixInfo*>(smem + Tr::INFO_OFF);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + S);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < S; ++st) {
+            mbar_init(full0 + 8 * st, 1);
+            mbar_init(empty0 + 8 * st, NC);
+        }
+        fence_mbar_init();
+    }
+    if (warp == NC && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+
+    // ---- work range of this CTA (warp 0) ----
+    if (warp == 0) {
+        long long w = 0;
+        bool malformed = false;
+        for (int gi = lane; gi < p.n_groups; gi += 32) {
+            int s0, s1, pb;
+            malformed |= !group_of(p, gi, s0, s1, pb);
+            w += (long long)p.Hkv * group_chunks(p, s0, s1, RC) * pb;
+        }
+        if (__any_sync(0xffffffffu, malformed) && blockIdx.x == 0 && lane == 0) set_err(p.err, PA_DEVERR_GROUP);
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        const long long W = w;
+        const long long geff = W < (long long)gridDim.x ? W : (long long)gridDim.x;
+        long long lo = 0, hi = 0;
+        int g0 = 0, kvh0 = 0, ch0 = 0, b0 = 0;
+        if ((long long)blockIdx.x < geff) {
+            lo = range_lo(blockIdx.x, W, geff);
+            hi = range_lo(blockIdx.x + 1, W, geff);
+            long long base = 0;
+            for (int gb = 0; gb < p.n_groups; gb += 32) {
+                const int gi = gb + lane;
+                const long long v = gi < p.n_groups ? group_work(p, gi, RC) : 0;
+                long long incl = v;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const long long total = __shfl_sync(0xffffffffu, incl, 31);
+                if (base + total > lo) {
+                    const unsigned m = __ballot_sync(0xffffffffu, base + incl > lo);
+                    const int fl = __ffs(m) - 1;
+                    const long long before = base + __shfl_sync(0xffffffffu, incl - v, fl);
+                    g0 = gb + fl;
+                    int s0, s1, pb;
+                    group_of(p, g0, s0, s1, pb);
+                    const int nch = group_chunks(p, s0, s1, RC);
+                    const long long off = lo - before;           // < Hkv * nch * pb
+                    const long long item = off / pb;
+                    b0 = (int)(off % pb);
+                    kvh0 = (int)(item / nch);
+                    ch0 = (int)(item % nch);
+                    break;
+                }
+                base += total;
+            }
+        }
+        if (lane == 0) {
+            info->lo = lo;
+            info->hi = hi;
+            info->W = W;
+            info->geff = geff;
+            info->g0 = g0;
+            info->kvh0 = kvh0;
+            info->ch0 = ch0;
+            info->b0 = b0;
+            info->abort = 0;
+            info->last = 0;
+            info->bad = 0;
+        }
+    }
+    __syncthreads();
+    const long long lo = info->lo, hi = info->hi, W = info->W, geff = info->geff;
+    if ((long long)blockIdx.x >= geff) return;
+
+    ItemIter it0;
+    it0.gi_flat = lo;
+    it0.grp = info->g0;
+    it0.kvh = info->kvh0;
+    it0.ch = info->ch0;
+    it0.b0 = info->b0;
+    group_of(p, it0.grp, it0.s0, it0.s1, it0.pb);
+    it0.nch = group_chunks(p, it0.s0, it0.s1, RC);
+
+    if (warp == NC) {
+        // =========================== producer ===========================
+        long long issued = 0;
+        bool aborted = false;
+        ItemIter it = it0;
+        while (it.gi_flat < hi && !aborted) {
+            const int len = (int)min((long long)(it.pb - it.b0), hi - it.gi_flat);
+            const int32_t* trow = p.block_tables + (size_t)it.s0 * p.MB + it.b0;
+            int tcur = lane < len ? __ldg(trow + lane) : 0;
+            for (int base = 0; base < len && !aborted; base += 32) {
+                const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
+                const int cnt = min(32, len - base);
+                for (int i = 0; i < cnt; ++i) {
+                    int id = __shfl_sync(0xffffffffu, tcur, i);
+                    int ok = 1;
+                    if (lane == 0) {
+                        const int st = (int)(issued % S);
+                        if (issued >= S) {
+                            const uint32_t par = (uint32_t)(((issued / S) - 1) & 1);
+                            if (!mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns)) ok = 0;
+                        }
+                        if (ok) {
+                            const bool bad = (unsigned)id >= (unsigned)p.NB;
+                            if (bad) {
+                                set_err(p.err, PA_DEVERR_BLOCK_ID);
+                                id = 0;
+                            }
+                            stage_poison[st] = bad ? 1 : 0;
+                            const uint32_t fb = full0 + 8 * st;
+                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                            const int y = (id * p.Hkv + it.kvh) * BS;
+                            const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
+#pragma unroll
+                            for (int h = 0; h < Gm::HALVES; ++h) {
+                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                            }
+                        } else {
+                            set_err(p.err, PA_DEVERR_TIMEOUT);
+                            *(volatile int*)&info->abort = 1;
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        aborted = true;
+                        break;
+                    }
+                    ++issued;
+                }
+                tcur = nxt;
+            }
+            if (!aborted) item_advance(it, len, p, RC);
+        }
+        if (lane == 0) {
+            const long long nst = issued < S ? issued : S;
+            for (long long st = 0; st < nst; ++st) {
+                const long long klast = st + ((issued - 1 - st) / S) * S;
+                if (!mbar_wait_bounded(full0 + 8 * (uint32_t)st, (uint32_t)((klast / S) & 1), p.timeout_ns))
+                    set_err(p.err, PA_DEVERR_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // ============================ consumers ============================
+    const int tid = threadIdx.x;
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    const float qnan = __int_as_float(0x7fc00000);
+    ItemIter it = it0;
+    WarpAcc<D, 1> acc;
+    while (it.gi_flat < hi) {
+        const int len = (int)min((long long)(it.pb - it.b0), hi - it.gi_flat);
+        const int R = (it.s1 - it.s0) * p.G;                 // rows of the group for this KV head
+        const int rbase = it.ch * RC + warp * Tr::RPW;       // first row of this warp
+        // Q fragments: fragment row g -> row rbase + g of the chunk.
+        const int r0 = rbase + g;
+        const uint16_t* q0 = r0 < R ? p.q + ((size_t)(it.s0 + r0 / p.G) * p.Hq + (size_t)it.kvh * p.G + r0 % p.G) * D
+                                    : nullptr;
+        uint32_t qa[Gm::KD][4];
+        load_q_frags<D>(qa, q0, nullptr, t4);
+        acc.reset();
+        int poisoned = 0;
+
+        for (int j = 0; j < len; ++j) {
+            const long long k = it.gi_flat + j - lo;
+            const int st = (int)(k % S);
+            const uint32_t par = (uint32_t)((k / S) & 1);
+            if (*(volatile int*)&info->abort) {
+                poisoned = 1;
+                continue;
+            }
+            if (!mbar_wait_bounded(full0 + 8 * st, par, p.timeout_ns)) {
+                if (lane == 0) {
+                    set_err(p.err, PA_DEVERR_TIMEOUT);
+                    *(volatile int*)&info->abort = 1;
+                }
+                poisoned = 1;
+                continue;
+            }
+            poisoned |= stage_poison[st];
+            const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
+            consume_block<Gm, 1, Tr::BF16>(kb, kb + Gm::CHUNK_BYTES, BS, qa, acc, p.scale_log2, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        }
+
+        // ---- the group must really share these blocks ----
+        {
+            const int members = it.s1 - it.s0;
+            const int32_t* first_row = p.block_tables + (size_t)it.s0 * p.MB;
+            int bad = 0;
+            for (int e = tid; e < members * it.pb; e += NC * 32) {
+                const int m = e / it.pb, i = e - m * it.pb;
+                const int s = it.s0 + m;
+                if (i == 0 && __ldg(p.context_lens + s) < it.pb * BS) bad = 1;
+                if (__ldg(p.block_tables + (size_t)s * p.MB + i) != __ldg(first_row + i)) bad = 1;
+            }
+            if (bad) atomicOr(&info->bad, 1);
+        }
+        acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 1);
+        acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 2);
+        named_bar_sync(1, NC * 32);
+        const bool group_bad = *(volatile int*)&info->bad != 0;
+        poisoned |= group_bad;
+        if (group_bad && tid == 0) set_err(p.err, PA_DEVERR_GROUP);
+
+        const long long P0 = it.gi_flat - it.b0;
+        const long long cfirst = cta_of(P0, W, geff);
+        const long long clast = cta_of(P0 + it.pb - 1, W, geff);
+        const bool complete = cfirst == clast;
+        const int slot = (it.gi_flat == lo) ? 0 : 1;
+        // This lane's O^T fragments: c0,c1 -> rows 2*t4, 2*t4+1 (of the warp's 8),
+        // dims 16*mt + g (+8 for c2, c3); m and l of row g sit in lane 4g.
+        if (complete) {
+#pragma unroll
+            for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = rbase + 2 * t4 + (e & 1);
+                    if (r < R) {
+                        float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) *
+                                                 Tr::PSTRIDE;
+                        c[16 * mt + g + 8 * (e >> 1)] = poisoned ? qnan : acc.o[mt][0][e];
+                    }
+                }
+            if (t4 == 0 && rbase + g < R) {
+                const int r = rbase + g;
+                float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) * Tr::PSTRIDE;
+                c[D] = acc.m[0];
+                c[D + 1] = acc.l[0];
+            }
+        } else {
+            float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * RC * Tr::PSTRIDE;
+#pragma unroll
+            for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = warp * Tr::RPW + 2 * t4 + (e & 1);
+                    prow[rr * Tr::PSTRIDE + 16 * mt + g + 8 * (e >> 1)] = poisoned ? qnan : acc.o[mt][0][e];
+                }
+            if (t4 == 0) {
+                const int rr = warp * Tr::RPW + g;
+                prow[rr * Tr::PSTRIDE + D] = acc.m[0];
+                prow[rr * Tr::PSTRIDE + D + 1] = acc.l[0];
+            }
+            __threadfence();
+            named_bar_sync(1, NC * 32);
+            const int cid = (it.s0 + it.ch * (RC / p.G)) * p.Hkv + it.kvh;
+            if (tid == 0) {
+                const int prev = atomicAdd(p.counters + cid, 1);
+                *(volatile int*)&info->last = (prev == (int)(clast - cfirst)) ? 1 : 0;
+            }
+            named_bar_sync(1, NC * 32);
+            if (*(volatile int*)&info->last) {
+                __threadfence();
+                const int rows = min(RC, R - it.ch * RC);
+                for (int idx = tid; idx < rows * (D + 2); idx += NC * 32) {
+                    const int rr = idx / (D + 2);
+                    const int col = idx - rr * (D + 2);
+                    float M = -INFINITY, L = 0.f, O = 0.f;
+                    for (long long c = cfirst; c <= clast; ++c) {
+                        const int sl_c = (c == cfirst && range_lo(c, W, geff) < P0) ? 1 : 0;
+                        const float* pr = p.partials + ((size_t)c * 2 + sl_c) * RC * Tr::PSTRIDE + rr * Tr::PSTRIDE;
+                        lse_fold(M, L, O, __ldcg(pr + D), __ldcg(pr + D + 1), col < D ? __ldcg(pr + col) : 0.f);
+                    }
+                    const int r = it.ch * RC + rr;
+                    float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) *
+                                             Tr::PSTRIDE;
+                    c[col] = col < D ? O : (col == D ? M : L);
+                }
+            }
+        }
+        named_bar_sync(1, NC * 32);
+        if (tid == 0) info->bad = 0;
+        named_bar_sync(1, NC * 32);
+        item_advance(it, len, p, RC);
+    }
+}
+
+struct PrefixLaunch {
+    const CUtensorMap* tmap_k;
+    const CUtensorMap* tmap_v;
+    PrefixParams p;
+    cudaStream_t stream;
+    int grid;
+};
+
+struct PrefixKernelInfo {
+    cudaError_t (*launch)(const PrefixLaunch&);
+    int (*max_ctas)(int device);
+};
+
+template <class Tr>
+cudaError_t prefix_launch(const PrefixLaunch& L) {
+    pa_prefix_kernel<Tr><<<L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream>>>(*L.tmap_k, *L.tmap_v, L.p);
+    return cudaGetLastError();
+}
+
+template <class Tr>
+PrefixKernelInfo prefix_info() {
+    return PrefixKernelInfo{&prefix_launch<Tr>, &persistent_ctas<pa_prefix_kernel<Tr>, Tr::THREADS, Tr::SMEM_BYTES>};
+}
+
+// Index: [bf16][d == 128][bs == 32]; defined in prefix_inst.cu.
+void prefix_table(PrefixKernelInfo (&t)[2][2][2]);
+
+}  // namespace pa

@@ -158,3 +158,59 @@ def pa_read_error(err, stream=None) -> int:
     _need_cuda("err", err, torch.int32)
     with torch.cuda.device(err.device):
         return int(_lib.load().pa_read_error(_ptr(err), _stream(err.device, stream)))
+
+
+def pa_decode_shared_prefix(q, k_pool, v_pool, block_tables, context_lens, group_starts, group_prefix_blocks,
+                            scale, out=None, workspace=None, err=None, stream=None):
+    """Prefix-aware decode (see include/pa.h): group_starts [G + 1] and
+    group_prefix_blocks [G] are int32 CUDA tensors describing sequences that
+    share their leading blocks."""
+    _need_cuda("q", q)
+    _need_cuda("k_pool", k_pool, q.dtype)
+    _need_cuda("v_pool", v_pool, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("group_starts", group_starts, torch.int32)
+    _need_cuda("group_prefix_blocks", group_prefix_blocks, torch.int32)
+    n_groups = group_prefix_blocks.shape[0]
+    if group_starts.shape != (n_groups + 1,):
+        raise ValueError("group_starts must have one more entry than group_prefix_blocks")
+    N, Hq, d = q.shape
+    if k_pool.shape != v_pool.shape or k_pool.shape[3] != d or block_tables.shape[0] != N:
+        raise ValueError("shape mismatch between q, pools and block_tables")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+    shape = _pool_shape(k_pool, N, Hq, block_tables.shape[1])
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        need = int(lib.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(shape)))
+        if workspace is None:
+            workspace = _shared_workspace(q.device, need, stream)
+        else:
+            _need_cuda("workspace", workspace)
+        if err is not None:
+            _need_cuda("err", err, torch.int32)
+        st = lib.pa_decode_shared_prefix(ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                         _ptr(block_tables), _ptr(context_lens), ctypes.c_int32(n_groups),
+                                         _ptr(group_starts), _ptr(group_prefix_blocks), ctypes.c_float(scale),
+                                         _ptr(out), _ptr(workspace),
+                                         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(err),
+                                         _stream(q.device, stream))
+    _lib.check(st, "pa_decode_shared_prefix")
+    return out
+
+
+_sp_cache = {}
+
+
+def _shared_workspace(device, need, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (device.index, s.cuda_stream)
+    with _ws_lock:
+        ws = _sp_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=device)
+            _sp_cache[key] = ws
+        return ws

@@ -140,3 +140,34 @@ def test_parallel_sampling_flow_matches_reference_at_full_size():
         rows = [bm.table((g, j)) for j in range(cfg.samples)]
         assert all(r[:63] == rows[0][:63] for r in rows)            # 63 full prompt blocks shared
         assert len({r[63] for r in rows}) == cfg.samples               # the half-full one: 7 copies + original
+
+
+def test_shared_prefix_groups_found_from_forks():
+    from oracle.attention import check_prefix_groups
+    B = 4
+    bm = BlockManager(200, B, seed=2)
+    bm.add_sequence("solo", 9)
+    bm.add_sequence("p", 10)                       # 2 full blocks + 2 tokens
+    for c in ("c1", "c2"):
+        bm.fork("p", c)
+    bm.append_slots([("p", 3), ("c1", 1), ("c2", 6)])   # each diverges in block 2
+    bm.add_sequence("q", 8)                        # exactly 2 full blocks
+    bm.fork("q", "q1")
+    bm.append_slots([("q1", 1)])
+    bm.add_sequence("tail", 3)
+    seqs = ["solo", "p", "c1", "c2", "q", "q1", "tail"]
+    starts, prefix = bm.shared_prefix_groups(seqs)
+    assert starts.tolist() == [1, 4, 6] and prefix.tolist() == [2, 2]
+    tables = bm.block_tables(seqs, 8)
+    assert check_prefix_groups(tables, bm.context_lens(seqs), starts, prefix, B)
+    assert bm.shared_prefix_groups(["solo", "tail"])[1].size == 0
+
+
+def test_shared_prefix_groups_fill_gaps():
+    bm = BlockManager(100, 4, seed=3)
+    for name in ("a", "x", "b"):
+        bm.add_sequence(name, 8)
+    bm.fork("a", "a2")
+    bm.fork("b", "b2")
+    starts, prefix = bm.shared_prefix_groups(["a", "a2", "x", "b", "b2"])
+    assert starts.tolist() == [0, 2, 3, 5] and prefix.tolist() == [2, 0, 2]

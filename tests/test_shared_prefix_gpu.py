@@ -1,0 +1,155 @@
+"""Prefix-aware decode (pa_decode_shared_prefix) against the oracle and
+against plain pa_decode, on small shapes with edge cases and on the full
+parallel-sampling workload."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import decode_ref, decode_shared_prefix_ref
+from oracle.kv_ops import append_ref, bits, copy_ref, slot_of
+from tests.gpu_util import ATOL, RTOL, assert_close, from_bits, need_gpu
+from workloads import SAMPLING, make_sampling_case, make_values, sampling_tables
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def pa():
+    import paged_kv_cache_254_gb300 as m
+    return m
+
+
+def grouped_case(seed, groups, Hq, Hkv, d, B, dtype, solo=(13, 1)):
+    """groups: list of (members, shared full blocks, tail lengths or None).
+    Members share the group's leading blocks, then own blocks.  `solo`
+    sequences follow, outside every group."""
+    r = np.random.Generator(np.random.PCG64(seed))
+    ctx, rows = [], []
+    nb_total = 0
+    starts, prefix = [0], []
+    for members, p, tails in groups:
+        shared = list(range(nb_total, nb_total + p))
+        nb_total += p
+        for m in range(members):
+            t = int(tails[m]) if tails is not None else int(r.integers(0, 3 * B))
+            n = p * B + t
+            own = -(-n // B) - p
+            rows.append(shared + list(range(nb_total, nb_total + own)))
+            nb_total += own
+            ctx.append(n)
+        starts.append(starts[-1] + members)
+        prefix.append(p)
+    for n in solo:
+        k = -(-n // B)
+        rows.append(list(range(nb_total, nb_total + k)))
+        nb_total += k
+        ctx.append(n)
+    NB = nb_total + 7
+    relabel = r.permutation(NB)                     # scatter blocks through the pool
+    MB = max(len(x) for x in rows) + 2
+    tables = np.full((len(rows), MB), -1, dtype=np.int32)
+    for i, x in enumerate(rows):
+        tables[i, :len(x)] = relabel[np.asarray(x, dtype=np.int64)] if x else []
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = make_values((len(rows), Hq, d), dtype, g, "cuda")
+    kp = make_values((NB, Hkv, B, d), dtype, g, "cuda")
+    vp = make_values((NB, Hkv, B, d), dtype, g, "cuda")
+    return q, kp, vp, tables, np.asarray(ctx, dtype=np.int32), np.asarray(starts, np.int32), \
+        np.asarray(prefix, np.int32)
+
+
+def run_sp(q, kp, vp, tables, ctx, starts, prefix, scale, err=None):
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    return pa().pa_decode_shared_prefix(q, kp, vp, c(tables), c(ctx), c(starts), c(prefix), scale, err=err)
+
+
+CASES = [
+    ("bf16", 128, 16, 4, [(8, 5, None), (1, 3, None), (3, 2, [0, 16, 40])]),
+    ("fp16", 64, 32, 8, [(5, 2, None), (2, 4, [0, 1])]),
+    ("bf16", 128, 32, 16, [(4, 3, None)]),
+    ("bf16", 64, 16, 1, [(20, 6, None)]),
+    ("bf16", 128, 16, 8, [(12, 4, None), (6, 1, None)]),   # 96 rows: three row chunks
+]
+
+
+@pytest.mark.parametrize("dtype,d,B,g,groups", CASES)
+def test_matches_oracle_and_plain_decode(dtype, d, B, g, groups):
+    Hkv = 2
+    q, kp, vp, tables, ctx, starts, prefix = grouped_case(d + B + g, groups, Hkv * g, Hkv, d, B, dtype)
+    scale = float(np.float32(d ** -0.5))
+    err = pa().new_error_word("cuda")
+    out = run_sp(q, kp, vp, tables, ctx, starts, prefix, scale, err=err)
+    assert pa().pa_read_error(err) == 0
+    ref = decode_shared_prefix_ref(q, kp, vp, tables, ctx, scale, starts, prefix)
+    assert_close(out, ref, what=f"shared prefix {dtype} d{d} B{B} g{g}")
+    plain = pa().pa_decode(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(), scale)
+    a, b = out.double(), plain.double()
+    assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
+
+
+def test_no_groups_is_plain_decode():
+    q, kp, vp, tables, ctx, _, _ = grouped_case(3, [(3, 2, None)], 8, 2, 128, 16, "bf16")
+    out = run_sp(q, kp, vp, tables, ctx, np.zeros(1, np.int32), np.zeros(0, np.int32), 0.088)
+    plain = pa().pa_decode(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(), 0.088)
+    assert torch.equal(out, plain)
+
+
+def test_member_breaking_the_prefix_is_flagged_and_poisoned():
+    q, kp, vp, tables, ctx, starts, prefix = grouped_case(5, [(4, 3, None), (3, 2, None)], 8, 2, 128, 16, "bf16")
+    bad = tables.copy()
+    bad[2, 1] = int(tables[5, 0])                               # a block of another group
+    err = pa().new_error_word("cuda")
+    out = run_sp(q, kp, vp, bad, ctx, starts, prefix, 0.088, err=err)
+    assert int(err.item()) & 32
+    assert torch.isnan(out[0:4].float()).all()                  # the whole first group
+    ref = decode_ref(q, kp, vp, tables, ctx, 0.088)
+    keep = list(range(4, len(ctx)))
+    assert_close(out[keep], ref[keep], what="other groups untouched")
+
+
+def test_malformed_description_falls_back_to_plain_attention():
+    q, kp, vp, tables, ctx, starts, prefix = grouped_case(6, [(3, 2, None)], 8, 2, 128, 16, "bf16")
+    err = pa().new_error_word("cuda")
+    wild = prefix.copy()
+    wild[0] = tables.shape[1] + 5                                # more blocks than the table has
+    out = run_sp(q, kp, vp, tables, ctx, starts, wild, 0.088, err=err)
+    assert int(err.item()) & 32
+    assert_close(out, decode_ref(q, kp, vp, tables, ctx, 0.088), what="malformed group")
+
+
+def test_parallel_sampling_full_size():
+    """64 prompts x 8 samples: copy-on-write, append, then prefix-aware
+    decode with the groups the host block manager finds."""
+    from paged_kv_cache_254_gb300 import BlockManager
+    case = make_sampling_case(SAMPLING, device="cuda")
+    cfg = case.cfg
+    B, S = cfg.block_size, cfg.samples
+    tables, ctx = sampling_tables(case)
+    pairs = np.array([[case.prompt_blocks[i // S][-1], case.private_last[i]]
+                      for i in range(len(ctx)) if case.private_last[i] >= 0], dtype=np.int32)
+    slots = np.concatenate([[slot_of(tables[i], t, B) for t in range(cfg.prompt_len, int(ctx[i]))]
+                            for i in range(len(ctx))]).astype(np.int64)
+    wk, wv = copy_ref(bits(case.k_pool), bits(case.v_pool), pairs)
+    wk, wv = append_ref(wk, wv, bits(case.k_new), bits(case.v_new), slots, B)
+    pa().pa_copy_blocks(torch.from_numpy(pairs).cuda(), case.k_pool, case.v_pool)
+    pa().pa_append_kv(case.k_new, case.v_new, torch.from_numpy(slots).cuda(), case.k_pool, case.v_pool)
+    starts = np.arange(0, len(ctx) + 1, S, dtype=np.int32)
+    prefix = np.full(cfg.groups, cfg.prompt_len // B, dtype=np.int32)          # 63 full shared blocks
+    err = pa().new_error_word("cuda")
+    out = run_sp(case.q, case.k_pool, case.v_pool, tables, ctx, starts, prefix, case.scale, err=err)
+    assert pa().pa_read_error(err) == 0
+    dt = case.q.dtype
+    r = np.random.Generator(np.random.PCG64(9))
+    rows = sorted({(int(s), int(h)) for s in r.integers(0, len(ctx), size=12) for h in r.integers(0, 32, size=2)})
+    ref = decode_shared_prefix_ref(case.q, from_bits(wk, dt), from_bits(wv, dt), tables, ctx, case.scale,
+                                   starts, prefix, rows=rows)
+    assert_close(out, ref, rows=rows, what="parallel sampling, prefix-aware")
+    plain = pa().pa_decode(case.q, case.k_pool, case.v_pool, torch.from_numpy(tables).cuda(),
+                           torch.from_numpy(ctx).cuda(), case.scale)
+    a, b = out.double(), plain.double()
+    assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
