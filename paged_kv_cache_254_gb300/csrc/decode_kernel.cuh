@@ -20,11 +20,11 @@
 // Everything about the split depends on context lengths only, never on block
 // ids, so results are bitwise independent of block placement.
 //
-// Shared prefixes (optional).  With prefix groups, the first
-// group_prefix_blocks blocks of a member sequence were already reduced by the
-// prefix kernel into a per-row state (the carry); here the pair covers only
-// the sequence's own blocks after the prefix, and the carry joins the final
-// log-sum-exp combination.
+// Shared prefixes (optional).  With prefix groups, the first first_blocks[s]
+// blocks of a member sequence were already reduced by the prefix kernel into
+// a per-row state (the carry); here the pair covers only the sequence's own
+// blocks after the prefix, and the carry joins the final log-sum-exp
+// combination.
 //
 // Inside a CTA.  Warp NC is the producer: it reads block ids from the table
 // (32 at a time, one per lane), and lane 0 issues two-dimensional TMA loads
@@ -50,11 +50,9 @@ struct DecodeParams {
     int32_t* counters;            // [N * Hkv], zeroed before each launch
     float* partials;              // [gridDim.x][2][G][D + 2]
     uint32_t* err;                // may be null
-    // shared prefixes (n_groups == 0: none)
-    const int32_t* grp_starts;    // [n_groups + 1], ascending
-    const int32_t* grp_prefix;    // [n_groups] shared leading blocks
+    // shared prefixes (first_blocks == null: none)
+    const int32_t* first_blocks;  // [N] blocks already covered by the prefix pass
     const float* carry;           // [N][Hq][D + 2] prefix states (o, m, l)
-    int32_t n_groups;
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
     uint64_t timeout_ns;
@@ -97,24 +95,9 @@ struct CtaInfo {
     int last;
 };
 
-// First block of sequence s read here: past its group's shared prefix, 0
-// outside every group.
-__device__ __forceinline__ int first_block_of(const DecodeParams& p, int s) {
-    if (p.n_groups == 0 || s < __ldg(p.grp_starts)) return 0;
-    int lo = 0, hi = p.n_groups;   // largest gi < n_groups with starts[gi] <= s
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.grp_starts + mid) <= s) lo = mid; else hi = mid;
-    }
-    // the same validity rule as the prefix kernel's: a malformed group has no prefix
-    const int s0 = __ldg(p.grp_starts + lo), s1 = __ldg(p.grp_starts + lo + 1);
-    const int pb = __ldg(p.grp_prefix + lo);
-    return (s0 >= 0 && s < s1 && s1 <= p.N && pb >= 0 && pb <= p.MB) ? pb : 0;
-}
-
 // Blocks of sequence s in this kernel's work list (and its first block).
 __device__ __forceinline__ int pair_blocks(const DecodeParams& p, int s, int BS, int& first) {
-    first = first_block_of(p, s);
+    first = p.first_blocks ? __ldg(p.first_blocks + s) : 0;
     const int nb = seq_blocks(__ldg(p.context_lens + s), BS, p.MB) - first;
     return nb > 0 ? nb : 0;
 }

@@ -137,11 +137,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace of prefix-aware decode: decode counters, prefix counters, carry
 // states, decode partials, prefix partials (offsets in off[0..4]).
-size_t shared_prefix_layout(const pa_shape* s, int dec_ctas, int pre_ctas, size_t (&off)[5]) {
+size_t shared_prefix_layout(const pa_shape* s, int dec_ctas, int pre_ctas, size_t (&off)[6]) {
     const size_t cb = counters_bytes(s);
-    off[0] = 0;
-    off[1] = cb;
-    off[2] = 2 * cb;
+    off[0] = 0;                                   // decode counters
+    off[1] = cb;                                  // prefix counters
+    off[5] = 2 * cb;                              // first block per sequence
+    off[2] = off[5] + align256((size_t)s->num_seqs * sizeof(int32_t));   // carry (after the zeroed part)
     const size_t carry = align256((size_t)s->num_seqs * s->num_q_heads * (s->head_dim + 2) * sizeof(float));
     off[3] = off[2] + carry;
     off[4] = off[3] + align256(partials_bytes(s, dec_ctas));
@@ -216,7 +217,7 @@ size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape) {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int dec = k->max_ctas(dev), pre = pick_prefix(shape).max_ctas(dev);
     if (dec <= 0 || pre <= 0) return 0;
-    size_t off[5];
+    size_t off[6];
     return shared_prefix_layout(shape, dec, pre, off);
 }
 
@@ -242,7 +243,7 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     const PrefixKernelInfo& pk = pick_prefix(shape);
     const int dec = k->max_ctas(dev), pre = pk.max_ctas(dev);
     if (dec <= 0 || pre <= 0) return PA_ERR_CUDA;
-    size_t off[5];
+    size_t off[6];
     const size_t need = shared_prefix_layout(shape, dec, pre, off);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
 
@@ -251,7 +252,7 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     const float scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
-    // both arrival-counter regions start at zero for every call
+    // both arrival-counter regions and the first-block array start at zero
     if (cudaMemsetAsync(ws, 0, off[2], strm) != cudaSuccess) return PA_ERR_CUDA;
 
     if (num_groups > 0) {
@@ -264,6 +265,7 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
         P.p.grp_starts = group_starts;
         P.p.grp_prefix = group_prefix_blocks;
         P.p.carry = reinterpret_cast<float*>(ws + off[2]);
+        P.p.first_blocks = reinterpret_cast<int32_t*>(ws + off[5]);
         P.p.counters = reinterpret_cast<int32_t*>(ws + off[1]);
         P.p.partials = reinterpret_cast<float*>(ws + off[4]);
         P.p.err = err_word;
@@ -291,10 +293,8 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     L.p.counters = reinterpret_cast<int32_t*>(ws + off[0]);
     L.p.partials = reinterpret_cast<float*>(ws + off[3]);
     L.p.err = err_word;
-    L.p.grp_starts = group_starts;
-    L.p.grp_prefix = group_prefix_blocks;
+    L.p.first_blocks = reinterpret_cast<const int32_t*>(ws + off[5]);
     L.p.carry = reinterpret_cast<const float*>(ws + off[2]);
-    L.p.n_groups = num_groups;
     L.p.N = shape->num_seqs;
     L.p.Hq = shape->num_q_heads;
     L.p.Hkv = shape->num_kv_heads;

@@ -11,14 +11,17 @@
 // prefix keys in `carry`; the decode kernel then covers each member's own
 // blocks and folds the carry in.  Items are cut into equal CTA ranges exactly
 // as in the decode kernel, with the same last-arriver merge for items that
-// straddle a range boundary.
+// straddle a range boundary.  Every CTA also writes, for the members of each
+// well-formed group, how many leading blocks the decode kernel must skip.
 //
-// Inside a CTA the roles differ from the decode kernel: all NC consumer warps
-// read every block of the ring (the empty barrier counts NC arrivals) and
-// warp w owns rows [8w, 8w + 8) of the chunk, so no warp merge is needed.
-// Shared blocks are full, so no masking is needed.  Each piece also checks
-// that every member's table repeats the first member's over the prefix and
-// that every member holds at least the prefix; a violation sets
+// Warps: one TMA producer and four consumers arranged as 2 row groups x 2
+// block lanes.  Warp (rg, bl) owns rows [16 rg, 16 rg + 16) of the chunk
+// (full m16 tiles) and the blocks k of the CTA range with k % 2 == bl; each
+// ring stage is read by the two warps of its lane (empty barrier count 2).
+// At a segment end the two lanes of each row group merge through shared
+// memory.  Shared blocks are full, so no masking is needed.  Each piece also
+// checks that every member's table repeats the first member's over the
+// prefix and that every member holds at least the prefix; a violation sets
 // PA_DEVERR_GROUP and poisons the rows with NaN.
 #pragma once
 
@@ -33,6 +36,7 @@ struct PrefixParams {
     const int32_t* grp_starts;    // [n_groups + 1]
     const int32_t* grp_prefix;    // [n_groups]
     float* carry;                 // [N][Hq][D + 2] (o, m, l) out
+    int32_t* first_blocks;        // [N] out: prefix blocks of each member (zeroed before the launch)
     int32_t* counters;            // [N * Hkv], zeroed before each launch
     float* partials;              // [gridDim.x][2][32][D + 2]
     uint32_t* err;
@@ -46,18 +50,25 @@ template <int D_, int BS_, bool BF16_>
 struct PrefixTraits : Geom<D_, BS_> {
     using Gm = Geom<D_, BS_>;
     static constexpr bool BF16 = BF16_;
-    static constexpr int NC = 4;
-    static constexpr int RPW = 8;                 // rows per consumer warp
-    static constexpr int RC = NC * RPW;           // rows per item (chunk)
+    static constexpr int NC = 4;                  // consumer warps
+    static constexpr int RG = 2;                  // row groups
+    static constexpr int BL = NC / RG;            // block lanes
+    static constexpr int RPW = 16;                // rows per warp
+    static constexpr int RC = RG * RPW;           // rows per item (chunk)
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int STAGES = (64 * 1024 / Gm::STAGE_BYTES) > 16 ? 16 : (64 * 1024 / Gm::STAGE_BYTES);
     static constexpr int PSTRIDE = D_ + 2;
-    static constexpr int BAR_OFF = STAGES * Gm::STAGE_BYTES;
-    static constexpr int PS_OFF = BAR_OFF + 2 * STAGES * 8;
-    static constexpr int INFO_OFF = PS_OFF + STAGES * 4;
+    static constexpr int OSTRIDE = D_ + 4;
+    static constexpr int SO_OFF = STAGES * Gm::STAGE_BYTES;
+    static constexpr int SM_OFF = SO_OFF + NC * RPW * OSTRIDE * 4;
+    static constexpr int SL_OFF = SM_OFF + NC * RPW * 4;
+    static constexpr int SP_OFF = SL_OFF + NC * RPW * 4;
+    static constexpr int PS_OFF = SP_OFF + NC * 4;
+    static constexpr int BAR_OFF = ((PS_OFF + STAGES * 4) + 7) & ~7;
+    static constexpr int INFO_OFF = BAR_OFF + 2 * STAGES * 8;
     static constexpr int INFO_BYTES = 64;
     static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;
-    static_assert(STAGES >= 2, "ring");
+    static_assert(STAGES >= 2 && STAGES % BL == 0, "each ring stage belongs to one block lane");
 };
 
 struct PrefixInfo {
@@ -66,8 +77,8 @@ struct PrefixInfo {
     int abort, last, bad;
 };
 
-// Members [s0, s1) and shared blocks of group gi, clamped to valid ranges;
-// returns false (and an empty group) when the description is malformed.
+// Members [s0, s1) and shared blocks of group gi; a malformed description
+// yields an empty group and returns false.
 __device__ __forceinline__ bool group_of(const PrefixParams& p, int gi, int& s0, int& s1, int& pb) {
     s0 = __ldg(p.grp_starts + gi);
     s1 = __ldg(p.grp_starts + gi + 1);
@@ -84,7 +95,6 @@ __device__ __forceinline__ int group_chunks(const PrefixParams& p, int s0, int s
     return ((s1 - s0) * p.G + RC - 1) / RC;
 }
 
-// Blocks that group gi contributes to the flattened list.
 __device__ __forceinline__ long long group_work(const PrefixParams& p, int gi, int RC) {
     int s0, s1, pb;
     group_of(p, gi, s0, s1, pb);
@@ -122,17 +132,26 @@ __device__ __forceinline__ void item_advance(ItemIter& it, int len, const Prefix
     }
 }
 
+__device__ __forceinline__ float* carry_row(const PrefixParams& p, int s0, int kvh, int r, int PSTRIDE) {
+    return p.carry + ((size_t)(s0 + r / p.G) * p.Hq + (size_t)kvh * p.G + r % p.G) * PSTRIDE;
+}
+
 template <class Tr>
 __global__ void __launch_bounds__(Tr::THREADS, 2)
 pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const PrefixParams p) {
     using Gm = typename Tr::Gm;
-    constexpr int D = Tr::D, BS = Tr::BS, NC = Tr::NC, S = Tr::STAGES, RC = Tr::RC;
+    constexpr int D = Tr::D, BS = Tr::BS, NC = Tr::NC, S = Tr::STAGES, RC = Tr::RC, RG = Tr::RG, BL = Tr::BL;
+    constexpr int RPW = Tr::RPW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::BAR_OFF);
+    float* so = reinterpret_cast<float*>(smem + Tr::SO_OFF);
+    float* sm = reinterpret_cast<float*>(smem + Tr::SM_OFF);
+    float* sl = reinterpret_cast<float*>(smem + Tr::SL_OFF);
+    int* spois = reinterpret_cast<int*>(smem + Tr::SP_OFF);
     volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::BAR_OFF);
     PrefixInfo* info = reinterpret_cast<PrefixInfo*>(smem + Tr::INFO_OFF);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + S);
@@ -142,13 +161,19 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (threadIdx.x == 0) {
         for (int st = 0; st < S; ++st) {
             mbar_init(full0 + 8 * st, 1);
-            mbar_init(empty0 + 8 * st, NC);
+            mbar_init(empty0 + 8 * st, RG);
         }
         fence_mbar_init();
     }
     if (warp == NC && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
+    }
+    // blocks the decode kernel skips for each member of a well-formed group
+    for (int gi = blockIdx.x; gi < p.n_groups; gi += gridDim.x) {
+        int s0, s1, pb;
+        group_of(p, gi, s0, s1, pb);
+        for (int s = s0 + threadIdx.x; s < s1; s += Tr::THREADS) p.first_blocks[s] = pb;
     }
 
     // ---- work range of this CTA (warp 0) ----
@@ -292,23 +317,27 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int tid = threadIdx.x;
     const int g = lane >> 2;
     const int t4 = lane & 3;
+    const int rg = warp % RG;
+    const int bl = warp / RG;
     const float qnan = __int_as_float(0x7fc00000);
     ItemIter it = it0;
-    WarpAcc<D, 1> acc;
+    WarpAcc<D, 2> acc;
     while (it.gi_flat < hi) {
         const int len = (int)min((long long)(it.pb - it.b0), hi - it.gi_flat);
         const int R = (it.s1 - it.s0) * p.G;                 // rows of the group for this KV head
-        const int rbase = it.ch * RC + warp * Tr::RPW;       // first row of this warp
-        // Q fragments: fragment row g -> row rbase + g of the chunk.
-        const int r0 = rbase + g;
-        const uint16_t* q0 = r0 < R ? p.q + ((size_t)(it.s0 + r0 / p.G) * p.Hq + (size_t)it.kvh * p.G + r0 % p.G) * D
-                                    : nullptr;
+        const int rbase = it.ch * RC + rg * RPW;             // first row of this warp
+        auto qptr = [&](int r) -> const uint16_t* {
+            return r < R ? p.q + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) * D : nullptr;
+        };
         uint32_t qa[Gm::KD][4];
-        load_q_frags<D>(qa, q0, nullptr, t4);
+        load_q_frags<D>(qa, qptr(rbase + g), qptr(rbase + g + 8), t4);
         acc.reset();
         int poisoned = 0;
 
-        for (int j = 0; j < len; ++j) {
+        // block k (k = gi_flat - lo) of the range goes to lane k % BL
+        int j0 = bl - (int)((it.gi_flat - lo) % BL);
+        if (j0 < 0) j0 += BL;
+        for (int j = j0; j < len; j += BL) {
             const long long k = it.gi_flat + j - lo;
             const int st = (int)(k % S);
             const uint32_t par = (uint32_t)((k / S) & 1);
@@ -326,7 +355,7 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             poisoned |= stage_poison[st];
             const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
-            consume_block<Gm, 1, Tr::BF16>(kb, kb + Gm::CHUNK_BYTES, BS, qa, acc, p.scale_log2, lane);
+            consume_block<Gm, 2, Tr::BF16>(kb, kb + Gm::CHUNK_BYTES, BS, qa, acc, p.scale_log2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
         }
@@ -344,52 +373,66 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             if (bad) atomicOr(&info->bad, 1);
         }
-        acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 1);
-        acc.l[0] += __shfl_xor_sync(0xffffffffu, acc.l[0], 2);
+
+        // ---- write this warp's state; merge the two block lanes ----
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
+            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
+        }
+        {
+            float* mine = so + warp * RPW * Tr::OSTRIDE;
+#pragma unroll
+            for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        mine[(8 * r + 2 * t4 + (e & 1)) * Tr::OSTRIDE + 16 * mt + g + 8 * (e >> 1)] = acc.o[mt][r][e];
+            if (t4 == 0) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    sm[warp * RPW + g + 8 * r] = acc.m[r];
+                    sl[warp * RPW + g + 8 * r] = acc.l[r];
+                }
+            }
+            if (lane == 0) spois[warp] = poisoned;
+        }
         named_bar_sync(1, NC * 32);
         const bool group_bad = *(volatile int*)&info->bad != 0;
-        poisoned |= group_bad;
         if (group_bad && tid == 0) set_err(p.err, PA_DEVERR_GROUP);
+        int anybad = group_bad ? 1 : 0;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) anybad |= spois[w];
 
         const long long P0 = it.gi_flat - it.b0;
         const long long cfirst = cta_of(P0, W, geff);
         const long long clast = cta_of(P0 + it.pb - 1, W, geff);
         const bool complete = cfirst == clast;
         const int slot = (it.gi_flat == lo) ? 0 : 1;
-        // This lane's O^T fragments: c0,c1 -> rows 2*t4, 2*t4+1 (of the warp's 8),
-        // dims 16*mt + g (+8 for c2, c3); m and l of row g sit in lane 4g.
-        if (complete) {
-#pragma unroll
-            for (int mt = 0; mt < Gm::KD; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = rbase + 2 * t4 + (e & 1);
-                    if (r < R) {
-                        float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) *
-                                                 Tr::PSTRIDE;
-                        c[16 * mt + g + 8 * (e >> 1)] = poisoned ? qnan : acc.o[mt][0][e];
-                    }
-                }
-            if (t4 == 0 && rbase + g < R) {
-                const int r = rbase + g;
-                float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) * Tr::PSTRIDE;
-                c[D] = acc.m[0];
-                c[D + 1] = acc.l[0];
+        const int rows = min(RC, R - it.ch * RC);
+        float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * RC * Tr::PSTRIDE;
+        for (int idx = tid; idx < rows * D; idx += NC * 32) {
+            const int rloc = idx / D;
+            const int dim = idx - rloc * D;
+            const int rr = rloc % RPW;
+            const int w0 = rloc / RPW, w1 = w0 + RG;          // the two lanes of this row group
+            const float m0 = sm[w0 * RPW + rr], m1 = sm[w1 * RPW + rr];
+            const float M = fmaxf(m0, m1);
+            const float f0 = ex2(m0 - M), f1 = ex2(m1 - M);
+            const float L = sl[w0 * RPW + rr] * f0 + sl[w1 * RPW + rr] * f1;
+            float O = so[(w0 * RPW + rr) * Tr::OSTRIDE + dim] * f0 + so[(w1 * RPW + rr) * Tr::OSTRIDE + dim] * f1;
+            if (anybad) O = qnan;
+            float* dst = complete ? carry_row(p, it.s0, it.kvh, it.ch * RC + rloc, Tr::PSTRIDE)
+                                  : prow + rloc * Tr::PSTRIDE;
+            dst[dim] = O;
+            if (dim == 0) {
+                dst[D] = M;
+                dst[D + 1] = L;
             }
-        } else {
-            float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * RC * Tr::PSTRIDE;
-#pragma unroll
-            for (int mt = 0; mt < Gm::KD; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int rr = warp * Tr::RPW + 2 * t4 + (e & 1);
-                    prow[rr * Tr::PSTRIDE + 16 * mt + g + 8 * (e >> 1)] = poisoned ? qnan : acc.o[mt][0][e];
-                }
-            if (t4 == 0) {
-                const int rr = warp * Tr::RPW + g;
-                prow[rr * Tr::PSTRIDE + D] = acc.m[0];
-                prow[rr * Tr::PSTRIDE + D + 1] = acc.l[0];
-            }
+        }
+
+        if (!complete) {
             __threadfence();
             named_bar_sync(1, NC * 32);
             const int cid = (it.s0 + it.ch * (RC / p.G)) * p.Hkv + it.kvh;
@@ -400,20 +443,17 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             named_bar_sync(1, NC * 32);
             if (*(volatile int*)&info->last) {
                 __threadfence();
-                const int rows = min(RC, R - it.ch * RC);
                 for (int idx = tid; idx < rows * (D + 2); idx += NC * 32) {
-                    const int rr = idx / (D + 2);
-                    const int col = idx - rr * (D + 2);
+                    const int rloc = idx / (D + 2);
+                    const int col = idx - rloc * (D + 2);
                     float M = -INFINITY, L = 0.f, O = 0.f;
                     for (long long c = cfirst; c <= clast; ++c) {
                         const int sl_c = (c == cfirst && range_lo(c, W, geff) < P0) ? 1 : 0;
-                        const float* pr = p.partials + ((size_t)c * 2 + sl_c) * RC * Tr::PSTRIDE + rr * Tr::PSTRIDE;
+                        const float* pr = p.partials + ((size_t)c * 2 + sl_c) * RC * Tr::PSTRIDE + rloc * Tr::PSTRIDE;
                         lse_fold(M, L, O, __ldcg(pr + D), __ldcg(pr + D + 1), col < D ? __ldcg(pr + col) : 0.f);
                     }
-                    const int r = it.ch * RC + rr;
-                    float* c = p.carry + ((size_t)(it.s0 + r / p.G) * p.Hq + (size_t)it.kvh * p.G + r % p.G) *
-                                             Tr::PSTRIDE;
-                    c[col] = col < D ? O : (col == D ? M : L);
+                    float* dst = carry_row(p, it.s0, it.kvh, it.ch * RC + rloc, Tr::PSTRIDE);
+                    dst[col] = col < D ? O : (col == D ? M : L);
                 }
             }
         }
