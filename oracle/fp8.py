@@ -1,0 +1,131 @@
+"""8-bit floating-point KV cache: the E4M3 and E5M2 encodings.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+The pages: storing keys and values in 8 bits (FP8) instead of 16 halves the
+KV memory (ontq "AI Inference Serving at Scale", section 6); the vLLM
+deployment script on thewebvale (section 5) names fp8_e5m2 as a KV-cache
+dtype.  They give neither the bit layout nor a scaling rule.  Readings taken:
+
+  * E4M3 is the OCP 8-bit format with 1 sign, 4 exponent (bias 7), 3 mantissa
+    bits, subnormals, no infinities, one NaN pattern per sign (S.1111.111);
+    its largest finite magnitude is 448.  E5M2 has 5 exponent bits (bias 15),
+    2 mantissa bits, subnormals, infinities and NaNs, largest finite 57344.
+  * A cache tensor stores code(x / s) for a per-tensor fp32 scale s (one for
+    K, one for V); decoding multiplies by s.  The division is one fp32
+    division, rounded to nearest.
+  * Encoding rounds to the nearest representable value, ties to the even
+    code, and saturates finite values beyond the largest magnitude to it;
+    NaN stays NaN.
+
+Everything below is written from those definitions: values are enumerated
+from the bit fields, and encoding picks the nearest enumerated value.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+FORMATS = {"e4m3": (4, 3, 7), "e5m2": (5, 2, 15)}
+
+
+def decode_code(code: int, fmt: str) -> float:
+    """Value of one 8-bit code (Python float; inf/nan where the format has them)."""
+    e_bits, m_bits, bias = FORMATS[fmt]
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> m_bits) & ((1 << e_bits) - 1)
+    m = code & ((1 << m_bits) - 1)
+    e_max = (1 << e_bits) - 1
+    if fmt == "e4m3":
+        if e == e_max and m == (1 << m_bits) - 1:
+            return float("nan")
+    elif e == e_max:
+        return sign * float("inf") if m == 0 else float("nan")
+    if e == 0:
+        return sign * (m / (1 << m_bits)) * 2.0 ** (1 - bias)
+    return sign * (1.0 + m / (1 << m_bits)) * 2.0 ** (e - bias)
+
+
+def _finite_table(fmt):
+    """Non-negative finite codes and their values, ascending."""
+    codes = [c for c in range(0x80) if np.isfinite(decode_code(c, fmt))]
+    vals = [decode_code(c, fmt) for c in codes]
+    order = np.argsort(vals, kind="stable")
+    return np.array(codes)[order], np.array(vals)[order]
+
+
+def max_finite(fmt: str) -> float:
+    return float(_finite_table(fmt)[1][-1])
+
+
+def encode_value(x: float, fmt: str) -> int:
+    """Nearest code to x (ties to the even code), saturating to the largest
+    finite magnitude; NaN -> the format's NaN code (positive sign)."""
+    if np.isnan(x):
+        return 0x7F
+    codes, vals = _finite_table(fmt)
+    a = abs(float(x))
+    sign = 0x80 if (np.signbit(x) and a != 0.0) else 0
+    if np.signbit(x) and a == 0.0:
+        sign = 0x80
+    if a >= vals[-1]:
+        return sign | int(codes[-1])
+    i = int(np.searchsorted(vals, a))           # vals[i-1] < a <= vals[i]
+    if vals[i] == a:
+        return sign | int(codes[i])
+    lo, hi = i - 1, i
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    if dlo < dhi:
+        pick = lo
+    elif dhi < dlo:
+        pick = hi
+    else:
+        pick = lo if (codes[lo] & 1) == 0 else hi   # even mantissa
+    return sign | int(codes[pick])
+
+
+def decode_array(codes, fmt: str) -> np.ndarray:
+    table = np.array([decode_code(c, fmt) for c in range(256)])
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def quantize(x, scale: float, fmt: str) -> np.ndarray:
+    """Codes of x / scale (fp32 division) for an array of 16-bit values."""
+    xf = np.asarray(x, dtype=np.float32) / np.float32(scale)
+    flat = xf.ravel()
+    out = np.fromiter((encode_value(float(v), fmt) for v in flat), dtype=np.uint8, count=flat.size)
+    return out.reshape(xf.shape)
+
+
+def dequantize(codes, scale: float, fmt: str) -> np.ndarray:
+    """fp64 values of stored codes: decode(code) * scale."""
+    return decode_array(codes, fmt) * float(np.float32(scale))
+
+
+# ---------------------------------------------------------------------------
+# The 8-bit cache.  Reading taken for the layout: K codes as the 16-bit cache,
+# [blocks][kv heads][B][d]; V codes with each (block, head) chunk stored dims
+# first, [blocks][kv heads][d][B] (the pages fix no layout).
+# ---------------------------------------------------------------------------
+
+def append_fp8_ref(k_codes, v_codes, k_new, v_new, slot_mapping, block_size, k_scale, v_scale, fmt):
+    """New (k_codes, v_codes) with row i of k_new / v_new (16-bit values
+    [T, Hkv, d]) quantized into slot slot_mapping[i]; negative slots skip."""
+    k = np.array(k_codes, copy=True)
+    v = np.array(v_codes, copy=True)
+    kn = np.asarray(k_new, dtype=np.float32)
+    vn = np.asarray(v_new, dtype=np.float32)
+    for i, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if slot < 0:
+            continue
+        blk, off = int(slot) // block_size, int(slot) % block_size
+        k[blk, :, off, :] = quantize(kn[i], k_scale, fmt)
+        v[blk, :, :, off] = quantize(vn[i], v_scale, fmt)
+    return k, v
+
+
+def dequantized_pools(k_codes, v_codes, k_scale, v_scale, fmt):
+    """fp64 pools in the 16-bit cache's layout [blocks][kv heads][B][d]."""
+    k = dequantize(k_codes, k_scale, fmt)
+    v = dequantize(np.swapaxes(np.asarray(v_codes), 2, 3), v_scale, fmt)
+    return k, v

@@ -1,0 +1,96 @@
+"""Pins for the FP8 encodings of the oracle: every code, the formats' known
+constants, rounding ties, saturation."""
+
+import numpy as np
+import pytest
+
+from oracle.fp8 import decode_code, encode_value, max_finite, quantize, dequantize
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_every_finite_code_round_trips(fmt):
+    for c in range(256):
+        v = decode_code(c, fmt)
+        if np.isfinite(v):
+            got = encode_value(v, fmt)
+            assert decode_code(got, fmt) == v and (got == c or v == 0.0), (c, v, got)
+
+
+def test_known_constants():
+    assert max_finite("e4m3") == 448.0
+    assert max_finite("e5m2") == 57344.0
+    assert decode_code(0x01, "e4m3") == 2.0 ** -9          # smallest subnormal
+    assert decode_code(0x08, "e4m3") == 2.0 ** -6          # smallest normal
+    assert decode_code(0x7E, "e4m3") == 448.0
+    assert np.isnan(decode_code(0x7F, "e4m3")) and np.isnan(decode_code(0xFF, "e4m3"))
+    assert decode_code(0x38, "e4m3") == 1.0
+    assert decode_code(0x3C, "e5m2") == 1.0
+    assert decode_code(0x7C, "e5m2") == np.inf
+    assert decode_code(0x01, "e5m2") == 2.0 ** -16
+    assert decode_code(0xC0, "e4m3") == -2.0
+
+
+def test_ties_go_to_even_and_saturation():
+    # 1.0 = 0x38 and 1.125 = 0x39 in E4M3: the midpoint 1.0625 goes to 0x38 (even)
+    assert encode_value(1.0625, "e4m3") == 0x38
+    # 1.125 (0x39) and 1.25 (0x3A): midpoint 1.1875 goes to 0x3A
+    assert encode_value(1.1875, "e4m3") == 0x3A
+    assert encode_value(1.19, "e4m3") == 0x3A and encode_value(1.18, "e4m3") == 0x39
+    assert encode_value(1e6, "e4m3") == 0x7E and encode_value(-1e6, "e4m3") == 0xFE
+    assert encode_value(1e9, "e5m2") == 0x7B                # largest finite, not inf
+    assert encode_value(2.0 ** -12, "e4m3") == 0x00         # below half the smallest subnormal
+    assert encode_value(3 * 2.0 ** -10, "e4m3") == 0x02     # 1.5 subnormal steps: tie -> even code
+    assert encode_value(5 * 2.0 ** -10, "e4m3") == 0x02     # 2.5 steps: tie -> even code
+    assert np.isnan(decode_code(encode_value(float("nan"), "e4m3"), "e4m3"))
+
+
+def test_quantize_divides_by_the_scale_in_fp32():
+    x = np.array([0.5, -3.0, 100.0, 7.0e-4], dtype=np.float32)
+    codes = quantize(x, 0.25, "e4m3")
+    # 100 / 0.25 = 400 lies halfway between 384 and 416: the even code (384)
+    np.testing.assert_array_equal(dequantize(codes, 0.25, "e4m3"), [0.5, -3.0, 96.0, 0.25 * 2.0 ** -9])
+
+
+def test_append_then_dequantize_returns_the_quantized_rows():
+    from oracle.fp8 import append_fp8_ref, dequantized_pools
+    from oracle.attention import gather_sequence
+    r = np.random.Generator(np.random.PCG64(1))
+    NB, Hkv, B, d = 6, 2, 4, 8
+    k = r.integers(0, 0x7E, size=(NB, Hkv, B, d)).astype(np.uint8)
+    v = r.integers(0, 0x7E, size=(NB, Hkv, d, B)).astype(np.uint8)
+    kn = r.standard_normal((3, Hkv, d)).astype(np.float32)
+    vn = r.standard_normal((3, Hkv, d)).astype(np.float32)
+    row = [4, 1]
+    slots = [4 * 4 + 0, 1 * 4 + 3, -1]
+    k2, v2 = append_fp8_ref(k, v, kn, vn, slots, B, 0.5, 2.0, "e4m3")
+    kf, vf = dequantized_pools(k2, v2, 0.5, 2.0, "e4m3")
+    K, V = gather_sequence(kf, vf, row, 8, 1, B)
+    np.testing.assert_array_equal(K[0], dequantize(quantize(kn[0, 1], 0.5, "e4m3"), 0.5, "e4m3"))
+    np.testing.assert_array_equal(V[7], dequantize(quantize(vn[1, 1], 2.0, "e4m3"), 2.0, "e4m3"))
+    # untouched slots keep their codes; V chunks are stored dims-first
+    np.testing.assert_array_equal(v2[4, :, :, 1:], v[4, :, :, 1:])
+    np.testing.assert_array_equal(np.swapaxes(v2, 2, 3)[4, 0, 0], quantize(vn[0, 0], 2.0, "e4m3"))
+
+
+def test_representable_values_survive_the_8_bit_cache():
+    """Values already on the E4M3 grid (times the scales) decode exactly: the
+    8-bit cache then gives the 16-bit cache's attention."""
+    from oracle.fp8 import append_fp8_ref, dequantized_pools
+    from oracle.attention import decode_ref
+    r = np.random.Generator(np.random.PCG64(2))
+    NB, Hkv, B, d, ctx = 5, 1, 4, 8, 13
+    grid = np.array([decode_code(c, "e4m3") for c in range(0x70)])
+    kc = r.choice(grid, size=(NB, Hkv, B, d)) * 0.25
+    vc = r.choice(grid, size=(NB, Hkv, B, d)) * 4.0
+    row = [3, 0, 4, 1]
+    slots = [row[t // B] * B + t % B for t in range(ctx)]
+    k8 = np.zeros((NB, Hkv, B, d), np.uint8)
+    v8 = np.zeros((NB, Hkv, d, B), np.uint8)
+    kn = np.stack([kc[row[t // B], :, t % B] for t in range(ctx)])
+    vn = np.stack([vc[row[t // B], :, t % B] for t in range(ctx)])
+    k8, v8 = append_fp8_ref(k8, v8, kn, vn, slots, B, 0.25, 4.0, "e4m3")
+    kf, vf = dequantized_pools(k8, v8, 0.25, 4.0, "e4m3")
+    q = r.standard_normal((1, 2, d))
+    a = decode_ref(q, kf, vf, np.array([row]), np.array([ctx]), 0.3)
+    b = decode_ref(q, kc, vc, np.array([row]), np.array([ctx]), 0.3)
+    np.testing.assert_array_equal(a, b)
