@@ -90,11 +90,20 @@ def decode_array(codes, fmt: str) -> np.ndarray:
 
 
 def quantize(x, scale: float, fmt: str) -> np.ndarray:
-    """Codes of x / scale (fp32 division) for an array of 16-bit values."""
+    """Codes of x / scale (one fp32 division each) for an array of 16-bit
+    values: the same nearest / ties-to-even / saturating rule as
+    encode_value, applied with a sorted table of the format's values."""
     xf = np.asarray(x, dtype=np.float32) / np.float32(scale)
-    flat = xf.ravel()
-    out = np.fromiter((encode_value(float(v), fmt) for v in flat), dtype=np.uint8, count=flat.size)
-    return out.reshape(xf.shape)
+    codes, vals = _finite_table(fmt)
+    a = np.abs(xf).astype(np.float64)
+    i = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)     # vals[i-1] < a <= vals[i]
+    lo, hi = i - 1, i
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    even_lo = (codes[lo] & 1) == 0
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(even_lo, lo, hi)))
+    pick = np.where(a >= vals[-1], len(vals) - 1, pick)
+    out = codes[pick].astype(np.uint8) | np.where(np.signbit(xf), 0x80, 0).astype(np.uint8)
+    return np.where(np.isnan(xf), np.uint8(0x7F), out).astype(np.uint8)
 
 
 def dequantize(codes, scale: float, fmt: str) -> np.ndarray:

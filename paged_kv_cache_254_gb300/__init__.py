@@ -15,7 +15,10 @@ from .ops import (  # noqa: F401
     new_error_word,
     pa_append_kv,
     pa_copy_blocks,
+    pa_append_kv_fp8,
+    pa_copy_blocks_fp8,
     pa_decode,
+    pa_decode_fp8,
     pa_decode_shared_prefix,
     pa_decode_workspace_bytes,
     pa_read_error,

@@ -19,13 +19,13 @@ STATUS_NAMES = {
     0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
     4: "PA_ERR_OUT_OF_RANGE", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_WORKSPACE",
 }
-PA_FP16, PA_BF16 = 0, 1
+PA_FP16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3
 DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, DEVERR_GROUP = 1, 2, 4, 8, 16, 32
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
            "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
-           "pa_decode_shared_prefix")
+           "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -91,6 +91,13 @@ def load() -> ctypes.CDLL:
         lib.pa_decode_shared_prefix_workspace_bytes.restype = SZ
         lib.pa_decode_shared_prefix.argtypes = [SP, P, P, P, P, P, I32, P, P, ctypes.c_float, P, P, SZ, P, P]
         lib.pa_decode_shared_prefix.restype = I32
+        F = ctypes.c_float
+        lib.pa_decode_fp8_workspace_bytes.argtypes = [SP, I32]
+        lib.pa_decode_fp8_workspace_bytes.restype = SZ
+        lib.pa_decode_fp8.argtypes = [SP, I32, P, P, P, P, P, F, F, F, P, P, SZ, P, P]
+        lib.pa_decode_fp8.restype = I32
+        lib.pa_append_kv_fp8.argtypes = [SP, I32, I32, P, P, P, P, P, F, F, P, P]
+        lib.pa_append_kv_fp8.restype = I32
         _lib = lib
         return lib
 

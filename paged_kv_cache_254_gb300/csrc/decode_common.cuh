@@ -14,11 +14,14 @@ namespace pa {
 
 // One (block, KV head) chunk as it sits in a ring stage: HALVES boxes of
 // BS rows x 128 bytes, 128-byte swizzled; the K chunk, then the V chunk.
-template <int D_, int BS_>
+// ELEM is the byte size of a cached element (2, or 1 for the 8-bit cache,
+// whose V chunk is stored dims-first and copied as one contiguous piece).
+template <int D_, int BS_, int ELEM_ = 2>
 struct Geom {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
-    static constexpr int HALVES = D / 64;
+    static constexpr int ELEM = ELEM_;
+    static constexpr int HALVES = D * ELEM / 128;
     static constexpr int BOX_BYTES = BS * 128;
     static constexpr int CHUNK_BYTES = HALVES * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
@@ -27,6 +30,7 @@ struct Geom {
     static constexpr int KD = D / 16;    // 16-dim k-steps of QK, m-tiles of PV
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
+    static_assert(ELEM == 2 || (ELEM == 1 && D == 128), "8-bit cache rows are 128 bytes");
 };
 
 __device__ __forceinline__ int seq_blocks(int ctx, int BS, int MB) {
@@ -209,6 +213,164 @@ __device__ __forceinline__ void consume_block(uint32_t kb, uint32_t vb, int vali
                 mma16816<BF16>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
             }
         }
+}
+
+// ---------------------------------------------------------------- 8-bit cache
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// Token order of the 8-bit path.  In n-tile nt of S^T, column n holds block
+// token perm_token(nt, n); it makes the tokens that the PV fragments pair up
+// (2 t4 + e and 2 t4 + 8 + e of a 16-token k-step) sit next to each other in
+// the dims-first V chunk, so a lane reads them with one 4-byte load.
+__device__ __forceinline__ int perm_token(int nt, int n) {
+    return 16 * (nt >> 1) + 4 * (n >> 1) + 2 * (nt & 1) + (n & 1);
+}
+
+// Q fragments for the 8-bit path, in fp16, with the head dims in the order
+// the K bytes are read: k-step kk, fragment column 2 t4 + e -> dim
+// 32 t4 + 4 kk + e, column 2 t4 + 8 + e -> dim 32 t4 + 4 kk + 2 + e.
+template <int D, bool QBF16>
+__device__ __forceinline__ void load_q_frags8(uint32_t (&qa)[D / 16][4], const uint16_t* row0,
+                                              const uint16_t* row1, int t4) {
+    auto ld = [](const uint16_t* p) -> uint32_t {
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
+        if constexpr (QBF16) return bf16x2_to_f16x2(v);
+        return v;
+    };
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const int c = 32 * t4 + 4 * kk;
+        qa[kk][0] = row0 ? ld(row0 + c) : 0u;
+        qa[kk][2] = row0 ? ld(row0 + c + 2) : 0u;
+        qa[kk][1] = row1 ? ld(row1 + c) : 0u;
+        qa[kk][3] = row1 ? ld(row1 + c + 2) : 0u;
+    }
+}
+
+// consume_block for the 8-bit cache: K rows (BS x 128 bytes, swizzled) and
+// the dims-first V chunk (D rows x BS bytes) are turned into fp16 fragments
+// in registers; scores and PV run on the fp16 MMA.  The scales are applied
+// outside (K's inside scale_log2, V's at the final write).
+template <class Gm, int NR, bool E5M2>
+__device__ __forceinline__ void consume_block8(uint32_t kb, uint32_t vb, int valid,
+                                               const uint32_t (&qa)[Gm::KD][4], WarpAcc<Gm::D, NR>& acc,
+                                               float scale_log2, int lane) {
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    float sacc[Gm::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        const int row = perm_token(nt, g);
+        uint32_t w[8];
+        uint32_t w0[4], w1[4];
+        lds128(kb + row * 128 + (((2 * t4) ^ (row & 7)) << 4), w0);
+        lds128(kb + row * 128 + (((2 * t4 + 1) ^ (row & 7)) << 4), w1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[i] = w0[i];
+            w[i + 4] = w1[i];
+        }
+#pragma unroll
+        for (int kk = 0; kk < Gm::KD; ++kk) {
+            const uint32_t b0 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] & 0xffffu));
+            const uint32_t b1 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] >> 16));
+            mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+        }
+    }
+
+    float mx[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) mx[r] = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tok = perm_token(nt, 2 * t4 + (e & 1));
+            const float v = tok < valid ? sacc[nt][e] * scale_log2 : -INFINITY;
+            sacc[nt][e] = v;
+            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], v);
+        }
+    float alpha[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float m_new = fmaxf(acc.m[r], mx[r]);
+        alpha[r] = ex2(acc.m[r] - m_new);
+        acc.m[r] = m_new;
+        acc.l[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = e >> 1;
+            if (r < NR) {
+                const float pe = ex2(sacc[nt][e] - acc.m[r]);
+                sacc[nt][e] = pe;
+                acc.l[r] += pe;
+            }
+        }
+    uint32_t pb[Gm::KT][NR][2], pl[Gm::KT][NR][2];
+#pragma unroll
+    for (int kt = 0; kt < Gm::KT; ++kt)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float x0 = sacc[2 * kt + h][2 * r], x1 = sacc[2 * kt + h][2 * r + 1];
+                const uint32_t hi = pack2<false>(x0, x1);
+                pb[kt][r][h] = hi;
+                pl[kt][r][h] = pack2<false>(x0 - lo_of<false>(hi), x1 - hi_of<false>(hi));
+            }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
+        const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
+#pragma unroll
+        for (int mt = 0; mt < Gm::KD; ++mt) {
+            acc.o[mt][r][0] *= aa;
+            acc.o[mt][r][1] *= ab;
+            acc.o[mt][r][2] *= aa;
+            acc.o[mt][r][3] *= ab;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+        for (int kt = 0; kt < Gm::KT; ++kt) {
+            const uint32_t x = lds32(vb + (16 * mt + g) * Gm::BS + 16 * kt + 4 * t4);
+            const uint32_t y = lds32(vb + (16 * mt + g + 8) * Gm::BS + 16 * kt + 4 * t4);
+            const uint32_t a0 = fp8x2_to_f16x2<E5M2>((uint16_t)(x & 0xffffu));
+            const uint32_t a2 = fp8x2_to_f16x2<E5M2>((uint16_t)(x >> 16));
+            const uint32_t a1 = fp8x2_to_f16x2<E5M2>((uint16_t)(y & 0xffffu));
+            const uint32_t a3 = fp8x2_to_f16x2<E5M2>((uint16_t)(y >> 16));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
+                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
+            }
+        }
+}
+
+// Zero the bytes of tokens >= valid in every dim row of a dims-first V chunk.
+template <class Gm>
+__device__ __forceinline__ void zero_v8_tail(uint32_t vb, int valid, int lane) {
+    const int w = Gm::BS - valid;
+    for (int i = lane; i < Gm::D * w; i += 32) {
+        const uint32_t a = vb + (i / w) * Gm::BS + valid + i % w;
+        asm volatile("st.shared.u8 [%0], %1;" :: "r"(a), "h"((uint16_t)0) : "memory");
+    }
 }
 
 // Zero the V rows at offsets >= valid of a partly filled block (they may hold

@@ -53,16 +53,21 @@ struct DecodeParams {
     // shared prefixes (first_blocks == null: none)
     const int32_t* first_blocks;  // [N] blocks already covered by the prefix pass
     const float* carry;           // [N][Hq][D + 2] prefix states (o, m, l)
+    const uint8_t* v8;            // 8-bit cache only: the V pool, chunks dims-first
+    float v_scale;                // multiplies the output (V's cache scale; 1 for 16-bit)
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
     uint64_t timeout_ns;
 };
 
-template <int D_, int BS_, int G_, bool BF16_>
-struct DecodeTraits : Geom<D_, BS_> {
-    using Gm = Geom<D_, BS_>;
+// KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2.
+template <int D_, int BS_, int G_, bool BF16_, int KVF_ = 0>
+struct DecodeTraits : Geom<D_, BS_, KVF_ ? 1 : 2> {
+    using Gm = Geom<D_, BS_, KVF_ ? 1 : 2>;
     static constexpr int G = G_;
     static constexpr bool BF16 = BF16_;
+    static constexpr bool KV8 = KVF_ != 0;
+    static constexpr bool E5M2 = KVF_ == 2;
     static constexpr int NC = 4;                            // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
     static constexpr int RING_TARGET = 64 * 1024;
@@ -226,7 +231,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     v = qnan16<Tr::BF16>();
                 } else if (first > 0 && ctx > 0) {
                     const float* c = p.carry + ((size_t)s * p.Hq + i / D) * Tr::PSTRIDE;
-                    v = f32_to_16<Tr::BF16>(__ldg(c + i % D) / __ldg(c + D + 1));
+                    v = f32_to_16<Tr::BF16>(__ldg(c + i % D) / __ldg(c + D + 1) * p.v_scale);
                 }
                 row[i] = v;
             }
@@ -276,10 +281,15 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                             mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
                             const int y = (id * p.Hkv + it.kvh) * BS;
                             const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
+                            if constexpr (Tr::KV8) {
+                                tma_load_2d(kdst, &tmap_k, 0, y, fb);
+                                bulk_load(kdst + Gm::CHUNK_BYTES, p.v8 + (size_t)y * D, Gm::CHUNK_BYTES, fb);
+                            } else {
 #pragma unroll
-                            for (int h = 0; h < Gm::HALVES; ++h) {
-                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                                for (int h = 0; h < Gm::HALVES; ++h) {
+                                    tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                                    tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                                }
                             }
                         } else {
                             set_err(p.err, PA_DEVERR_TIMEOUT);
@@ -322,7 +332,11 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // Q fragments (A operand of S^T = Q K^T): rows = heads of the group.
         const uint16_t* qrow = p.q + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
         uint32_t qa[Gm::KD][4];
-        load_q_frags<D>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
+        if constexpr (Tr::KV8) {
+            load_q_frags8<D, Tr::BF16>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
+        } else {
+            load_q_frags<D>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
+        }
         acc.reset();
         int poisoned = 0;
 
@@ -351,11 +365,19 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const int valid = min(BS, ctx - (it.first + it.b0 + j) * BS);
             const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
             const uint32_t vb = kb + Gm::CHUNK_BYTES;
-            if (valid < BS) {
-                zero_v_tail<Gm>(vb, valid, lane);
-                __syncwarp();
+            if constexpr (Tr::KV8) {
+                if (valid < BS) {
+                    zero_v8_tail<Gm>(vb, valid, lane);
+                    __syncwarp();
+                }
+                consume_block8<Gm, Tr::NR, Tr::E5M2>(kb, vb, valid, qa, acc, p.scale_log2, lane);
+            } else {
+                if (valid < BS) {
+                    zero_v_tail<Gm>(vb, valid, lane);
+                    __syncwarp();
+                }
+                consume_block<Gm, Tr::NR, Tr::BF16>(kb, vb, valid, qa, acc, p.scale_log2, lane);
             }
-            consume_block<Gm, Tr::NR, Tr::BF16>(kb, vb, valid, qa, acc, p.scale_log2, lane);
             if (valid < BS) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -425,7 +447,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     const float* c = crow + head * Tr::PSTRIDE;
                     lse_fold(M, L, O, __ldg(c + D), __ldg(c + D + 1), __ldg(c + dim));
                 }
-                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L);
+                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
             } else {
                 prow[head * Tr::PSTRIDE + dim] = O;
                 if (dim == 0) {
@@ -460,7 +482,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                         const float* cr = crow + head * Tr::PSTRIDE;
                         lse_fold(M, L, O, __ldg(cr + D), __ldg(cr + D + 1), __ldg(cr + dim));
                     }
-                    orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L);
+                    orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
                 }
             }
         }
@@ -498,7 +520,9 @@ DecodeKernelInfo decode_info() {
 }
 
 // Per-(dtype, head_dim) tables, defined in the instantiation units.
-// Index: [bs == 32][log2(g)].
+// Index: [bs == 32][log2(g)]; the 8-bit tables add [e5m2] in front.
+void decode8_table_bf16(DecodeKernelInfo (&t)[2][2][5]);
+void decode8_table_fp16(DecodeKernelInfo (&t)[2][2][5]);
 void decode_table_bf16_d128(DecodeKernelInfo (&t)[2][5]);
 void decode_table_bf16_d64(DecodeKernelInfo (&t)[2][5]);
 void decode_table_fp16_d128(DecodeKernelInfo (&t)[2][5]);

@@ -11,7 +11,9 @@
 #include <cstdint>
 
 #include "kv_ops.cuh"
+#include "ptx.cuh"
 #include "../../include/pa.h"
+#include <cuda_fp16.h>
 
 namespace pa {
 
@@ -72,6 +74,94 @@ pa_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k_pool, ui
             vd[v] = vs[v];
         }
     }
+}
+
+// Quantising append for the 8-bit cache.  One thread per 16 head dims of one
+// (token, KV head) row: each 16-bit value is divided by the cache scale in
+// fp32 (round to nearest) and rounded to the nearest 8-bit code (ties to
+// even, saturating).  K bytes go to the row [block][head][slot][:]; V bytes
+// to the dims-first chunk [block][head][dim][slot].
+template <bool BF16, bool E5M2>
+__global__ void __launch_bounds__(256)
+pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                  const int64_t* __restrict__ slots, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                  Append8Args a) {
+    const int groups = a.D / 16;
+    const long long total = (long long)a.T * a.Hkv * groups;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int grp = (int)(idx % groups);
+        const long long rest = idx / groups;
+        const int h = (int)(rest % a.Hkv);
+        const long long i = rest / a.Hkv;
+        const long long slot = __ldg(slots + i);
+        if (slot < 0) continue;
+        if (slot >= a.num_slots) {
+            if (h == 0 && grp == 0 && a.err) atomicOr(a.err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const long long blk = slot / a.BS;
+        const int off = (int)(slot - blk * a.BS);
+        const long long src = (i * a.Hkv + h) * a.D + 16 * grp;
+        auto widen = [](uint16_t x) -> float {
+            if constexpr (BF16) return __uint_as_float((uint32_t)x << 16);
+            return __half2float(__ushort_as_half(x));
+        };
+        uint16_t kv[16], vv[16];
+        {
+            const uint4 k0 = __ldg(reinterpret_cast<const uint4*>(k_new + src));
+            const uint4 k1 = __ldg(reinterpret_cast<const uint4*>(k_new + src + 8));
+            const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(v_new + src));
+            const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(v_new + src + 8));
+            const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+            const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                kv[2 * j] = (uint16_t)(kw[j] & 0xffffu);
+                kv[2 * j + 1] = (uint16_t)(kw[j] >> 16);
+                vv[2 * j] = (uint16_t)(vw[j] & 0xffffu);
+                vv[2 * j + 1] = (uint16_t)(vw[j] >> 16);
+            }
+        }
+        uint32_t kq[4];
+        uint8_t vq[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint16_t kp = f32x2_to_fp8x2<E5M2>(__fdiv_rn(widen(kv[2 * j]), a.k_scale),
+                                                     __fdiv_rn(widen(kv[2 * j + 1]), a.k_scale));
+            const uint16_t vp = f32x2_to_fp8x2<E5M2>(__fdiv_rn(widen(vv[2 * j]), a.v_scale),
+                                                     __fdiv_rn(widen(vv[2 * j + 1]), a.v_scale));
+            if (j & 1) kq[j >> 1] |= (uint32_t)kp << 16; else kq[j >> 1] = kp;
+            vq[2 * j] = (uint8_t)(vp & 0xffu);
+            vq[2 * j + 1] = (uint8_t)(vp >> 8);
+        }
+        uint8_t* kdst = k_pool + ((blk * a.Hkv + h) * a.BS + off) * a.D + 16 * grp;
+        *reinterpret_cast<uint4*>(kdst) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+        uint8_t* vdst = v_pool + ((blk * a.Hkv + h) * a.D + 16 * grp) * a.BS + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) vdst[(long long)j * a.BS] = vq[j];
+    }
+}
+
+cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool, void* v_pool,
+                           const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms) {
+    const long long total = (long long)a.T * a.Hkv * (a.D / 16);
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    auto kn = static_cast<const uint16_t*>(k_new);
+    auto vn = static_cast<const uint16_t*>(v_new);
+    auto kp = static_cast<uint8_t*>(k_pool);
+    auto vp = static_cast<uint8_t*>(v_pool);
+    if (bf16) {
+        if (e5m2) pa_append8_kernel<true, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+        else pa_append8_kernel<true, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+    } else {
+        if (e5m2) pa_append8_kernel<false, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+        else pa_append8_kernel<false, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t append_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool,

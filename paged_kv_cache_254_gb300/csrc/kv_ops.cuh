@@ -22,6 +22,15 @@ struct CopyArgs {
     uint32_t* err;
 };
 
+struct Append8Args {
+    int32_t T, Hkv, D, BS;
+    long long num_slots;
+    float k_scale, v_scale;
+    uint32_t* err;
+};
+
+cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool, void* v_pool,
+                           const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms);
 cudaError_t append_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool,
                           void* v_pool, const AppendArgs& a, cudaStream_t stream, int sms);
 cudaError_t copy_launch(const int32_t* pairs, void* k_pool, void* v_pool, const CopyArgs& a,

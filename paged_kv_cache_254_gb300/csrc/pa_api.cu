@@ -47,13 +47,23 @@ int log2_exact(int g) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+int elem_bytes(int dtype) {
+    switch (dtype) {
+        case PA_FP16:
+        case PA_BF16: return 2;
+        case PA_FP8_E4M3:
+        case PA_FP8_E5M2: return 1;
+        default: return 0;
+    }
+}
+
 // Checks shared by all entry points (fields every call uses).
 pa_status check_common(const pa_shape* s) {
     if (!s) return PA_ERR_INVALID_ARG;
     if (s->num_kv_heads <= 0 || s->head_dim <= 0 || s->block_size <= 0 || s->num_blocks <= 0)
         return PA_ERR_INVALID_ARG;
-    if (s->dtype != PA_FP16 && s->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-    if (s->head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;   // 16-byte rows
+    if (elem_bytes(s->dtype) == 0) return PA_ERR_INVALID_ARG;
+    if ((s->head_dim * elem_bytes(s->dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;   // 16-byte rows
     if ((long long)s->num_blocks * s->num_kv_heads * s->block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -61,6 +71,7 @@ pa_status check_common(const pa_shape* s) {
 pa_status pick_decode(const pa_shape* s, const DecodeKernelInfo** out) {
     pa_status st = check_common(s);
     if (st != PA_OK) return st;
+    if (s->dtype != PA_FP16 && s->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (s->num_seqs < 0 || s->num_q_heads <= 0 || s->max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
     if (s->num_q_heads % s->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if ((long long)s->max_blocks_per_seq * s->block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
@@ -123,6 +134,41 @@ int current_sms() {
     return sms;
 }
 
+
+const DecodeKernelInfo* pick_decode8(const pa_shape* s, int kv_format) {
+    static const auto tab = [] {
+        struct T { DecodeKernelInfo bf[2][2][5], fp[2][2][5]; } x;
+        decode8_table_bf16(x.bf);
+        decode8_table_fp16(x.fp);
+        return x;
+    }();
+    const int lg = log2_exact(s->num_q_heads / s->num_kv_heads);
+    const int f = kv_format == PA_FP8_E5M2 ? 1 : 0;
+    const int b = s->block_size == 32 ? 1 : 0;
+    return s->dtype == PA_BF16 ? &tab.bf[f][b][lg] : &tab.fp[f][b][lg];
+}
+
+// The 8-bit K pool as a 2-D tensor of bytes: rows (block, kv head, slot) x d.
+bool pool_map8(CUtensorMap* m, const void* pool, const pa_shape* s) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
+                                (cuuint64_t)s->num_blocks * s->num_kv_heads * s->block_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim};
+    const cuuint32_t box[2] = {128, (cuuint32_t)s->block_size};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+pa_status check_fp8(const pa_shape* s, int kv_format, float k_scale, float v_scale) {
+    if (kv_format != PA_FP8_E4M3 && kv_format != PA_FP8_E5M2) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if (s->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
 
 const PrefixKernelInfo& pick_prefix(const pa_shape* s) {
     static const auto tab = [] {
@@ -202,6 +248,7 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     L.p.MB = shape->max_blocks_per_seq;
     L.p.scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
     L.p.timeout_ns = kTimeoutNs;
+    L.p.v_scale = 1.0f;
     L.stream = static_cast<cudaStream_t>(stream);
     L.grid = ctas;
     // Arrival counters start at zero for every call (the region may hold
@@ -302,9 +349,101 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     L.p.MB = shape->max_blocks_per_seq;
     L.p.scale_log2 = scale_log2;
     L.p.timeout_ns = kTimeoutNs;
+    L.p.v_scale = 1.0f;
     L.stream = strm;
     L.grid = dec;
     return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_fp8_workspace_bytes(const pa_shape* shape, int32_t kv_format) {
+    const DecodeKernelInfo* k16 = nullptr;
+    if (pick_decode(shape, &k16) != PA_OK || check_fp8(shape, kv_format, 1.f, 1.f) != PA_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int ctas = pick_decode8(shape, kv_format)->max_ctas(dev);
+    if (ctas <= 0) return 0;
+    return counters_bytes(shape) + partials_bytes(shape, ctas);
+}
+
+pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* k_pool,
+                        const void* v_pool, const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, void* out, void* workspace, size_t workspace_bytes,
+                        uint32_t* err_word, void* stream) {
+    const DecodeKernelInfo* k16 = nullptr;
+    pa_status st = pick_decode(shape, &k16);
+    if (st != PA_OK) return st;
+    st = check_fp8(shape, kv_format, k_scale, v_scale);
+    if (st != PA_OK) return st;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->num_seqs == 0) return PA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    const DecodeKernelInfo* k = pick_decode8(shape, kv_format);
+    const int ctas = k->max_ctas(dev);
+    if (ctas <= 0) return PA_ERR_CUDA;
+    const size_t need = counters_bytes(shape) + partials_bytes(shape, ctas);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    CUtensorMap mk;
+    if (!pool_map8(&mk, k_pool, shape)) return PA_ERR_CUDA;
+
+    DecodeLaunch L{};
+    L.tmap_k = &mk;
+    L.tmap_v = &mk;   // V chunks are bulk-copied from p.v8
+    L.p.q = static_cast<const uint16_t*>(q);
+    L.p.block_tables = block_tables;
+    L.p.context_lens = context_lens;
+    L.p.out = static_cast<uint16_t*>(out);
+    L.p.counters = static_cast<int32_t*>(workspace);
+    L.p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counters_bytes(shape));
+    L.p.err = err_word;
+    L.p.v8 = static_cast<const uint8_t*>(v_pool);
+    L.p.v_scale = v_scale;
+    L.p.N = shape->num_seqs;
+    L.p.Hq = shape->num_q_heads;
+    L.p.Hkv = shape->num_kv_heads;
+    L.p.NB = shape->num_blocks;
+    L.p.MB = shape->max_blocks_per_seq;
+    // K's scale folds into the scores: s = scale * k_scale * <q, code>
+    L.p.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+    L.p.timeout_ns = kTimeoutNs;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.grid = ctas;
+    if (cudaMemsetAsync(workspace, 0, counters_bytes(shape), L.stream) != cudaSuccess) return PA_ERR_CUDA;
+    return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_append_kv_fp8(const pa_shape* shape, int32_t kv_format, int32_t num_tokens, const void* k_new,
+                           const void* v_new, const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                           float k_scale, float v_scale, uint32_t* err_word, void* stream) {
+    pa_status st = check_common(shape);
+    if (st != PA_OK) return st;
+    if (elem_bytes(shape->dtype) != 2 || num_tokens < 0) return PA_ERR_INVALID_ARG;
+    st = check_fp8(shape, kv_format, k_scale, v_scale);
+    if (st != PA_OK) return st;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    Append8Args a;
+    a.T = num_tokens;
+    a.Hkv = shape->num_kv_heads;
+    a.D = shape->head_dim;
+    a.BS = shape->block_size;
+    a.num_slots = (long long)shape->num_blocks * shape->block_size;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.err = err_word;
+    return append8_launch(k_new, v_new, slot_mapping, k_pool, v_pool, a, shape->dtype == PA_BF16,
+                          kv_format == PA_FP8_E5M2, static_cast<cudaStream_t>(stream), sms) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 pa_status pa_append_kv(const pa_shape* shape, int32_t num_tokens, const void* k_new, const void* v_new,
@@ -312,7 +451,7 @@ pa_status pa_append_kv(const pa_shape* shape, int32_t num_tokens, const void* k_
                        void* stream) {
     pa_status st = check_common(shape);
     if (st != PA_OK) return st;
-    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (elem_bytes(shape->dtype) != 2 || num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
     if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
@@ -345,7 +484,7 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
     if (sms <= 0) return PA_ERR_CUDA;
     CopyArgs a;
     a.n = num_pairs;
-    a.vec_per_block = (long long)shape->num_kv_heads * shape->block_size * shape->head_dim * 2 / 16;
+    a.vec_per_block = (long long)shape->num_kv_heads * shape->block_size * shape->head_dim * elem_bytes(shape->dtype) / 16;
     a.NB = shape->num_blocks;
     a.err = err_word;
     return copy_launch(src_dst_pairs, k_pool, v_pool, a, static_cast<cudaStream_t>(stream), sms) == cudaSuccess

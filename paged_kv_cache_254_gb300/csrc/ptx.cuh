@@ -75,6 +75,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory (16-byte aligned, size a
+// multiple of 16); completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
@@ -150,6 +158,39 @@ __device__ __forceinline__ float hi_of(uint32_t v) {
         asm("{\n\t.reg .f16 h;\n\tmov.b32 {_, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));
         return f;
     }
+}
+
+// Two 8-bit float codes (low byte = first element) -> two fp16 values, exact.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    if constexpr (E5M2) {
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(v));
+    } else {
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    }
+    return r;
+}
+
+// Two floats -> two 8-bit float codes (low byte = first), round to nearest
+// even, finite values beyond the format's range saturate.
+template <bool E5M2>
+__device__ __forceinline__ uint16_t f32x2_to_fp8x2(float lo, float hi) {
+    uint16_t r;
+    if constexpr (E5M2) {
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    } else {
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    }
+    return r;
+}
+
+// A bf16 pair -> an fp16 pair (through fp32; exact inside fp16's normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {

@@ -89,7 +89,7 @@ def test_append_and_copy_checks(lib):
     assert lib.pa_copy_blocks(ctypes.byref(s), FAKE, -2, FAKE, FAKE, NULL, NULL) == 1
     assert lib.pa_copy_blocks(ctypes.byref(s), NULL, 0, NULL, NULL, NULL, NULL) == 0
     assert lib.pa_copy_blocks(ctypes.byref(s), NULL, 4, FAKE, FAKE, NULL, NULL) == 1
-    bad = shape(dtype=3)
+    bad = shape(dtype=7)
     assert lib.pa_copy_blocks(ctypes.byref(bad), FAKE, 1, FAKE, FAKE, NULL, NULL) == 1
     assert lib.pa_read_error(NULL, NULL) == 1
 
@@ -104,3 +104,28 @@ def test_product_path_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(_lib, "library_path", lambda: "/nonexistent/libpa.so")
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _lib.load()
+
+
+def test_fp8_entry_point_checks(lib):
+    s = shape(head_dim=128, num_q_heads=8, num_kv_heads=2)
+    f = ctypes.c_float
+
+    def dec(sh, fmt=2, ks=1.0, vs=1.0, q=FAKE):
+        return lib.pa_decode_fp8(ctypes.byref(sh), fmt, q, FAKE, FAKE, FAKE, FAKE, f(0.1), f(ks), f(vs), FAKE,
+                                 FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+    assert dec(s, fmt=0) == 1                      # a 16-bit code is not an 8-bit format
+    assert dec(s, ks=0.0) == 1 and dec(s, vs=float("inf")) == 1
+    assert dec(shape(head_dim=64)) == 2            # 8-bit cache rows must be 128 bytes
+    assert dec(shape(head_dim=128, dtype=2)) == 1  # queries must be 16-bit
+    assert dec(s, q=NULL) == 1
+    assert dec(shape(head_dim=128, num_seqs=0)) == 0
+
+    def app(sh, fmt=2, n=4, ks=1.0):
+        return lib.pa_append_kv_fp8(ctypes.byref(sh), fmt, n, FAKE, FAKE, FAKE, FAKE, FAKE, f(ks), f(1.0), NULL,
+                                    NULL)
+    assert app(s, fmt=5) == 1 and app(s, ks=-1.0) == 1 and app(s, n=-1) == 1
+    assert app(shape(head_dim=128, dtype=3)) == 1  # new values must be 16-bit
+    assert app(s, n=0) == 0
+    # 16-bit entry points refuse an 8-bit dtype
+    assert lib.pa_append_kv(ctypes.byref(shape(dtype=2)), 1, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 1
+    assert decode_status(lib, shape(dtype=2)) == 1

@@ -94,3 +94,13 @@ def test_representable_values_survive_the_8_bit_cache():
     a = decode_ref(q, kf, vf, np.array([row]), np.array([ctx]), 0.3)
     b = decode_ref(q, kc, vc, np.array([row]), np.array([ctx]), 0.3)
     np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_array_quantizer_equals_the_scalar_rule(fmt):
+    r = np.random.Generator(np.random.PCG64(3))
+    x = np.concatenate([r.standard_normal(3000) * 10 ** r.uniform(-4, 3, 3000),
+                        [0.0, -0.0, 1.0625, 1.1875, 3 * 2.0 ** -10, 1e6, -1e6, 447.9, 448.0, 464.0, 480.0]])
+    x = x.astype(np.float32)
+    want = np.array([encode_value(float(v), fmt) for v in x], dtype=np.uint8)
+    np.testing.assert_array_equal(quantize(x, 1.0, fmt), want)

@@ -14,6 +14,7 @@ from .synth import (  # noqa: F401
     DecodeCase,
     SamplingConfig,
     SamplingCase,
+    make_codes,
     make_decode_case,
     make_sampling_case,
     make_values,

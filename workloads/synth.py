@@ -318,3 +318,11 @@ def sampling_tables(case: SamplingCase):
         tables[i, :len(row)] = row
     ctx = (cfg.prompt_len + case.tails.astype(np.int64) + 1).astype(np.int32)
     return tables, ctx
+
+
+def make_codes(shape, gen: torch.Generator, device, below: int = 0x50) -> torch.Tensor:
+    """Random 8-bit codes: a uniform magnitude byte in [0, below) and a
+    random top (sign) bit, as uint8.  Used to fill 8-bit caches directly."""
+    mag = torch.randint(0, below, shape, generator=gen, device=device, dtype=torch.int32)
+    sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32)
+    return (mag | (sign << 7)).to(torch.uint8)
