@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3", "fp8_e5m2"], default="bf16",
+                    help="cache element type (fp8: 8-bit cache, quantising append, 8-bit decode)")
     ap.add_argument("--plain-decode", action="store_true",
                     help="decode shared-prompt batches without the prefix-aware pass")
     ap.add_argument("--num-seqs", type=int, default=None,
@@ -73,20 +75,21 @@ def parse_args(argv=None):
 
 
 # --------------------------------------------------------------------------- accounting
-def decode_bytes(ctx, Hq, Hkv, d, B, elem=2) -> int:
+def decode_bytes(ctx, Hq, Hkv, d, B, elem=2, q_elem=2) -> int:
     """Bytes the method must move for one decode call: every cached K and V
-    element once, Q and O once, the block-table entries in use and the
-    context lengths."""
+    element once (elem bytes each), Q and O once, the block-table entries in
+    use and the context lengths."""
     ctx = [int(c) for c in ctx]
     kv = sum(ctx) * Hkv * d * elem * 2
-    qo = 2 * len(ctx) * Hq * d * elem
+    qo = 2 * len(ctx) * Hq * d * q_elem
     tables = sum(-(-c // B) for c in ctx) * 4
     return kv + qo + tables + 4 * len(ctx)
 
 
-def append_bytes(T, Hkv, d, elem=2) -> int:
-    """K and V rows read and written, plus the int64 slots."""
-    return 2 * T * Hkv * d * elem * 2 + 8 * T
+def append_bytes(T, Hkv, d, elem=2, new_elem=2) -> int:
+    """K and V rows read (new_elem bytes each) and written to the cache (elem
+    bytes each), plus the int64 slots."""
+    return T * Hkv * d * (elem + new_elem) * 2 + 8 * T
 
 
 def copy_bytes(n, Hkv, B, d, elem=2) -> int:
@@ -179,7 +182,7 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 
 # --------------------------------------------------------------------------- workload
-def unique_decode_bytes(tables, ctx, Hq, Hkv, d, B, elem=2) -> int:
+def unique_decode_bytes(tables, ctx, Hq, Hkv, d, B, elem=2, q_elem=2) -> int:
     """Like decode_bytes, but each physical block's valid tokens count once
     however many sequences share it (the shared-prompt workload)."""
     filled = {}
@@ -189,11 +192,14 @@ def unique_decode_bytes(tables, ctx, Hq, Hkv, d, B, elem=2) -> int:
             b = int(row[i])
             filled[b] = max(filled.get(b, 0), min(B, n - i * B))
     kv = sum(filled.values()) * Hkv * d * elem * 2
-    qo = 2 * len(ctx) * Hq * d * elem
+    qo = 2 * len(ctx) * Hq * d * q_elem
     return kv + qo + sum(-(-int(c) // B) for c in ctx) * 4 + 4 * len(ctx)
 
 
-def make_workload(name, device, seed, num_seqs=None) -> dict:
+FP8_SCALE = 0.25
+
+
+def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
     """Device tensors of one decode step.  Block tables, lengths, slot mapping
     and copy list come from the host BlockManager (seeded random placement);
     values from the seeded workload generators."""
@@ -243,6 +249,16 @@ def make_workload(name, device, seed, num_seqs=None) -> dict:
     gstarts, gprefix = bm.shared_prefix_groups(seqs)
     slots = slots.astype(np.int64)
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    if kv_dtype != "bf16":
+        # an 8-bit cache of random codes (K rows [B][d], V chunks dims-first)
+        from workloads import make_codes
+        g8 = torch.Generator(device=device).manual_seed((seed or 0) + 99)
+        NB, Hkv_, B_, d_ = case.k_pool.shape
+        case.k_pool = None
+        case.v_pool = None
+        torch.cuda.empty_cache()
+        case.k_pool = make_codes((NB, Hkv_, B_, d_), g8, device)
+        case.v_pool = make_codes((NB, Hkv_, d_, B_), g8, device)
     return {
         "name": name, "description": desc, "Hq": Hq, "Hkv": Hkv, "d": d, "B": B,
         "num_blocks": case.num_blocks, "scale": case.scale,
@@ -250,7 +266,7 @@ def make_workload(name, device, seed, num_seqs=None) -> dict:
         "tables_h": tables, "ctx_h": ctx, "slots_h": slots, "copies_h": copies,
         "tables": to(tables), "ctx": to(ctx), "slots": to(slots), "copies": to(copies),
         "host_block_manager_ms": host_ms, "bm_stats": bm.stats(),
-        "shared": name == SAMPLING.name,
+        "shared": name == SAMPLING.name, "kv_dtype": kv_dtype,
         "group_starts": to(gstarts), "group_prefix": to(gprefix), "n_groups": int(gprefix.size),
     }
 
@@ -364,25 +380,36 @@ def gpu_arm(args):
     _build.build()
 
     seed = None if args.seed is None and rank == 0 else (args.seed or 0) + 1000 * rank
-    st = make_workload(args.config, device, seed, args.num_seqs)
+    st = make_workload(args.config, device, seed, args.num_seqs, args.kv_dtype)
     Hq, Hkv, d, B = st["Hq"], st["Hkv"], st["d"], st["B"]
     N = len(st["ctx_h"])
     T = int(st["slots_h"].shape[0])
     stream = torch.cuda.current_stream(device)
     out = torch.empty_like(st["q"])
-    ws = pa.workspace_for(st["q"], st["k_pool"], st["tables"])
+    fp8 = args.kv_dtype != "bf16"
+    fmt = args.kv_dtype[4:] if fp8 else None
+    ws = None if fp8 else pa.workspace_for(st["q"], st["k_pool"], st["tables"])
     n_copies = int(st["copies"].shape[0])
-    use_prefix = st["n_groups"] > 0 and not args.plain_decode
+    use_prefix = st["n_groups"] > 0 and not args.plain_decode and not fp8
 
     def step(q, k_new, v_new, slots, tables, ctx, ev=None):
         launches = 0
         if n_copies:
-            pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
+            if fp8:
+                pa.pa_copy_blocks_fp8(st["copies"], st["k_pool"], st["v_pool"], kv_format=fmt)
+            else:
+                pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
             launches += 1
-        pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
+        if fp8:
+            pa.pa_append_kv_fp8(k_new, v_new, slots, st["k_pool"], st["v_pool"], FP8_SCALE, FP8_SCALE, kv_format=fmt)
+        else:
+            pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
             ev[0].record(stream)
-        if use_prefix:
+        if fp8:
+            pa.pa_decode_fp8(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], FP8_SCALE, FP8_SCALE,
+                             kv_format=fmt, out=out)
+        elif use_prefix:
             pa.pa_decode_shared_prefix(q, st["k_pool"], st["v_pool"], tables, ctx, st["group_starts"],
                                        st["group_prefix"], st["scale"], out=out)
             launches += 1
@@ -449,9 +476,10 @@ def gpu_arm(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, device)
 
     # ---- numbers ----
-    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B)
-    ubytes = unique_decode_bytes(st["tables_h"], st["ctx_h"], Hq, Hkv, d, B) if st["shared"] else dbytes
-    extra = append_bytes(T, Hkv, d) + copy_bytes(n_copies, Hkv, B, d)
+    kv_elem = 1 if fp8 else 2
+    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem)
+    ubytes = unique_decode_bytes(st["tables_h"], st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem) if st["shared"] else dbytes
+    extra = append_bytes(T, Hkv, d, elem=kv_elem) + copy_bytes(n_copies, Hkv, B, d, elem=kv_elem)
     step_bytes = ubytes + extra
     value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
     tokens = world * args.steps * N / (max_ms * 1e-3)
@@ -463,7 +491,7 @@ def gpu_arm(args):
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None else None
+    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not fp8 else None
 
     if rank != 0:
         return
@@ -475,21 +503,23 @@ def gpu_arm(args):
                "mean_context": float(np.mean(st["ctx_h"])), "appended_tokens": T, "cow_copies": n_copies,
                "bytes_per_step": step_bytes,
                "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
-               "parallelism": f"replicas x{world}", "truncated_batch": args.num_seqs}
+               "parallelism": f"replicas x{world}", "truncated_batch": args.num_seqs,
+               "kv_cache": args.kv_dtype}
     if st["shared"]:
         cfg_out["bytes_note"] = ("value counts each shared physical block once (unique bytes); "
                                  "logical_gbs counts every sequence's reads")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not fp8 else f"bf16 q/out, {fmt} cache",
         "data": "synthetic (seeded N(0,1) values, random block placement)",
         "config": cfg_out,
         "tokens_per_s": round(tokens, 1),
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_prefix_kernel + pa_decode_kernel" if use_prefix else "pa_decode_kernel",
+                     "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
+                                "pa_decode_kernel (8-bit cache)" if fp8 else "pa_decode_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},
