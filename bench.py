@@ -250,15 +250,15 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
     slots = slots.astype(np.int64)
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     if kv_dtype != "bf16":
-        # an 8-bit cache of random codes (K rows [B][d], V chunks dims-first)
+        # an 8-bit cache of random codes: per (block, head) K rows, then V dims-first
         from workloads import make_codes
         g8 = torch.Generator(device=device).manual_seed((seed or 0) + 99)
         NB, Hkv_, B_, d_ = case.k_pool.shape
         case.k_pool = None
         case.v_pool = None
         torch.cuda.empty_cache()
-        case.k_pool = make_codes((NB, Hkv_, B_, d_), g8, device)
-        case.v_pool = make_codes((NB, Hkv_, d_, B_), g8, device)
+        case.k_pool = make_codes((NB, Hkv_, 2, B_, d_), g8, device)   # the one 8-bit pool
+        case.v_pool = None
     return {
         "name": name, "description": desc, "Hq": Hq, "Hkv": Hkv, "d": d, "B": B,
         "num_blocks": case.num_blocks, "scale": case.scale,
@@ -396,19 +396,18 @@ def gpu_arm(args):
         launches = 0
         if n_copies:
             if fp8:
-                pa.pa_copy_blocks_fp8(st["copies"], st["k_pool"], st["v_pool"], kv_format=fmt)
+                pa.pa_copy_blocks_fp8(st["copies"], st["k_pool"], kv_format=fmt)
             else:
                 pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
             launches += 1
         if fp8:
-            pa.pa_append_kv_fp8(k_new, v_new, slots, st["k_pool"], st["v_pool"], FP8_SCALE, FP8_SCALE, kv_format=fmt)
+            pa.pa_append_kv_fp8(k_new, v_new, slots, st["k_pool"], FP8_SCALE, FP8_SCALE, kv_format=fmt)
         else:
             pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
             ev[0].record(stream)
         if fp8:
-            pa.pa_decode_fp8(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], FP8_SCALE, FP8_SCALE,
-                             kv_format=fmt, out=out)
+            pa.pa_decode_fp8(q, st["k_pool"], tables, ctx, st["scale"], FP8_SCALE, FP8_SCALE, kv_format=fmt, out=out)
         elif use_prefix:
             pa.pa_decode_shared_prefix(q, st["k_pool"], st["v_pool"], tables, ctx, st["group_starts"],
                                        st["group_prefix"], st["scale"], out=out)

@@ -51,7 +51,7 @@ typedef enum pa_status {
 
 /* Element types.  PA_FP16 / PA_BF16: queries, outputs, new keys and values,
  * and the 16-bit cache.  PA_FP8_E4M3 / PA_FP8_E5M2: the 8-bit cache formats
- * (kv_format arguments, and shape->dtype of pa_copy_blocks on an 8-bit pool). */
+ * (kv_format arguments of the *_fp8 entry points). */
 typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2, PA_FP8_E5M2 = 3 } pa_dtype;
 
 /* Bits ORed into *err_word by the kernels. */
@@ -123,32 +123,37 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
  * (ontq "AI Inference Serving at Scale", section 6; the vLLM deployment
  * script on thewebvale, section 5, names fp8_e5m2 as a cache dtype).
  * kv_format: PA_FP8_E4M3 (OCP E4M3, largest 448, no infinities) or
- * PA_FP8_E5M2.  A pool stores code(x / scale) with one fp32 scale per pool
- * (k_scale for K, v_scale for V), rounded to nearest even and saturated.
- * Layout: k_pool bytes [NB][Hkv][B][d] (as the 16-bit cache); v_pool bytes
- * [NB][Hkv][d][B] -- each (block, head) chunk dims-first.  Supported:
- * head_dim 128, B in {16, 32}, g in {1, 2, 4, 8, 16}, q and out fp16/bf16.
+ * PA_FP8_E5M2.  The cache stores code(x / scale) with one fp32 scale for K
+ * (k_scale) and one for V (v_scale), rounded to nearest even and saturated.
+ * Layout: ONE pool of bytes [NB][Hkv][2][B * d]; each (block, KV head) piece
+ * holds its B K rows ([B][d]) and then its V dims-first ([d][B]), so a piece
+ * is one contiguous 2 * B * d bytes.  Supported: head_dim 128, B in {16, 32},
+ * g in {1, 2, 4, 8, 16}, q and out fp16/bf16.
  *
  * pa_append_kv_fp8: quantize k_new / v_new (shape->dtype, [T][Hkv][d]) into
- * the pools at slot_mapping (negative skips; past the pool: PA_DEVERR_SLOT).
- * pa_decode_fp8: pa_decode over the 8-bit pools, i.e. attention over
+ * the pool at slot_mapping (negative skips; past the pool: PA_DEVERR_SLOT).
+ * pa_decode_fp8: pa_decode over the 8-bit pool, i.e. attention over
  * K = k_scale * decode(code), V = v_scale * decode(code).  It computes in fp16
  * on the tensor cores: q is rounded to fp16 (exact inside fp16's normal
  * range), codes convert to fp16 exactly, accumulation is fp32.  Its workspace
- * is sized by pa_decode_fp8_workspace_bytes.  Copies of 8-bit blocks go
- * through pa_copy_blocks with shape->dtype = kv_format.
+ * is sized by pa_decode_fp8_workspace_bytes.
+ * pa_copy_blocks_fp8: copy-on-write copies of whole blocks (all pieces) of
+ * the 8-bit pool, as pa_copy_blocks; shape->dtype is the pool's kv_format.
  */
 size_t pa_decode_fp8_workspace_bytes(const pa_shape* shape, int32_t kv_format);
 
-pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* k_pool,
-                        const void* v_pool, const int32_t* block_tables, const int32_t* context_lens,
-                        float scale, float k_scale, float v_scale, void* out, void* workspace,
+pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* kv_pool,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, void* out, void* workspace,
                         size_t workspace_bytes, uint32_t* err_word, void* stream);
 
 pa_status pa_append_kv_fp8(const pa_shape* shape, int32_t kv_format, int32_t num_tokens,
                            const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                           void* k_pool, void* v_pool, float k_scale, float v_scale,
-                           uint32_t* err_word, void* stream);
+                           void* kv_pool, float k_scale, float v_scale, uint32_t* err_word,
+                           void* stream);
+
+pa_status pa_copy_blocks_fp8(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs,
+                             void* kv_pool, uint32_t* err_word, void* stream);
 
 /*
  * Prefix-aware paged decode: the same results as pa_decode (up to rounding

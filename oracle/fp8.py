@@ -112,16 +112,29 @@ def dequantize(codes, scale: float, fmt: str) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# The 8-bit cache.  Reading taken for the layout: K codes as the 16-bit cache,
-# [blocks][kv heads][B][d]; V codes with each (block, head) chunk stored dims
-# first, [blocks][kv heads][d][B] (the pages fix no layout).
+# The 8-bit cache.  Reading taken for the layout (the pages fix none): one
+# pool of bytes [blocks][kv heads][2][B * d]; for each (block, head) the first
+# half holds K codes token-major ([B][d], as the 16-bit cache) and the second
+# half V codes dims-first ([d][B]), so the whole piece is contiguous.
 # ---------------------------------------------------------------------------
 
-def append_fp8_ref(k_codes, v_codes, k_new, v_new, slot_mapping, block_size, k_scale, v_scale, fmt):
-    """New (k_codes, v_codes) with row i of k_new / v_new (16-bit values
-    [T, Hkv, d]) quantized into slot slot_mapping[i]; negative slots skip."""
-    k = np.array(k_codes, copy=True)
-    v = np.array(v_codes, copy=True)
+def split_pool(kv_codes, block_size):
+    """(K codes [NB][Hkv][B][d], V codes [NB][Hkv][d][B]) views of a pool."""
+    kv = np.asarray(kv_codes)
+    if kv.ndim == 5:                         # [NB][Hkv][2][B][d] byte view of the same pool
+        kv = kv.reshape(kv.shape[0], kv.shape[1], 2, -1)
+    NB, Hkv, two, n = kv.shape
+    d = n // block_size
+    return kv[:, :, 0].reshape(NB, Hkv, block_size, d), kv[:, :, 1].reshape(NB, Hkv, d, block_size)
+
+
+def append_fp8_ref(kv_codes, k_new, v_new, slot_mapping, block_size, k_scale, v_scale, fmt):
+    """New pool with row i of k_new / v_new (16-bit values [T, Hkv, d])
+    quantized into slot slot_mapping[i]; negative slots skip."""
+    kv = np.array(kv_codes, copy=True)
+    if kv.ndim == 5:
+        kv = kv.reshape(kv.shape[0], kv.shape[1], 2, -1)
+    k, v = split_pool(kv, block_size)
     kn = np.asarray(k_new, dtype=np.float32)
     vn = np.asarray(v_new, dtype=np.float32)
     for i, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
@@ -130,11 +143,10 @@ def append_fp8_ref(k_codes, v_codes, k_new, v_new, slot_mapping, block_size, k_s
         blk, off = int(slot) // block_size, int(slot) % block_size
         k[blk, :, off, :] = quantize(kn[i], k_scale, fmt)
         v[blk, :, :, off] = quantize(vn[i], v_scale, fmt)
-    return k, v
+    return kv
 
 
-def dequantized_pools(k_codes, v_codes, k_scale, v_scale, fmt):
-    """fp64 pools in the 16-bit cache's layout [blocks][kv heads][B][d]."""
-    k = dequantize(k_codes, k_scale, fmt)
-    v = dequantize(np.swapaxes(np.asarray(v_codes), 2, 3), v_scale, fmt)
-    return k, v
+def dequantized_pools(kv_codes, block_size, k_scale, v_scale, fmt):
+    """fp64 K and V pools in the 16-bit cache's layout [blocks][kv heads][B][d]."""
+    k, v = split_pool(kv_codes, block_size)
+    return dequantize(k, k_scale, fmt), dequantize(np.swapaxes(v, 2, 3), v_scale, fmt)

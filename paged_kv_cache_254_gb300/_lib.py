@@ -25,7 +25,8 @@ DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
            "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
-           "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8")
+           "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8",
+           "pa_copy_blocks_fp8")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -94,10 +95,12 @@ def load() -> ctypes.CDLL:
         F = ctypes.c_float
         lib.pa_decode_fp8_workspace_bytes.argtypes = [SP, I32]
         lib.pa_decode_fp8_workspace_bytes.restype = SZ
-        lib.pa_decode_fp8.argtypes = [SP, I32, P, P, P, P, P, F, F, F, P, P, SZ, P, P]
+        lib.pa_decode_fp8.argtypes = [SP, I32, P, P, P, P, F, F, F, P, P, SZ, P, P]
         lib.pa_decode_fp8.restype = I32
-        lib.pa_append_kv_fp8.argtypes = [SP, I32, I32, P, P, P, P, P, F, F, P, P]
+        lib.pa_append_kv_fp8.argtypes = [SP, I32, I32, P, P, P, P, F, F, P, P]
         lib.pa_append_kv_fp8.restype = I32
+        lib.pa_copy_blocks_fp8.argtypes = [SP, P, I32, P, P, P]
+        lib.pa_copy_blocks_fp8.restype = I32
         _lib = lib
         return lib
 

@@ -53,7 +53,7 @@ struct DecodeParams {
     // shared prefixes (first_blocks == null: none)
     const int32_t* first_blocks;  // [N] blocks already covered by the prefix pass
     const float* carry;           // [N][Hq][D + 2] prefix states (o, m, l)
-    const uint8_t* v8;            // 8-bit cache only: the V pool, chunks dims-first
+    const uint8_t* kv8;           // 8-bit cache only: the pool (K rows, then dims-first V, per piece)
     float v_scale;                // multiplies the output (V's cache scale; 1 for 16-bit)
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
@@ -70,9 +70,10 @@ struct DecodeTraits : Geom<D_, BS_, KVF_ ? 1 : 2> {
     static constexpr bool E5M2 = KVF_ == 2;
     static constexpr int NC = 4;                            // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
+    static constexpr int MIN_CTAS = 2;
     static constexpr int RING_TARGET = 64 * 1024;
     static constexpr int STAGES =
-        (RING_TARGET / Gm::STAGE_BYTES) > 16 ? 16 : (RING_TARGET / Gm::STAGE_BYTES);
+        ((RING_TARGET / Gm::STAGE_BYTES) > 16 ? 16 : (RING_TARGET / Gm::STAGE_BYTES)) / 4 * 4;
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
     static constexpr int OSTRIDE = D_ + 4;                  // padded scratch row (bank spread)
     static constexpr int PSTRIDE = D_ + 2;                  // state row: o[D], m, l
@@ -132,7 +133,7 @@ __device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodePa
 }
 
 template <class Tr>
-__global__ void __launch_bounds__(Tr::THREADS, 2)
+__global__ void __launch_bounds__(Tr::THREADS, Tr::MIN_CTAS)
 pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const DecodeParams p) {
     using Gm = typename Tr::Gm;
@@ -282,8 +283,10 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                             const int y = (id * p.Hkv + it.kvh) * BS;
                             const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
                             if constexpr (Tr::KV8) {
-                                tma_load_2d(kdst, &tmap_k, 0, y, fb);
-                                bulk_load(kdst + Gm::CHUNK_BYTES, p.v8 + (size_t)y * D, Gm::CHUNK_BYTES, fb);
+                                // one contiguous piece per (block, head): BS K rows of
+                                // 128 bytes, then the dims-first V (BS more rows' worth)
+                                tma_load_2d(kdst, &tmap_k, 0, 2 * y, fb);
+                                bulk_load(kdst + Gm::CHUNK_BYTES, p.kv8 + (size_t)(2 * y + BS) * D, Gm::CHUNK_BYTES, fb);
                             } else {
 #pragma unroll
                                 for (int h = 0; h < Gm::HALVES; ++h) {

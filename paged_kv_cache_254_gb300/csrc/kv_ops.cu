@@ -57,11 +57,15 @@ pa_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k_pool, ui
         }
         if (src == dst) continue;
         const uint4* ks = k_pool + (long long)src * a.vec_per_block;
-        const uint4* vs = v_pool + (long long)src * a.vec_per_block;
         uint4* kd = k_pool + (long long)dst * a.vec_per_block;
-        uint4* vd = v_pool + (long long)dst * a.vec_per_block;
         const long long step = (long long)gridDim.x * blockDim.x;
         long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+        if (v_pool == nullptr) {   // a single pool (the 8-bit cache)
+            for (; v < a.vec_per_block; v += step) kd[v] = ks[v];
+            continue;
+        }
+        const uint4* vs = v_pool + (long long)src * a.vec_per_block;
+        uint4* vd = v_pool + (long long)dst * a.vec_per_block;
         // four vectors of K and four of V in flight per thread
         for (; v + 3 * step < a.vec_per_block; v += 4 * step) {
             uint4 k0 = ks[v], k1 = ks[v + step], k2 = ks[v + 2 * step], k3 = ks[v + 3 * step];
@@ -79,13 +83,12 @@ pa_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k_pool, ui
 // Quantising append for the 8-bit cache.  One thread per 16 head dims of one
 // (token, KV head) row: each 16-bit value is divided by the cache scale in
 // fp32 (round to nearest) and rounded to the nearest 8-bit code (ties to
-// even, saturating).  K bytes go to the row [block][head][slot][:]; V bytes
-// to the dims-first chunk [block][head][dim][slot].
+// even, saturating).  Each (block, head) piece of the pool holds BS K rows
+// of D bytes and then the dims-first V ([D][BS] bytes).
 template <bool BF16, bool E5M2>
 __global__ void __launch_bounds__(256)
 pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
-                  const int64_t* __restrict__ slots, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
-                  Append8Args a) {
+                  const int64_t* __restrict__ slots, uint8_t* __restrict__ kv_pool, Append8Args a) {
     const int groups = a.D / 16;
     const long long total = (long long)a.T * a.Hkv * groups;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -135,15 +138,16 @@ pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict
             vq[2 * j] = (uint8_t)(vp & 0xffu);
             vq[2 * j + 1] = (uint8_t)(vp >> 8);
         }
-        uint8_t* kdst = k_pool + ((blk * a.Hkv + h) * a.BS + off) * a.D + 16 * grp;
+        uint8_t* piece = kv_pool + (blk * a.Hkv + h) * 2 * a.BS * a.D;
+        uint8_t* kdst = piece + (long long)off * a.D + 16 * grp;
         *reinterpret_cast<uint4*>(kdst) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-        uint8_t* vdst = v_pool + ((blk * a.Hkv + h) * a.D + 16 * grp) * a.BS + off;
+        uint8_t* vdst = piece + (long long)a.BS * a.D + (long long)(16 * grp) * a.BS + off;
 #pragma unroll
         for (int j = 0; j < 16; ++j) vdst[(long long)j * a.BS] = vq[j];
     }
 }
 
-cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool, void* v_pool,
+cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
                            const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms) {
     const long long total = (long long)a.T * a.Hkv * (a.D / 16);
     long long blocks = (total + 255) / 256;
@@ -152,14 +156,13 @@ cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* 
     if (blocks < 1) blocks = 1;
     auto kn = static_cast<const uint16_t*>(k_new);
     auto vn = static_cast<const uint16_t*>(v_new);
-    auto kp = static_cast<uint8_t*>(k_pool);
-    auto vp = static_cast<uint8_t*>(v_pool);
+    auto kv = static_cast<uint8_t*>(kv_pool);
     if (bf16) {
-        if (e5m2) pa_append8_kernel<true, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
-        else pa_append8_kernel<true, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+        if (e5m2) pa_append8_kernel<true, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
+        else pa_append8_kernel<true, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
     } else {
-        if (e5m2) pa_append8_kernel<false, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
-        else pa_append8_kernel<false, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kp, vp, a);
+        if (e5m2) pa_append8_kernel<false, true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
+        else pa_append8_kernel<false, false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
     }
     return cudaGetLastError();
 }

@@ -29,7 +29,7 @@ struct Append8Args {
     uint32_t* err;
 };
 
-cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool, void* v_pool,
+cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
                            const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms);
 cudaError_t append_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool,
                           void* v_pool, const AppendArgs& a, cudaStream_t stream, int sms);

@@ -148,12 +148,13 @@ const DecodeKernelInfo* pick_decode8(const pa_shape* s, int kv_format) {
     return s->dtype == PA_BF16 ? &tab.bf[f][b][lg] : &tab.fp[f][b][lg];
 }
 
-// The 8-bit K pool as a 2-D tensor of bytes: rows (block, kv head, slot) x d.
+// The 8-bit pool as a 2-D tensor of 128-byte rows: per (block, kv head), BS
+// K rows and then BS rows' worth of dims-first V; boxes of BS rows x 128.
 bool pool_map8(CUtensorMap* m, const void* pool, const pa_shape* s) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
-                                (cuuint64_t)s->num_blocks * s->num_kv_heads * s->block_size};
+                                (cuuint64_t)s->num_blocks * s->num_kv_heads * 2 * s->block_size};
     const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim};
     const cuuint32_t box[2] = {128, (cuuint32_t)s->block_size};
     const cuuint32_t estr[2] = {1, 1};
@@ -167,6 +168,7 @@ pa_status check_fp8(const pa_shape* s, int kv_format, float k_scale, float v_sca
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
         return PA_ERR_INVALID_ARG;
     if (s->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if ((long long)s->num_blocks * s->num_kv_heads * s->block_size * 2 >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
@@ -365,18 +367,18 @@ size_t pa_decode_fp8_workspace_bytes(const pa_shape* shape, int32_t kv_format) {
     return counters_bytes(shape) + partials_bytes(shape, ctas);
 }
 
-pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* k_pool,
-                        const void* v_pool, const int32_t* block_tables, const int32_t* context_lens, float scale,
-                        float k_scale, float v_scale, void* out, void* workspace, size_t workspace_bytes,
-                        uint32_t* err_word, void* stream) {
+pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* kv_pool,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale, float k_scale,
+                        float v_scale, void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                        void* stream) {
     const DecodeKernelInfo* k16 = nullptr;
     pa_status st = pick_decode(shape, &k16);
     if (st != PA_OK) return st;
     st = check_fp8(shape, kv_format, k_scale, v_scale);
     if (st != PA_OK) return st;
-    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    if (!q || !kv_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4))
         return PA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if (shape->num_seqs == 0) return PA_OK;
@@ -388,11 +390,11 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     const size_t need = counters_bytes(shape) + partials_bytes(shape, ctas);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
     CUtensorMap mk;
-    if (!pool_map8(&mk, k_pool, shape)) return PA_ERR_CUDA;
+    if (!pool_map8(&mk, kv_pool, shape)) return PA_ERR_CUDA;
 
     DecodeLaunch L{};
     L.tmap_k = &mk;
-    L.tmap_v = &mk;   // V chunks are bulk-copied from p.v8
+    L.tmap_v = &mk;   // V halves are bulk-copied from p.kv8
     L.p.q = static_cast<const uint16_t*>(q);
     L.p.block_tables = block_tables;
     L.p.context_lens = context_lens;
@@ -400,7 +402,7 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     L.p.counters = static_cast<int32_t*>(workspace);
     L.p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counters_bytes(shape));
     L.p.err = err_word;
-    L.p.v8 = static_cast<const uint8_t*>(v_pool);
+    L.p.kv8 = static_cast<const uint8_t*>(kv_pool);
     L.p.v_scale = v_scale;
     L.p.N = shape->num_seqs;
     L.p.Hq = shape->num_q_heads;
@@ -417,17 +419,16 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
 }
 
 pa_status pa_append_kv_fp8(const pa_shape* shape, int32_t kv_format, int32_t num_tokens, const void* k_new,
-                           const void* v_new, const int64_t* slot_mapping, void* k_pool, void* v_pool,
-                           float k_scale, float v_scale, uint32_t* err_word, void* stream) {
+                           const void* v_new, const int64_t* slot_mapping, void* kv_pool, float k_scale,
+                           float v_scale, uint32_t* err_word, void* stream) {
     pa_status st = check_common(shape);
     if (st != PA_OK) return st;
     if (elem_bytes(shape->dtype) != 2 || num_tokens < 0) return PA_ERR_INVALID_ARG;
     st = check_fp8(shape, kv_format, k_scale, v_scale);
     if (st != PA_OK) return st;
     if (num_tokens == 0) return PA_OK;
-    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PA_ERR_INVALID_ARG;
-    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
-        !aligned(slot_mapping, 8))
+    if (!k_new || !v_new || !slot_mapping || !kv_pool) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_pool, 16) || !aligned(slot_mapping, 8))
         return PA_ERR_INVALID_ARG;
     const int sms = current_sms();
     if (sms <= 0) return PA_ERR_CUDA;
@@ -440,7 +441,7 @@ pa_status pa_append_kv_fp8(const pa_shape* shape, int32_t kv_format, int32_t num
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.err = err_word;
-    return append8_launch(k_new, v_new, slot_mapping, k_pool, v_pool, a, shape->dtype == PA_BF16,
+    return append8_launch(k_new, v_new, slot_mapping, kv_pool, a, shape->dtype == PA_BF16,
                           kv_format == PA_FP8_E5M2, static_cast<cudaStream_t>(stream), sms) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -472,11 +473,30 @@ pa_status pa_append_kv(const pa_shape* shape, int32_t num_tokens, const void* k_
                : PA_ERR_CUDA;
 }
 
+pa_status pa_copy_blocks_fp8(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs,
+                             void* kv_pool, uint32_t* err_word, void* stream) {
+    pa_status st = check_common(shape);
+    if (st != PA_OK) return st;
+    if ((shape->dtype != PA_FP8_E4M3 && shape->dtype != PA_FP8_E5M2) || num_pairs < 0) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_dst_pairs || !kv_pool || !aligned(kv_pool, 16) || !aligned(src_dst_pairs, 4)) return PA_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    CopyArgs a;
+    a.n = num_pairs;
+    a.vec_per_block = (long long)shape->num_kv_heads * 2 * shape->block_size * shape->head_dim / 16;   // bytes / 16
+    a.NB = shape->num_blocks;
+    a.err = err_word;
+    return copy_launch(src_dst_pairs, kv_pool, nullptr, a, static_cast<cudaStream_t>(stream), sms) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs, void* k_pool,
                          void* v_pool, uint32_t* err_word, void* stream) {
     pa_status st = check_common(shape);
     if (st != PA_OK) return st;
-    if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+    if (elem_bytes(shape->dtype) != 2 || num_pairs < 0) return PA_ERR_INVALID_ARG;
     if (num_pairs == 0) return PA_OK;
     if (!src_dst_pairs || !k_pool || !v_pool) return PA_ERR_INVALID_ARG;
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(src_dst_pairs, 4)) return PA_ERR_INVALID_ARG;
@@ -484,7 +504,7 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
     if (sms <= 0) return PA_ERR_CUDA;
     CopyArgs a;
     a.n = num_pairs;
-    a.vec_per_block = (long long)shape->num_kv_heads * shape->block_size * shape->head_dim * elem_bytes(shape->dtype) / 16;
+    a.vec_per_block = (long long)shape->num_kv_heads * shape->block_size * shape->head_dim * 2 / 16;
     a.NB = shape->num_blocks;
     a.err = err_word;
     return copy_launch(src_dst_pairs, k_pool, v_pool, a, static_cast<cudaStream_t>(stream), sms) == cudaSuccess

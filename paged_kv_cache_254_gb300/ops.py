@@ -219,33 +219,32 @@ def _shared_workspace(device, need, stream=None):
 KV_FORMATS = {"e4m3": _lib.PA_FP8_E4M3, "e5m2": _lib.PA_FP8_E5M2}
 
 
-def _fp8_shape(q_or_new_dtype, k_pool, num_seqs=0, num_q_heads=1, max_blocks=1):
-    NB, Hkv, B, d = k_pool.shape
-    return make_shape(num_seqs, num_q_heads, Hkv, d, B, NB, max_blocks, q_or_new_dtype)
+def _need_pool8(kv_pool):
+    _need_cuda("kv_pool", kv_pool, torch.uint8)
+    if kv_pool.dim() != 5 or kv_pool.shape[2] != 2:
+        raise ValueError("kv_pool must be uint8 [NB, Hkv, 2, B, d] (the V half stored dims-first)")
+    return kv_pool.shape[0], kv_pool.shape[1], kv_pool.shape[3], kv_pool.shape[4]
 
 
-def pa_decode_fp8(q, k_pool, v_pool, block_tables, context_lens, scale, k_scale, v_scale, kv_format="e4m3",
-                  out=None, workspace=None, err=None, stream=None):
-    """Decode over an 8-bit cache (see include/pa.h): k_pool uint8 [NB, Hkv, B, d],
-    v_pool uint8 [NB, Hkv, d, B] (chunks dims-first)."""
+def pa_decode_fp8(q, kv_pool, block_tables, context_lens, scale, k_scale, v_scale, kv_format="e4m3", out=None,
+                  workspace=None, err=None, stream=None):
+    """Decode over the 8-bit cache (see include/pa.h)."""
     _need_cuda("q", q)
-    _need_cuda("k_pool", k_pool, torch.uint8)
-    _need_cuda("v_pool", v_pool, torch.uint8)
     _need_cuda("block_tables", block_tables, torch.int32)
     _need_cuda("context_lens", context_lens, torch.int32)
-    N, Hq, d = q.shape
-    NB, Hkv, B, dk = k_pool.shape
-    if dk != d or v_pool.shape != (NB, Hkv, d, B) or block_tables.shape[0] != N:
-        raise ValueError("q [N, Hq, d], k_pool [NB, Hkv, B, d], v_pool [NB, Hkv, d, B]")
+    NB, Hkv, B, d = _need_pool8(kv_pool)
+    N, Hq, dq = q.shape
+    if dq != d or block_tables.shape[0] != N:
+        raise ValueError("q [N, Hq, d] and kv_pool [NB, Hkv, 2, B, d] disagree")
     out = torch.empty_like(q) if out is None else out
     fmt = KV_FORMATS[kv_format]
-    shape = _fp8_shape(q.dtype, k_pool, N, Hq, block_tables.shape[1])
+    shape = make_shape(N, Hq, Hkv, d, B, NB, block_tables.shape[1], q.dtype)
     lib = _lib.load()
     with torch.cuda.device(q.device):
         if workspace is None:
             need = int(lib.pa_decode_fp8_workspace_bytes(ctypes.byref(shape), fmt))
             workspace = _shared_workspace(q.device, max(need, 1), stream)
-        st = lib.pa_decode_fp8(ctypes.byref(shape), fmt, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+        st = lib.pa_decode_fp8(ctypes.byref(shape), fmt, _ptr(q), _ptr(kv_pool), _ptr(block_tables),
                                _ptr(context_lens), ctypes.c_float(scale), ctypes.c_float(k_scale),
                                ctypes.c_float(v_scale), _ptr(out), _ptr(workspace),
                                ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(err),
@@ -254,33 +253,30 @@ def pa_decode_fp8(q, k_pool, v_pool, block_tables, context_lens, scale, k_scale,
     return out
 
 
-def pa_append_kv_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale, kv_format="e4m3", err=None,
+def pa_append_kv_fp8(k_new, v_new, slot_mapping, kv_pool, k_scale, v_scale, kv_format="e4m3", err=None,
                      stream=None):
-    """Quantize k_new / v_new [T, Hkv, d] (fp16/bf16) into the 8-bit pools."""
+    """Quantize k_new / v_new [T, Hkv, d] (fp16/bf16) into the 8-bit pool."""
     _need_cuda("k_new", k_new)
     _need_cuda("v_new", v_new, k_new.dtype)
-    _need_cuda("k_pool", k_pool, torch.uint8)
-    _need_cuda("v_pool", v_pool, torch.uint8)
     _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    NB, Hkv, B, d = _need_pool8(kv_pool)
     T = slot_mapping.shape[0]
-    shape = _fp8_shape(k_new.dtype, k_pool)
-    with torch.cuda.device(k_pool.device):
-        st = _lib.load().pa_append_kv_fp8(ctypes.byref(shape), KV_FORMATS[kv_format], ctypes.c_int32(T), _ptr(k_new),
-                                          _ptr(v_new), _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool),
+    shape = make_shape(0, 1, Hkv, d, B, NB, 1, k_new.dtype)
+    with torch.cuda.device(kv_pool.device):
+        st = _lib.load().pa_append_kv_fp8(ctypes.byref(shape), KV_FORMATS[kv_format], ctypes.c_int32(T),
+                                          _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(kv_pool),
                                           ctypes.c_float(k_scale), ctypes.c_float(v_scale), _ptr(err),
-                                          _stream(k_pool.device, stream))
+                                          _stream(kv_pool.device, stream))
     _lib.check(st, "pa_append_kv_fp8")
 
 
-def pa_copy_blocks_fp8(src_dst_pairs, k_pool, v_pool, kv_format="e4m3", err=None, stream=None):
-    """Copy-on-write copies of whole blocks of an 8-bit cache."""
-    _need_cuda("k_pool", k_pool, torch.uint8)
-    _need_cuda("v_pool", v_pool, torch.uint8)
+def pa_copy_blocks_fp8(src_dst_pairs, kv_pool, kv_format="e4m3", err=None, stream=None):
+    """Copy-on-write copies of whole blocks of the 8-bit pool."""
     _need_cuda("src_dst_pairs", src_dst_pairs, torch.int32)
-    NB, Hkv, B, d = k_pool.shape
+    NB, Hkv, B, d = _need_pool8(kv_pool)
     shape = _lib.PaShape(0, 1, Hkv, d, B, NB, 1, KV_FORMATS[kv_format])
-    with torch.cuda.device(k_pool.device):
-        st = _lib.load().pa_copy_blocks(ctypes.byref(shape), _ptr(src_dst_pairs),
-                                        ctypes.c_int32(src_dst_pairs.shape[0]), _ptr(k_pool), _ptr(v_pool),
-                                        _ptr(err), _stream(k_pool.device, stream))
-    _lib.check(st, "pa_copy_blocks")
+    with torch.cuda.device(kv_pool.device):
+        st = _lib.load().pa_copy_blocks_fp8(ctypes.byref(shape), _ptr(src_dst_pairs),
+                                            ctypes.c_int32(src_dst_pairs.shape[0]), _ptr(kv_pool), _ptr(err),
+                                            _stream(kv_pool.device, stream))
+    _lib.check(st, "pa_copy_blocks_fp8")

@@ -111,7 +111,7 @@ def test_fp8_entry_point_checks(lib):
     f = ctypes.c_float
 
     def dec(sh, fmt=2, ks=1.0, vs=1.0, q=FAKE):
-        return lib.pa_decode_fp8(ctypes.byref(sh), fmt, q, FAKE, FAKE, FAKE, FAKE, f(0.1), f(ks), f(vs), FAKE,
+        return lib.pa_decode_fp8(ctypes.byref(sh), fmt, q, FAKE, FAKE, FAKE, f(0.1), f(ks), f(vs), FAKE,
                                  FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
     assert dec(s, fmt=0) == 1                      # a 16-bit code is not an 8-bit format
     assert dec(s, ks=0.0) == 1 and dec(s, vs=float("inf")) == 1
@@ -121,11 +121,15 @@ def test_fp8_entry_point_checks(lib):
     assert dec(shape(head_dim=128, num_seqs=0)) == 0
 
     def app(sh, fmt=2, n=4, ks=1.0):
-        return lib.pa_append_kv_fp8(ctypes.byref(sh), fmt, n, FAKE, FAKE, FAKE, FAKE, FAKE, f(ks), f(1.0), NULL,
-                                    NULL)
+        return lib.pa_append_kv_fp8(ctypes.byref(sh), fmt, n, FAKE, FAKE, FAKE, FAKE, f(ks), f(1.0), NULL, NULL)
     assert app(s, fmt=5) == 1 and app(s, ks=-1.0) == 1 and app(s, n=-1) == 1
     assert app(shape(head_dim=128, dtype=3)) == 1  # new values must be 16-bit
     assert app(s, n=0) == 0
     # 16-bit entry points refuse an 8-bit dtype
     assert lib.pa_append_kv(ctypes.byref(shape(dtype=2)), 1, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 1
     assert decode_status(lib, shape(dtype=2)) == 1
+    # whole-block copies of the 8-bit pool take its format as shape->dtype
+    assert lib.pa_copy_blocks_fp8(ctypes.byref(shape(dtype=1)), FAKE, 1, FAKE, NULL, NULL) == 1
+    assert lib.pa_copy_blocks_fp8(ctypes.byref(shape(dtype=2)), FAKE, -1, FAKE, NULL, NULL) == 1
+    assert lib.pa_copy_blocks_fp8(ctypes.byref(shape(dtype=2)), NULL, 0, NULL, NULL, NULL) == 0
+    assert lib.pa_copy_blocks(ctypes.byref(shape(dtype=2)), FAKE, 1, FAKE, FAKE, NULL, NULL) == 1

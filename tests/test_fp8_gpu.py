@@ -37,20 +37,17 @@ def u8(t):
 def test_append_quantizes_bit_exactly(fmt, dtype, B):
     NB, Hkv, d, T = 30, 4, 128, 200
     g = torch.Generator(device="cuda").manual_seed(1)
-    k8 = make_codes((NB, Hkv, B, d), g, "cuda")
-    v8 = make_codes((NB, Hkv, d, B), g, "cuda")
+    kv = make_codes((NB, Hkv, 2, B, d), g, "cuda")
     kn = make_values((T, Hkv, d), dtype, g, "cuda") * 3
     vn = make_values((T, Hkv, d), dtype, g, "cuda")
     kn[0, 0, :4] = torch.tensor([1e4, -1e4, 1e-7, 0.0])         # saturation and underflow
     r = np.random.Generator(np.random.PCG64(2))
     slots = r.permutation(NB * B)[:T].astype(np.int64)
     slots[::9] = -1
-    want_k, want_v = append_fp8_ref(u8(k8), u8(v8), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, B,
-                                    0.25, 0.125, fmt)
-    pa().pa_append_kv_fp8(kn, vn, torch.from_numpy(slots).cuda(), k8, v8, 0.25, 0.125, kv_format=fmt)
+    want = append_fp8_ref(u8(kv), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, B, 0.25, 0.125, fmt)
+    pa().pa_append_kv_fp8(kn, vn, torch.from_numpy(slots).cuda(), kv, 0.25, 0.125, kv_format=fmt)
     torch.cuda.synchronize()
-    assert np.array_equal(u8(k8), want_k)
-    assert np.array_equal(u8(v8), want_v)
+    assert np.array_equal(u8(kv).reshape(want.shape), want)
 
 
 def fp8_case(ctx, Hq, Hkv, B, dtype, fmt, seed):
@@ -59,19 +56,18 @@ def fp8_case(ctx, Hq, Hkv, B, dtype, fmt, seed):
     case = make_decode_case(cfg, device="cuda", values=False)
     g = torch.Generator(device="cuda").manual_seed(seed)
     q = make_values((len(ctx), Hq, 128), dtype, g, "cuda")
-    k8 = make_codes((case.num_blocks, Hkv, B, 128), g, "cuda", BELOW[fmt])
-    v8 = make_codes((case.num_blocks, Hkv, 128, B), g, "cuda", BELOW[fmt])
-    return case, q, k8, v8
+    kv = make_codes((case.num_blocks, Hkv, 2, B, 128), g, "cuda", BELOW[fmt])
+    return case, q, kv
 
 
-def run(case, q, k8, v8, ks, vs, fmt, err=None):
+def run(case, q, kv, ks, vs, fmt, err=None):
     bt = torch.from_numpy(case.block_tables).cuda()
     cl = torch.from_numpy(case.context_lens).cuda()
-    return pa().pa_decode_fp8(q, k8, v8, bt, cl, case.scale, ks, vs, kv_format=fmt, err=err)
+    return pa().pa_decode_fp8(q, kv, bt, cl, case.scale, ks, vs, kv_format=fmt, err=err)
 
 
-def oracle(case, q, k8, v8, ks, vs, fmt, rows=None):
-    kf, vf = dequantized_pools(u8(k8), u8(v8), ks, vs, fmt)
+def oracle(case, q, kv, ks, vs, fmt, rows=None):
+    kf, vf = dequantized_pools(u8(kv), case.cfg.block_size, ks, vs, fmt)
     return decode_ref(q, kf, vf, case.block_tables, case.context_lens, case.scale, rows=rows)
 
 
@@ -83,39 +79,37 @@ EDGE = [1, 2, 15, 16, 17, 33, 100, 513, 1000, 3001]
 @pytest.mark.parametrize("B", [16, 32])
 @pytest.mark.parametrize("g", [1, 4, 8, 16])
 def test_decode_matches_oracle(fmt, dtype, B, g):
-    case, q, k8, v8 = fp8_case(EDGE, 2 * g, 2, B, dtype, fmt, seed=10 + g + B)
+    case, q, kv = fp8_case(EDGE, 2 * g, 2, B, dtype, fmt, seed=10 + g + B)
     err = pa().new_error_word("cuda")
-    out = run(case, q, k8, v8, 0.3, 0.5, fmt, err=err)
+    out = run(case, q, kv, 0.3, 0.5, fmt, err=err)
     assert pa().pa_read_error(err) == 0
-    assert_close(out, oracle(case, q, k8, v8, 0.3, 0.5, fmt), what=f"fp8 {fmt} {dtype} B{B} g{g}")
+    assert_close(out, oracle(case, q, kv, 0.3, 0.5, fmt), what=f"fp8 {fmt} {dtype} B{B} g{g}")
 
 
 def test_copy_blocks_of_an_8_bit_cache():
     g = torch.Generator(device="cuda").manual_seed(3)
-    k8 = make_codes((20, 8, 32, 128), g, "cuda")
-    v8 = make_codes((20, 8, 128, 32), g, "cuda")
+    kv = make_codes((20, 8, 2, 32, 128), g, "cuda")
     pairs = np.array([[2, 9], [2, 10], [5, 19]], dtype=np.int32)
-    wk, wv = copy_ref(u8(k8), u8(v8), pairs)
-    pa().pa_copy_blocks_fp8(torch.from_numpy(pairs).cuda(), k8, v8)
+    want, _ = copy_ref(u8(kv), u8(kv), pairs)
+    pa().pa_copy_blocks_fp8(torch.from_numpy(pairs).cuda(), kv)
     torch.cuda.synchronize()
-    assert np.array_equal(u8(k8), wk) and np.array_equal(u8(v8), wv)
+    assert np.array_equal(u8(kv), want)
 
 
 def test_append_then_decode():
     """The newest token of each sequence goes in through the quantising
     append; decode then reads it back from the 8-bit cache."""
     from oracle.kv_ops import slot_of
-    case, q, k8, v8 = fp8_case([40, 300, 17, 1], 16, 2, 16, "bf16", "e4m3", seed=5)
+    case, q, kv = fp8_case([40, 300, 17, 1], 16, 2, 16, "bf16", "e4m3", seed=5)
     g = torch.Generator(device="cuda").manual_seed(6)
     kn = make_values((4, 2, 128), "bf16", g, "cuda")
     vn = make_values((4, 2, 128), "bf16", g, "cuda")
     slots = np.array([slot_of(case.block_tables[s], int(case.context_lens[s]) - 1, 16) for s in range(4)],
                      dtype=np.int64)
-    wk, wv = append_fp8_ref(u8(k8), u8(v8), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, 16, 0.2,
-                            0.4, "e4m3")
-    pa().pa_append_kv_fp8(kn, vn, torch.from_numpy(slots).cuda(), k8, v8, 0.2, 0.4)
-    out = run(case, q, k8, v8, 0.2, 0.4, "e4m3")
-    kf, vf = dequantized_pools(wk, wv, 0.2, 0.4, "e4m3")
+    want = append_fp8_ref(u8(kv), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, 16, 0.2, 0.4, "e4m3")
+    pa().pa_append_kv_fp8(kn, vn, torch.from_numpy(slots).cuda(), kv, 0.2, 0.4)
+    out = run(case, q, kv, 0.2, 0.4, "e4m3")
+    kf, vf = dequantized_pools(want, 16, 0.2, 0.4, "e4m3")
     assert_close(out, decode_ref(q, kf, vf, case.block_tables, case.context_lens, case.scale), what="append+decode")
 
 
@@ -124,23 +118,20 @@ def test_llama3_70b_shape_full_size_sampled():
     case = make_decode_case(cfg, device="cuda", values=False)
     g = torch.Generator(device="cuda").manual_seed(cfg.seed)
     q = make_values((cfg.num_seqs, 64, 128), "bf16", g, "cuda")
-    k8 = make_codes((case.num_blocks, 8, 16, 128), g, "cuda")
-    v8 = make_codes((case.num_blocks, 8, 128, 16), g, "cuda")
-    out = run(case, q, k8, v8, 0.25, 0.25, "e4m3")
+    kv = make_codes((case.num_blocks, 8, 2, 16, 128), g, "cuda")
+    out = run(case, q, kv, 0.25, 0.25, "e4m3")
     assert torch.isfinite(out.float()).all()
     r = np.random.Generator(np.random.PCG64(7))
     rows = sorted({(int(s), int(h)) for s in r.integers(0, cfg.num_seqs, 8) for h in r.integers(0, 64, 2)})
-    kf_rows = oracle_rows(case, q, k8, v8, rows)
+    kf_rows = oracle_rows(case, q, kv, rows)
     assert_close(out, kf_rows, rows=rows, what="fp8 llama3_70b_b256")
 
 
-def oracle_rows(case, q, k8, v8, rows):
+def oracle_rows(case, q, kv, rows):
     """Dequantise only the blocks the sampled rows read."""
-    from oracle.fp8 import dequantize
     need = sorted({int(b) for s, _ in rows for b in case.block_tables[s][:-(-int(case.context_lens[s]) // 16)]})
     remap = {b: i for i, b in enumerate(need)}
     idx = torch.tensor(need, device="cuda")
-    kf = dequantize(u8(k8.index_select(0, idx)), 0.25, "e4m3")
-    vf = np.swapaxes(dequantize(u8(v8.index_select(0, idx)), 0.25, "e4m3"), 2, 3)
+    kf, vf = dequantized_pools(u8(kv.index_select(0, idx)), 16, 0.25, 0.25, "e4m3")
     tables = np.vectorize(lambda b: remap.get(int(b), -1))(case.block_tables)
     return decode_ref(q, kf, vf, tables, case.context_lens, case.scale, rows=rows)

@@ -52,24 +52,26 @@ def test_quantize_divides_by_the_scale_in_fp32():
 
 
 def test_append_then_dequantize_returns_the_quantized_rows():
-    from oracle.fp8 import append_fp8_ref, dequantized_pools
+    from oracle.fp8 import append_fp8_ref, dequantized_pools, split_pool
     from oracle.attention import gather_sequence
     r = np.random.Generator(np.random.PCG64(1))
     NB, Hkv, B, d = 6, 2, 4, 8
-    k = r.integers(0, 0x7E, size=(NB, Hkv, B, d)).astype(np.uint8)
-    v = r.integers(0, 0x7E, size=(NB, Hkv, d, B)).astype(np.uint8)
+    kv = r.integers(0, 0x7E, size=(NB, Hkv, 2, B * d)).astype(np.uint8)
     kn = r.standard_normal((3, Hkv, d)).astype(np.float32)
     vn = r.standard_normal((3, Hkv, d)).astype(np.float32)
     row = [4, 1]
     slots = [4 * 4 + 0, 1 * 4 + 3, -1]
-    k2, v2 = append_fp8_ref(k, v, kn, vn, slots, B, 0.5, 2.0, "e4m3")
-    kf, vf = dequantized_pools(k2, v2, 0.5, 2.0, "e4m3")
+    kv2 = append_fp8_ref(kv, kn, vn, slots, B, 0.5, 2.0, "e4m3")
+    kf, vf = dequantized_pools(kv2, B, 0.5, 2.0, "e4m3")
     K, V = gather_sequence(kf, vf, row, 8, 1, B)
     np.testing.assert_array_equal(K[0], dequantize(quantize(kn[0, 1], 0.5, "e4m3"), 0.5, "e4m3"))
     np.testing.assert_array_equal(V[7], dequantize(quantize(vn[1, 1], 2.0, "e4m3"), 2.0, "e4m3"))
-    # untouched slots keep their codes; V chunks are stored dims-first
-    np.testing.assert_array_equal(v2[4, :, :, 1:], v[4, :, :, 1:])
-    np.testing.assert_array_equal(np.swapaxes(v2, 2, 3)[4, 0, 0], quantize(vn[0, 0], 2.0, "e4m3"))
+    # untouched slots keep their codes; the V half of a piece is dims-first
+    k0, v0 = split_pool(kv, B)
+    k2, v2 = split_pool(kv2, B)
+    np.testing.assert_array_equal(v2[4, :, :, 1:], v0[4, :, :, 1:])
+    np.testing.assert_array_equal(v2[4, 0, :, 0], quantize(vn[0, 0], 2.0, "e4m3"))
+    np.testing.assert_array_equal(kv2[4, 0, 1, 0:B], [v2[4, 0, 0, t] for t in range(B)])
 
 
 def test_representable_values_survive_the_8_bit_cache():
@@ -84,12 +86,11 @@ def test_representable_values_survive_the_8_bit_cache():
     vc = r.choice(grid, size=(NB, Hkv, B, d)) * 4.0
     row = [3, 0, 4, 1]
     slots = [row[t // B] * B + t % B for t in range(ctx)]
-    k8 = np.zeros((NB, Hkv, B, d), np.uint8)
-    v8 = np.zeros((NB, Hkv, d, B), np.uint8)
+    kv = np.zeros((NB, Hkv, 2, B * d), np.uint8)
     kn = np.stack([kc[row[t // B], :, t % B] for t in range(ctx)])
     vn = np.stack([vc[row[t // B], :, t % B] for t in range(ctx)])
-    k8, v8 = append_fp8_ref(k8, v8, kn, vn, slots, B, 0.25, 4.0, "e4m3")
-    kf, vf = dequantized_pools(k8, v8, 0.25, 4.0, "e4m3")
+    kv = append_fp8_ref(kv, kn, vn, slots, B, 0.25, 4.0, "e4m3")
+    kf, vf = dequantized_pools(kv, B, 0.25, 4.0, "e4m3")
     q = r.standard_normal((1, 2, d))
     a = decode_ref(q, kf, vf, np.array([row]), np.array([ctx]), 0.3)
     b = decode_ref(q, kc, vc, np.array([row]), np.array([ctx]), 0.3)
