@@ -127,7 +127,9 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
  * (k_scale) and one for V (v_scale), rounded to nearest even and saturated.
  * Layout: ONE pool of bytes [NB][Hkv][2][B * d]; each (block, KV head) piece
  * holds its B K rows ([B][d]) and then its V dims-first ([d][B]), so a piece
- * is one contiguous 2 * B * d bytes.  Supported: head_dim 128, B in {16, 32},
+ * is one contiguous 2 * B * d bytes.  Within K row r the sixteen-byte parts
+ * are permuted: part c (dims 16c .. 16c + 15) sits at part position
+ * c XOR (r mod 8); the row keeps its own 128 bytes.  Supported: head_dim 128, B in {16, 32},
  * g in {1, 2, 4, 8, 16}, q and out fp16/bf16.
  *
  * pa_append_kv_fp8: quantize k_new / v_new (shape->dtype, [T][Hkv][d]) into

@@ -115,33 +115,55 @@ def dequantize(codes, scale: float, fmt: str) -> np.ndarray:
 # The 8-bit cache.  Reading taken for the layout (the pages fix none): one
 # pool of bytes [blocks][kv heads][2][B * d]; for each (block, head) the first
 # half holds K codes token-major ([B][d], as the 16-bit cache) and the second
-# half V codes dims-first ([d][B]), so the whole piece is contiguous.
+# half V codes dims-first ([d][B]), so the whole piece is contiguous.  Inside
+# the K half, each 128-byte span of a token row keeps its bytes but stores its
+# eight 16-byte pieces in a permuted order: piece c of row r sits at piece
+# position c XOR (r mod 8).  Rows whose width is not a multiple of 128 bytes
+# keep the plain order.
 # ---------------------------------------------------------------------------
 
-def split_pool(kv_codes, block_size):
-    """(K codes [NB][Hkv][B][d], V codes [NB][Hkv][d][B]) views of a pool."""
+def k_positions(block_size: int, d: int) -> np.ndarray:
+    """[B][d] index, inside a K half, of the code of (token row r, dim c)."""
+    r = np.arange(block_size)[:, None]
+    c = np.arange(d)[None, :]
+    if d % 128:
+        return r * d + c
+    return r * d + (c // 128) * 128 + 16 * (((c % 128) // 16) ^ (r % 8)) + c % 16
+
+
+def _flat(kv_codes):
     kv = np.asarray(kv_codes)
     if kv.ndim == 5:                         # [NB][Hkv][2][B][d] byte view of the same pool
         kv = kv.reshape(kv.shape[0], kv.shape[1], 2, -1)
+    return kv
+
+
+def split_pool(kv_codes, block_size):
+    """(K codes [NB][Hkv][B][d], V codes [NB][Hkv][d][B]) of a pool; K is a
+    gathered copy (the row pieces put back in order), V a view."""
+    kv = _flat(kv_codes)
     NB, Hkv, two, n = kv.shape
     d = n // block_size
-    return kv[:, :, 0].reshape(NB, Hkv, block_size, d), kv[:, :, 1].reshape(NB, Hkv, d, block_size)
+    k = kv[:, :, 0][..., k_positions(block_size, d)]
+    return k, kv[:, :, 1].reshape(NB, Hkv, d, block_size)
 
 
 def append_fp8_ref(kv_codes, k_new, v_new, slot_mapping, block_size, k_scale, v_scale, fmt):
     """New pool with row i of k_new / v_new (16-bit values [T, Hkv, d])
     quantized into slot slot_mapping[i]; negative slots skip."""
-    kv = np.array(kv_codes, copy=True)
-    if kv.ndim == 5:
-        kv = kv.reshape(kv.shape[0], kv.shape[1], 2, -1)
-    k, v = split_pool(kv, block_size)
+    kv = np.array(_flat(kv_codes), copy=True)
+    NB, Hkv, two, n = kv.shape
+    d = n // block_size
+    pos = k_positions(block_size, d)
+    v = kv[:, :, 1].reshape(NB, Hkv, d, block_size)
     kn = np.asarray(k_new, dtype=np.float32)
     vn = np.asarray(v_new, dtype=np.float32)
     for i, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
         if slot < 0:
             continue
         blk, off = int(slot) // block_size, int(slot) % block_size
-        k[blk, :, off, :] = quantize(kn[i], k_scale, fmt)
+        khalf = kv[blk, :, 0]                # [Hkv][B * d] view
+        khalf[:, pos[off]] = quantize(kn[i], k_scale, fmt)
         v[blk, :, :, off] = quantize(vn[i], v_scale, fmt)
     return kv
 

@@ -12,25 +12,41 @@
 
 namespace pa {
 
-// One (block, KV head) chunk as it sits in a ring stage: HALVES boxes of
-// BS rows x 128 bytes, 128-byte swizzled; the K chunk, then the V chunk.
-// ELEM is the byte size of a cached element (2, or 1 for the 8-bit cache,
-// whose V chunk is stored dims-first and copied as one contiguous piece).
-template <int D_, int BS_, int ELEM_ = 2>
+// One (block, KV head) chunk of the 16-bit cache as it sits in a ring stage:
+// HALVES boxes of BS rows x 128 bytes, 128-byte swizzled; the K chunk, then
+// the V chunk.  One stage holds one block.
+template <int D_, int BS_>
 struct Geom {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
-    static constexpr int ELEM = ELEM_;
-    static constexpr int HALVES = D * ELEM / 128;
+    static constexpr int HALVES = D * 2 / 128;
     static constexpr int BOX_BYTES = BS * 128;
     static constexpr int CHUNK_BYTES = HALVES * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
+    static constexpr int UB = 1;         // blocks per stage
     static constexpr int NT = BS / 8;    // 8-token n-tiles of S^T
     static constexpr int KT = BS / 16;   // 16-token k-steps of PV
     static constexpr int KD = D / 16;    // 16-dim k-steps of QK, m-tiles of PV
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(ELEM == 2 || (ELEM == 1 && D == 128), "8-bit cache rows are 128 bytes");
+};
+
+// The 8-bit cache (head_dim 128): a (block, KV head) piece is BS K rows of
+// 128 bytes (16-byte parts of row r permuted by XOR with r % 8, so a plain
+// copy lands them bank-spread) followed by the dims-first V (128 rows of BS
+// bytes), one contiguous run of PIECE_BYTES in the pool.  A ring stage holds
+// UB consecutive blocks of one (sequence, KV head) pair: 32 tokens.
+template <int BS_>
+struct Geom8 {
+    static constexpr int D = 128;
+    static constexpr int BS = BS_;
+    static constexpr int PIECE_BYTES = 2 * BS * 128;
+    static constexpr int UB = 32 / BS;
+    static constexpr int STAGE_BYTES = UB * PIECE_BYTES;
+    static constexpr int NT = 4;         // 8-token n-tiles of S^T per stage
+    static constexpr int KT = 2;         // 16-token k-steps of PV per stage
+    static constexpr int KD = D / 16;
+    static_assert(BS == 16 || BS == 32, "block_size");
 };
 
 __device__ __forceinline__ int seq_blocks(int ctx, int BS, int MB) {
@@ -226,10 +242,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-// Token order of the 8-bit path.  In n-tile nt of S^T, column n holds block
-// token perm_token(nt, n); it makes the tokens that the PV fragments pair up
-// (2 t4 + e and 2 t4 + 8 + e of a 16-token k-step) sit next to each other in
-// the dims-first V chunk, so a lane reads them with one 4-byte load.
+// Token order of the 8-bit path.  In n-tile nt of S^T, column n holds stage
+// token perm_token(nt, n) (n-tiles 0, 1: tokens 0..15; 2, 3: tokens 16..31);
+// it makes the tokens that the PV fragments pair up (2 t4 + e and
+// 2 t4 + 8 + e of a 16-token k-step) sit next to each other in the
+// dims-first V, so a lane reads them with one 4-byte load.
 __device__ __forceinline__ int perm_token(int nt, int n) {
     return 16 * (nt >> 1) + 4 * (n >> 1) + 2 * (nt & 1) + (n & 1);
 }
@@ -255,14 +272,17 @@ __device__ __forceinline__ void load_q_frags8(uint32_t (&qa)[D / 16][4], const u
     }
 }
 
-// consume_block for the 8-bit cache: K rows (BS x 128 bytes, swizzled) and
-// the dims-first V chunk (D rows x BS bytes) are turned into fp16 fragments
-// in registers; scores and PV run on the fp16 MMA.  The scales are applied
-// outside (K's inside scale_log2, V's at the final write).
+// consume_block for the 8-bit cache, over one 32-token stage at kb (Geom8
+// layout).  K rows and dims-first V are turned into fp16 fragments in
+// registers; scores and PV run on the fp16 MMA.  Tokens >= valid are masked
+// out; 16-token groups wholly past valid are skipped (their bytes may belong
+// to no copy at all), and the caller has zeroed the V bytes of the masked
+// tokens inside the last group that is used.  The scales are applied outside
+// (K's inside scale_log2, V's at the final write).
 template <class Gm, int NR, bool E5M2>
-__device__ __forceinline__ void consume_block8(uint32_t kb, uint32_t vb, int valid,
-                                               const uint32_t (&qa)[Gm::KD][4], WarpAcc<Gm::D, NR>& acc,
-                                               float scale_log2, int lane) {
+__device__ __forceinline__ void consume_stage8(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
+                                               WarpAcc<Gm::D, NR>& acc, float scale_log2, int lane) {
+    constexpr int BS = Gm::BS, PIECE = Gm::PIECE_BYTES;
     const int g = lane >> 2;
     const int t4 = lane & 3;
     float sacc[Gm::NT][4];
@@ -270,21 +290,24 @@ __device__ __forceinline__ void consume_block8(uint32_t kb, uint32_t vb, int val
     for (int nt = 0; nt < Gm::NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-        const int row = perm_token(nt, g);
-        uint32_t w[8];
-        uint32_t w0[4], w1[4];
-        lds128(kb + row * 128 + (((2 * t4) ^ (row & 7)) << 4), w0);
-        lds128(kb + row * 128 + (((2 * t4 + 1) ^ (row & 7)) << 4), w1);
+        if (16 * (nt >> 1) < valid) {
+            const int tok = perm_token(nt, g);
+            const uint32_t rb = kb + (tok / BS) * PIECE + (tok % BS) * 128;
+            uint32_t w[8];
+            uint32_t w0[4], w1[4];
+            lds128(rb + (((2 * t4) ^ (tok & 7)) << 4), w0);
+            lds128(rb + (((2 * t4 + 1) ^ (tok & 7)) << 4), w1);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w[i] = w0[i];
-            w[i + 4] = w1[i];
-        }
+            for (int i = 0; i < 4; ++i) {
+                w[i] = w0[i];
+                w[i + 4] = w1[i];
+            }
 #pragma unroll
-        for (int kk = 0; kk < Gm::KD; ++kk) {
-            const uint32_t b0 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] & 0xffffu));
-            const uint32_t b1 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] >> 16));
-            mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            for (int kk = 0; kk < Gm::KD; ++kk) {
+                const uint32_t b0 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] & 0xffffu));
+                const uint32_t b1 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] >> 16));
+                mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            }
         }
     }
 
@@ -346,11 +369,14 @@ __device__ __forceinline__ void consume_block8(uint32_t kb, uint32_t vb, int val
         }
     }
 #pragma unroll
-    for (int mt = 0; mt < Gm::KD; ++mt)
+    for (int kt = 0; kt < Gm::KT; ++kt) {
+        if (16 * kt >= valid) break;
+        // V bytes of tokens 16 kt + 4 t4 .. + 3 for dim rows g and g + 8
+        const uint32_t vb = kb + ((16 * kt) / BS) * PIECE + BS * 128 + (16 * kt) % BS + 4 * t4;
 #pragma unroll
-        for (int kt = 0; kt < Gm::KT; ++kt) {
-            const uint32_t x = lds32(vb + (16 * mt + g) * Gm::BS + 16 * kt + 4 * t4);
-            const uint32_t y = lds32(vb + (16 * mt + g + 8) * Gm::BS + 16 * kt + 4 * t4);
+        for (int mt = 0; mt < Gm::KD; ++mt) {
+            const uint32_t x = lds32(vb + (16 * mt + g) * BS);
+            const uint32_t y = lds32(vb + (16 * mt + g + 8) * BS);
             const uint32_t a0 = fp8x2_to_f16x2<E5M2>((uint16_t)(x & 0xffffu));
             const uint32_t a2 = fp8x2_to_f16x2<E5M2>((uint16_t)(x >> 16));
             const uint32_t a1 = fp8x2_to_f16x2<E5M2>((uint16_t)(y & 0xffffu));
@@ -361,14 +387,22 @@ __device__ __forceinline__ void consume_block8(uint32_t kb, uint32_t vb, int val
                 mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
             }
         }
+    }
 }
 
-// Zero the bytes of tokens >= valid in every dim row of a dims-first V chunk.
+// Zero, in a 32-token 8-bit stage, the V bytes of tokens valid .. the end of
+// valid's 16-token group (0 < valid < 32; nothing when valid is a multiple
+// of 16, since consume_stage8 skips wholly masked groups).
 template <class Gm>
-__device__ __forceinline__ void zero_v8_tail(uint32_t vb, int valid, int lane) {
-    const int w = Gm::BS - valid;
+__device__ __forceinline__ void zero_v8_tail(uint32_t kb, int valid, int lane) {
+    constexpr int BS = Gm::BS;
+    const int end = (valid + 15) & ~15;
+    const int w = end - valid;
+    if (w == 0) return;
+    const uint32_t vb = kb + (valid / BS) * Gm::PIECE_BYTES + BS * 128 + valid % BS;
     for (int i = lane; i < Gm::D * w; i += 32) {
-        const uint32_t a = vb + (i / w) * Gm::BS + valid + i % w;
+        const int dim = i / w;
+        const uint32_t a = vb + dim * BS + (i - dim * w);
         asm volatile("st.shared.u8 [%0], %1;" :: "r"(a), "h"((uint16_t)0) : "memory");
     }
 }

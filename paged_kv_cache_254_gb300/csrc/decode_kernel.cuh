@@ -38,6 +38,8 @@
 // set error bits and poison the affected rows with NaN instead of trapping.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace pa {
@@ -62,11 +64,14 @@ struct DecodeParams {
 
 // KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2.
 template <int D_, int BS_, int G_, bool BF16_, int KVF_ = 0>
-struct DecodeTraits : Geom<D_, BS_, KVF_ ? 1 : 2> {
-    using Gm = Geom<D_, BS_, KVF_ ? 1 : 2>;
+struct DecodeTraits {
+    static constexpr bool KV8 = KVF_ != 0;
+    using Gm = std::conditional_t<KV8, Geom8<BS_>, Geom<D_, BS_>>;
+    static constexpr int D = D_;
+    static constexpr int BS = BS_;
+    static constexpr int UB = Gm::UB;                       // blocks per ring stage
     static constexpr int G = G_;
     static constexpr bool BF16 = BF16_;
-    static constexpr bool KV8 = KVF_ != 0;
     static constexpr bool E5M2 = KVF_ == 2;
     static constexpr int NC = 4;                            // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;
@@ -161,9 +166,11 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         fence_mbar_init();
     }
-    if (warp == NC && lane == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
+    if constexpr (!Tr::KV8) {
+        if (warp == NC && lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
     }
 
     // ---- work range of this CTA (warp 0) ----
@@ -252,6 +259,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
     if (warp == NC) {
         // =========================== producer ===========================
+        // One ring stage per UB consecutive blocks of a segment; `issued`
+        // counts stages.  A batch of 32 table entries never splits a stage
+        // (32 is a multiple of UB).
         long long issued = 0;
         bool aborted = false;
         SegIter it = it0;
@@ -262,8 +272,11 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             for (int base = 0; base < len && !aborted; base += 32) {
                 const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
                 const int cnt = min(32, len - base);
-                for (int i = 0; i < cnt; ++i) {
-                    int id = __shfl_sync(0xffffffffu, tcur, i);
+                for (int i = 0; i < cnt; i += Tr::UB) {
+                    int ids[Tr::UB];
+#pragma unroll
+                    for (int u = 0; u < Tr::UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, i + u);
+                    const int nblk = min(Tr::UB, cnt - i);
                     int ok = 1;
                     if (lane == 0) {
                         const int st = (int)(issued % S);
@@ -272,22 +285,30 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                             if (!mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns)) ok = 0;
                         }
                         if (ok) {
-                            const bool bad = (unsigned)id >= (unsigned)p.NB;
-                            if (bad) {
-                                set_err(p.err, PA_DEVERR_BLOCK_ID);
-                                id = 0;
+                            bool bad = false;
+#pragma unroll
+                            for (int u = 0; u < Tr::UB; ++u) {
+                                if (u < nblk && (unsigned)ids[u] >= (unsigned)p.NB) {
+                                    bad = true;
+                                    ids[u] = 0;
+                                }
                             }
+                            if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
                             stage_poison[st] = bad ? 1 : 0;
                             const uint32_t fb = full0 + 8 * st;
-                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-                            const int y = (id * p.Hkv + it.kvh) * BS;
                             const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
                             if constexpr (Tr::KV8) {
-                                // one contiguous piece per (block, head): BS K rows of
-                                // 128 bytes, then the dims-first V (BS more rows' worth)
-                                tma_load_2d(kdst, &tmap_k, 0, 2 * y, fb);
-                                bulk_load(kdst + Gm::CHUNK_BYTES, p.kv8 + (size_t)(2 * y + BS) * D, Gm::CHUNK_BYTES, fb);
+                                // each block's piece is one contiguous run in the pool
+                                mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
+#pragma unroll
+                                for (int u = 0; u < Tr::UB; ++u)
+                                    if (u < nblk)
+                                        bulk_load(kdst + u * Gm::PIECE_BYTES,
+                                                  p.kv8 + ((size_t)ids[u] * p.Hkv + it.kvh) * Gm::PIECE_BYTES,
+                                                  Gm::PIECE_BYTES, fb);
                             } else {
+                                mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                                const int y = (ids[0] * p.Hkv + it.kvh) * BS;
 #pragma unroll
                                 for (int h = 0; h < Gm::HALVES; ++h) {
                                     tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
@@ -327,6 +348,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int g = lane >> 2;       // fragment row group
     const int t4 = lane & 3;       // fragment column pair
     SegIter it = it0;
+    long long ubase = 0;   // stages of the CTA before this segment
     WarpAcc<D, Tr::NR> acc;
     while (it.gi < hi) {
         const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
@@ -343,13 +365,15 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         acc.reset();
         int poisoned = 0;
 
-        // Block k of the CTA range (k = gi - lo) goes to warp k % NC.  With
-        // STAGES a multiple of NC every ring stage is owned by one warp, which
-        // consumes its fills strictly in order (no mbarrier phase aliasing).
-        int j0 = warp - (int)((it.gi - lo) % NC);
+        // Stage k of the CTA (k = ubase + u, UB blocks each) goes to warp
+        // k % NC.  With STAGES a multiple of NC every ring stage is owned by one
+        // warp, which consumes its fills strictly in order (no mbarrier phase
+        // aliasing).
+        const int nu = (len + Tr::UB - 1) / Tr::UB;
+        int j0 = warp - (int)(ubase % NC);
         if (j0 < 0) j0 += NC;
-        for (int j = j0; j < len; j += NC) {
-            const long long k = it.gi + j - lo;
+        for (int u = j0; u < nu; u += NC) {
+            const long long k = ubase + u;
             const int st = (int)(k % S);
             const uint32_t par = (uint32_t)((k / S) & 1);
             if (*(volatile int*)&info->abort) {
@@ -365,26 +389,32 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 continue;
             }
             poisoned |= stage_poison[st];
-            const int valid = min(BS, ctx - (it.first + it.b0 + j) * BS);
+            const int b = u * Tr::UB;
+            const int nblk = min(Tr::UB, len - b);
+            const int valid = min(nblk * BS, ctx - (it.first + it.b0 + b) * BS);
             const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
-            const uint32_t vb = kb + Gm::CHUNK_BYTES;
+            bool zeroed = false;
             if constexpr (Tr::KV8) {
-                if (valid < BS) {
-                    zero_v8_tail<Gm>(vb, valid, lane);
+                if (valid < 32 && (valid & 15)) {
+                    zero_v8_tail<Gm>(kb, valid, lane);
                     __syncwarp();
+                    zeroed = true;
                 }
-                consume_block8<Gm, Tr::NR, Tr::E5M2>(kb, vb, valid, qa, acc, p.scale_log2, lane);
+                consume_stage8<Gm, Tr::NR, Tr::E5M2>(kb, valid, qa, acc, p.scale_log2, lane);
             } else {
+                const uint32_t vb = kb + Gm::CHUNK_BYTES;
                 if (valid < BS) {
                     zero_v_tail<Gm>(vb, valid, lane);
                     __syncwarp();
+                    zeroed = true;
                 }
                 consume_block<Gm, Tr::NR, Tr::BF16>(kb, vb, valid, qa, acc, p.scale_log2, lane);
             }
-            if (valid < BS) fence_proxy_async_smem();
+            if (zeroed) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
         }
+        ubase += nu;
 
         // ---- merge the NC warp states of this segment ----
 #pragma unroll

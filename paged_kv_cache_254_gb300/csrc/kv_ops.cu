@@ -84,7 +84,8 @@ pa_copy_kernel(const int32_t* __restrict__ pairs, uint4* __restrict__ k_pool, ui
 // (token, KV head) row: each 16-bit value is divided by the cache scale in
 // fp32 (round to nearest) and rounded to the nearest 8-bit code (ties to
 // even, saturating).  Each (block, head) piece of the pool holds BS K rows
-// of D bytes and then the dims-first V ([D][BS] bytes).
+// of D bytes (16-byte parts permuted by XOR with the row index mod 8) and
+// then the dims-first V ([D][BS] bytes).
 template <bool BF16, bool E5M2>
 __global__ void __launch_bounds__(256)
 pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
@@ -139,7 +140,8 @@ pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict
             vq[2 * j + 1] = (uint8_t)(vp >> 8);
         }
         uint8_t* piece = kv_pool + (blk * a.Hkv + h) * 2 * a.BS * a.D;
-        uint8_t* kdst = piece + (long long)off * a.D + 16 * grp;
+        // K row `off`: 16-byte part grp stored at part position grp ^ (off % 8)
+        uint8_t* kdst = piece + (long long)off * a.D + 16 * (grp ^ (off & 7));
         *reinterpret_cast<uint4*>(kdst) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
         uint8_t* vdst = piece + (long long)a.BS * a.D + (long long)(16 * grp) * a.BS + off;
 #pragma unroll

@@ -148,21 +148,6 @@ const DecodeKernelInfo* pick_decode8(const pa_shape* s, int kv_format) {
     return s->dtype == PA_BF16 ? &tab.bf[f][b][lg] : &tab.fp[f][b][lg];
 }
 
-// The 8-bit pool as a 2-D tensor of 128-byte rows: per (block, kv head), BS
-// K rows and then BS rows' worth of dims-first V; boxes of BS rows x 128.
-bool pool_map8(CUtensorMap* m, const void* pool, const pa_shape* s) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
-                                (cuuint64_t)s->num_blocks * s->num_kv_heads * 2 * s->block_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim};
-    const cuuint32_t box[2] = {128, (cuuint32_t)s->block_size};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 pa_status check_fp8(const pa_shape* s, int kv_format, float k_scale, float v_scale) {
     if (kv_format != PA_FP8_E4M3 && kv_format != PA_FP8_E5M2) return PA_ERR_INVALID_ARG;
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
@@ -389,12 +374,13 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     if (ctas <= 0) return PA_ERR_CUDA;
     const size_t need = counters_bytes(shape) + partials_bytes(shape, ctas);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
-    CUtensorMap mk;
-    if (!pool_map8(&mk, kv_pool, shape)) return PA_ERR_CUDA;
+    // every (block, head) piece is bulk-copied from p.kv8; the tensor-map
+    // parameters of the kernel go unused
+    CUtensorMap unused{};
 
     DecodeLaunch L{};
-    L.tmap_k = &mk;
-    L.tmap_v = &mk;   // V halves are bulk-copied from p.kv8
+    L.tmap_k = &unused;
+    L.tmap_v = &unused;
     L.p.q = static_cast<const uint16_t*>(q);
     L.p.block_tables = block_tables;
     L.p.context_lens = context_lens;

@@ -105,3 +105,32 @@ def test_array_quantizer_equals_the_scalar_rule(fmt):
     x = x.astype(np.float32)
     want = np.array([encode_value(float(v), fmt) for v in x], dtype=np.uint8)
     np.testing.assert_array_equal(quantize(x, 1.0, fmt), want)
+
+
+def test_k_rows_of_128_bytes_store_permuted_pieces():
+    """d = 128: each K token row keeps its own 128 bytes, with 16-byte piece c
+    of row r at piece position c XOR (r mod 8); V stays dims-first.  The
+    round trip through the pool gives back exactly the quantized rows."""
+    from oracle.fp8 import append_fp8_ref, dequantized_pools, k_positions, split_pool
+    r = np.random.Generator(np.random.PCG64(7))
+    NB, Hkv, B, d = 3, 2, 16, 128
+    kv = np.zeros((NB, Hkv, 2, B * d), np.uint8)
+    kn = r.standard_normal((B, Hkv, d)).astype(np.float32)
+    vn = r.standard_normal((B, Hkv, d)).astype(np.float32)
+    slots = [2 * B + t for t in range(B)]
+    kv = append_fp8_ref(kv, kn, vn, slots, B, 0.5, 0.5, "e4m3")
+    raw = kv[2, 1, 0]
+    for t in (0, 1, 7, 8, 13):
+        want = quantize(kn[t, 1], 0.5, "e4m3")
+        row = raw[t * 128:(t + 1) * 128]
+        assert sorted(row.tolist()) == sorted(want.tolist())          # the row's own bytes
+        for c in range(8):
+            np.testing.assert_array_equal(row[16 * (c ^ (t % 8)):16 * (c ^ (t % 8)) + 16], want[16 * c:16 * c + 16])
+    assert sorted(k_positions(B, d).ravel().tolist()) == list(range(B * d))  # a permutation
+    np.testing.assert_array_equal(k_positions(B, 64), np.arange(B * 64).reshape(B, 64))
+    k, v = split_pool(kv, B)
+    kf, vf = dequantized_pools(kv, B, 0.5, 0.5, "e4m3")
+    for t in range(B):
+        np.testing.assert_array_equal(k[2, 1, t], quantize(kn[t, 1], 0.5, "e4m3"))
+        np.testing.assert_array_equal(v[2, 0, :, t], quantize(vn[t, 0], 0.5, "e4m3"))
+        np.testing.assert_array_equal(kf[2, 0, t], dequantize(quantize(kn[t, 0], 0.5, "e4m3"), 0.5, "e4m3"))
