@@ -261,7 +261,12 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // =========================== producer ===========================
         // One ring stage per UB consecutive blocks of a segment; `issued`
         // counts stages.  A batch of 32 table entries never splits a stage
-        // (32 is a multiple of UB).
+        // (32 is a multiple of UB).  Stages are filled in rounds: lane j
+        // probes (without blocking) whether ring stage issued + j is free,
+        // and the leading run of free stages is filled at once, one stage per
+        // lane; only when the oldest stage is still busy does lane 0 block on
+        // it.  At most S stages are probed per round, so no two lanes touch
+        // the same ring slot.
         long long issued = 0;
         bool aborted = false;
         SegIter it = it0;
@@ -272,60 +277,74 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             for (int base = 0; base < len && !aborted; base += 32) {
                 const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
                 const int cnt = min(32, len - base);
-                for (int i = 0; i < cnt; i += Tr::UB) {
+                const int nst = (cnt + Tr::UB - 1) / Tr::UB;   // stages in this batch
+                int done = 0;
+                while (done < nst) {
+                    const int want = min(nst - done, S);
+                    const long long my = issued + lane;
+                    bool is_free = false;
+                    if (lane < want)
+                        is_free = my < S || mbar_test_wait(empty0 + 8 * (uint32_t)(my % S),
+                                                           (uint32_t)(((my / S) - 1) & 1));
+                    const unsigned fm = __ballot_sync(0xffffffffu, is_free);
+                    int run = (fm == 0xffffffffu) ? 32 : __ffs(~fm) - 1;
+                    if (run == 0) {
+                        int ok = 1;
+                        if (lane == 0)
+                            ok = mbar_wait_bounded(empty0 + 8 * (uint32_t)(issued % S),
+                                                   (uint32_t)(((issued / S) - 1) & 1), p.timeout_ns) ? 1 : 0;
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) {
+                            if (lane == 0) {
+                                set_err(p.err, PA_DEVERR_TIMEOUT);
+                                *(volatile int*)&info->abort = 1;
+                            }
+                            aborted = true;
+                            break;
+                        }
+                        run = 1;
+                    }
+                    // lane j < run fills stage issued + j with batch entries (done + j) * UB ..
+                    const int first = (done + lane) * Tr::UB;
                     int ids[Tr::UB];
 #pragma unroll
-                    for (int u = 0; u < Tr::UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, i + u);
-                    const int nblk = min(Tr::UB, cnt - i);
-                    int ok = 1;
-                    if (lane == 0) {
-                        const int st = (int)(issued % S);
-                        if (issued >= S) {
-                            const uint32_t par = (uint32_t)(((issued / S) - 1) & 1);
-                            if (!mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns)) ok = 0;
+                    for (int u = 0; u < Tr::UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, (first + u) & 31);
+                    if (lane < run) {
+                        const int nblk = min(Tr::UB, cnt - first);
+                        const int st = (int)(my % S);
+                        bool bad = false;
+#pragma unroll
+                        for (int u = 0; u < Tr::UB; ++u) {
+                            if (u < nblk && (unsigned)ids[u] >= (unsigned)p.NB) {
+                                bad = true;
+                                ids[u] = 0;
+                            }
                         }
-                        if (ok) {
-                            bool bad = false;
+                        if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
+                        stage_poison[st] = bad ? 1 : 0;
+                        const uint32_t fb = full0 + 8 * st;
+                        const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
+                        if constexpr (Tr::KV8) {
+                            // each block's piece is one contiguous run in the pool
+                            mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
 #pragma unroll
-                            for (int u = 0; u < Tr::UB; ++u) {
-                                if (u < nblk && (unsigned)ids[u] >= (unsigned)p.NB) {
-                                    bad = true;
-                                    ids[u] = 0;
-                                }
-                            }
-                            if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
-                            stage_poison[st] = bad ? 1 : 0;
-                            const uint32_t fb = full0 + 8 * st;
-                            const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
-                            if constexpr (Tr::KV8) {
-                                // each block's piece is one contiguous run in the pool
-                                mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
-#pragma unroll
-                                for (int u = 0; u < Tr::UB; ++u)
-                                    if (u < nblk)
-                                        bulk_load(kdst + u * Gm::PIECE_BYTES,
-                                                  p.kv8 + ((size_t)ids[u] * p.Hkv + it.kvh) * Gm::PIECE_BYTES,
-                                                  Gm::PIECE_BYTES, fb);
-                            } else {
-                                mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-                                const int y = (ids[0] * p.Hkv + it.kvh) * BS;
-#pragma unroll
-                                for (int h = 0; h < Gm::HALVES; ++h) {
-                                    tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                                    tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-                                }
-                            }
+                            for (int u = 0; u < Tr::UB; ++u)
+                                if (u < nblk)
+                                    bulk_load(kdst + u * Gm::PIECE_BYTES,
+                                              p.kv8 + ((size_t)ids[u] * p.Hkv + it.kvh) * Gm::PIECE_BYTES,
+                                              Gm::PIECE_BYTES, fb);
                         } else {
-                            set_err(p.err, PA_DEVERR_TIMEOUT);
-                            *(volatile int*)&info->abort = 1;
+                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                            const int y = (ids[0] * p.Hkv + it.kvh) * BS;
+#pragma unroll
+                            for (int h = 0; h < Gm::HALVES; ++h) {
+                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                            }
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) {
-                        aborted = true;
-                        break;
-                    }
-                    ++issued;
+                    issued += run;
+                    done += run;
                 }
                 tcur = nxt;
             }
