@@ -88,7 +88,8 @@ struct DecodeTraits {
     static constexpr int SO_BYTES = NC * G * OSTRIDE * 4;
     static constexpr int SM_OFF = SO_OFF + SO_BYTES;        // m per (warp, head)
     static constexpr int SL_OFF = SM_OFF + NC * G * 4;      // l per (warp, head)
-    static constexpr int SP_OFF = SL_OFF + NC * G * 4;      // poison flag per warp
+    static constexpr int SH_OFF = SL_OFF + NC * G * 4;      // per head: M, L, carry factors
+    static constexpr int SP_OFF = SH_OFF + 4 * G * 4;       // poison flag per warp
     static constexpr int PS_OFF = SP_OFF + NC * 4;          // poison flag per stage
     static constexpr int BAR_OFF = ((PS_OFF + STAGES * 4) + 7) & ~7;
     static constexpr int INFO_OFF = BAR_OFF + 2 * STAGES * 8;
@@ -149,6 +150,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     float* so = reinterpret_cast<float*>(smem + Tr::SO_OFF);
     float* sm = reinterpret_cast<float*>(smem + Tr::SM_OFF);
     float* sl = reinterpret_cast<float*>(smem + Tr::SL_OFF);
+    float* sh = reinterpret_cast<float*>(smem + Tr::SH_OFF);
     int* spois = reinterpret_cast<int*>(smem + Tr::SP_OFF);
     volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::BAR_OFF);
@@ -369,18 +371,25 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     SegIter it = it0;
     long long ubase = 0;   // stages of the CTA before this segment
     WarpAcc<D, Tr::NR> acc;
+    // Q fragments (A operand of S^T = Q K^T), rows = heads of the group
+    auto load_q = [&](uint32_t (&qa)[Gm::KD][4], const SegIter& sg) {
+        const uint16_t* qrow = p.q + ((size_t)sg.s * p.Hq + (size_t)sg.kvh * G) * D;
+        const uint16_t* r0 = g < G ? qrow + g * D : nullptr;
+        const uint16_t* r1 = (G > 8) ? qrow + (g + 8) * D : nullptr;
+        if constexpr (Tr::KV8) {
+            load_q_frags8<D, Tr::BF16>(qa, r0, r1, t4);
+        } else {
+            load_q_frags<D>(qa, r0, r1, t4);
+        }
+    };
+    uint32_t qa[Gm::KD][4];
+    int ctx = 0;
+    if (it.gi < hi) {
+        ctx = __ldg(p.context_lens + it.s);
+        load_q(qa, it);
+    }
     while (it.gi < hi) {
         const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
-        const int ctx = __ldg(p.context_lens + it.s);
-
-        // Q fragments (A operand of S^T = Q K^T): rows = heads of the group.
-        const uint16_t* qrow = p.q + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
-        uint32_t qa[Gm::KD][4];
-        if constexpr (Tr::KV8) {
-            load_q_frags8<D, Tr::BF16>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
-        } else {
-            load_q_frags<D>(qa, g < G ? qrow + g * D : nullptr, (G > 8) ? qrow + (g + 8) * D : nullptr, t4);
-        }
         acc.reset();
         int poisoned = 0;
 
@@ -435,6 +444,16 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         ubase += nu;
 
+        // The next segment's position, length and Q: loaded now so that the
+        // loads overlap the merge below.
+        SegIter nx = it;
+        seg_advance(nx, len, p, BS);
+        int ctx_next = 0;
+        if (nx.gi < hi) {
+            ctx_next = __ldg(p.context_lens + nx.s);
+            load_q(qa, nx);
+        }
+
         // ---- merge the NC warp states of this segment ----
 #pragma unroll
         for (int r = 0; r < Tr::NR; ++r) {
@@ -480,31 +499,52 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         uint16_t* orow = p.out + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
         const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::PSTRIDE;
         float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * G * Tr::PSTRIDE;
+        // Per head, once: the common max M, each warp's factor exp2(m_w - M)
+        // (in place of m_w), L, and for a finished pair with a prefix state
+        // the factors that fold the carry in (the log-sum-exp rule).
+        if (tid < G) {
+            const int hd = tid;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) M = fmaxf(M, sm[w * G + hd]);
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) {
+                const float f = ex2(sm[w * G + hd] - M);
+                sm[w * G + hd] = f;
+                L += sl[w * G + hd] * f;
+            }
+            float fa = 1.f, fb = 0.f;
+            if (complete && has_carry) {
+                const float* c = crow + hd * Tr::PSTRIDE;
+                const float cm = __ldg(c + D), cl = __ldg(c + D + 1);
+                const float Mn = fmaxf(M, cm);
+                fa = ex2(M - Mn);
+                fb = ex2(cm - Mn);
+                L = L * fa + cl * fb;
+                M = Mn;
+            }
+            sh[hd] = M;
+            sh[G + hd] = L;
+            sh[2 * G + hd] = fa;
+            sh[3 * G + hd] = fb;
+        }
+        named_bar_sync(1, NC * 32);
         for (int idx = tid; idx < G * D; idx += NC * 32) {
             const int head = idx / D;
             const int dim = idx - head * D;
-            float M = -INFINITY;
+            float O = 0.f;
 #pragma unroll
-            for (int w = 0; w < NC; ++w) M = fmaxf(M, sm[w * G + head]);
-            float L = 0.f, O = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) {
-                const float f = ex2(sm[w * G + head] - M);
-                L += sl[w * G + head] * f;
-                O += so[(w * G + head) * Tr::OSTRIDE + dim] * f;
-            }
+            for (int w = 0; w < NC; ++w) O += so[(w * G + head) * Tr::OSTRIDE + dim] * sm[w * G + head];
             if (bad) O = qnan;
             if (complete) {
-                if (has_carry) {
-                    const float* c = crow + head * Tr::PSTRIDE;
-                    lse_fold(M, L, O, __ldg(c + D), __ldg(c + D + 1), __ldg(c + dim));
-                }
-                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
+                if (has_carry) O = O * sh[2 * G + head] + __ldg(crow + head * Tr::PSTRIDE + dim) * sh[3 * G + head];
+                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / sh[G + head] * p.v_scale);
             } else {
                 prow[head * Tr::PSTRIDE + dim] = O;
                 if (dim == 0) {
-                    prow[head * Tr::PSTRIDE + D] = M;
-                    prow[head * Tr::PSTRIDE + D + 1] = L;
+                    prow[head * Tr::PSTRIDE + D] = sh[head];
+                    prow[head * Tr::PSTRIDE + D + 1] = sh[G + head];
                 }
             }
         }
@@ -539,7 +579,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         }
         named_bar_sync(1, NC * 32);
-        seg_advance(it, len, p, BS);
+        it = nx;
+        ctx = ctx_next;
     }
 }
 
