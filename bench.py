@@ -416,7 +416,7 @@ def gpu_arm(args):
             pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], out=out, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
-        return launches + 2
+        return launches + 4   # append, and the decode call's pre-pass, attention and merge kernels
 
     dev_args = (st["q"], st["k_new"], st["v_new"], st["slots"], st["tables"], st["ctx"])
     for _ in range(args.warmup):

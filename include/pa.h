@@ -46,7 +46,7 @@ typedef enum pa_status {
     PA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
     PA_ERR_OUT_OF_RANGE = 4,  /* device found a bad block id, context length, slot or copy pair */
     PA_ERR_TIMEOUT = 5,       /* a device-side wait ran past its limit; the kernel gave up */
-    PA_ERR_WORKSPACE = 6      /* workspace missing or smaller than pa_decode_workspace_bytes() */
+    PA_ERR_WORKSPACE = 6      /* workspace missing, misaligned or below the shape's minimum */
 } pa_status;
 
 /* Element types.  PA_FP16 / PA_BF16: queries, outputs, new keys and values,
@@ -74,14 +74,20 @@ typedef struct pa_shape {
 } pa_shape;
 
 /*
- * Bytes of scratch that pa_decode needs for `shape` on the CURRENT device.
- * The workspace holds the per-(sequence, KV head) arrival counters and the
- * partial softmax states of sequences whose keys are split across thread
- * blocks.  It needs no initialisation: pa_decode clears the counter region on
- * `stream` (cudaMemsetAsync) before its kernel.  The same buffer can serve any
- * later call on the same stream, whatever its shape; calls that may run at the
- * same time must use different workspaces.  Returns 0 if the shape is invalid
- * or unsupported.
+ * Bytes of scratch that pa_decode prefers for `shape` on the CURRENT device.
+ * The workspace holds a work-chunk counter, the per-sequence block prefix
+ * sums that place the work chunks, and the partial
+ * softmax states of sequences whose keys are split across chunks.  It needs
+ * no initialisation: pa_decode's first launch (a one-block pre-pass on
+ * `stream`) clears the counter and writes the prefix sums; the attention
+ * kernel follows, then a merge kernel for the sequences split across chunks
+ * (three launches on `stream` in all).  A smaller
+ * workspace is accepted down to the static split's minimum (one chunk per
+ * worker warp); below the preferred size fewer chunks are balanced at run
+ * time, and results are deterministic for each workspace size.  The same
+ * buffer can serve any later call on the same stream, whatever its shape;
+ * calls that may run at the same time must use different workspaces.  Returns
+ * 0 if the shape is invalid or unsupported.
  */
 size_t pa_decode_workspace_bytes(const pa_shape* shape);
 
@@ -230,8 +236,9 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
  * a static device buffer of PA_NOALLOC_SCRATCH_BYTES inside the library, held
  * on every GPU that loads it until the process exits.  This call allocates
  * nothing.
- *  - Shapes whose pa_decode_workspace_bytes() exceeds PA_NOALLOC_SCRATCH_BYTES
- *    are rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *  - Shapes whose minimum scratch exceeds PA_NOALLOC_SCRATCH_BYTES are
+ *    rejected with PA_ERR_WORKSPACE before anything is enqueued; shapes whose
+ *    preferred scratch exceeds it run with fewer run-time balanced chunks.
  *  - The first call on a device looks up the buffer's address on that device
  *    (with it current); make that first call before any stream capture.
  *  - Every call on a device shares the one buffer and it keeps the last call's
@@ -239,7 +246,7 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
  *    overlap on the GPU -- on different streams, or unordered from different
  *    threads -- race on it and give wrong results; order them on one stream.
  */
-#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 pa_status pa_decode_noalloc(const pa_shape* shape, const void* q, const void* k_pool,
                             const void* v_pool, const int32_t* block_tables,

@@ -27,7 +27,7 @@ EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_bl
            "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
            "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8",
            "pa_copy_blocks_fp8")
-NOALLOC_SCRATCH_BYTES = 8 << 20
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class PaShape(ctypes.Structure):

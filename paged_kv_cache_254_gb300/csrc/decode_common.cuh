@@ -251,17 +251,14 @@ __device__ __forceinline__ int perm_token(int nt, int n) {
     return 16 * (nt >> 1) + 4 * (n >> 1) + 2 * (nt & 1) + (n & 1);
 }
 
-// Q fragments for the 8-bit path, in fp16, with the head dims in the order
-// the K bytes are read: k-step kk, fragment column 2 t4 + e -> dim
-// 32 t4 + 4 kk + e, column 2 t4 + 8 + e -> dim 32 t4 + 4 kk + 2 + e.
-template <int D, bool QBF16>
+// Q fragments for the 8-bit path with the head dims in the order the K bytes
+// are read: k-step kk, fragment column 2 t4 + e -> dim 32 t4 + 4 kk + e,
+// column 2 t4 + 8 + e -> dim 32 t4 + 4 kk + 2 + e.  Loaded as stored (q's
+// 16-bit type); q_frags8_to_f16 then turns bf16 pairs into fp16 pairs.
+template <int D>
 __device__ __forceinline__ void load_q_frags8(uint32_t (&qa)[D / 16][4], const uint16_t* row0,
                                               const uint16_t* row1, int t4) {
-    auto ld = [](const uint16_t* p) -> uint32_t {
-        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
-        if constexpr (QBF16) return bf16x2_to_f16x2(v);
-        return v;
-    };
+    auto ld = [](const uint16_t* p) -> uint32_t { return __ldg(reinterpret_cast<const uint32_t*>(p)); };
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const int c = 32 * t4 + 4 * kk;
@@ -269,6 +266,16 @@ __device__ __forceinline__ void load_q_frags8(uint32_t (&qa)[D / 16][4], const u
         qa[kk][2] = row0 ? ld(row0 + c + 2) : 0u;
         qa[kk][1] = row1 ? ld(row1 + c) : 0u;
         qa[kk][3] = row1 ? ld(row1 + c + 2) : 0u;
+    }
+}
+
+template <int D, bool QBF16>
+__device__ __forceinline__ void q_frags8_to_f16(uint32_t (&qa)[D / 16][4]) {
+    if constexpr (QBF16) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qa[kk][i] = bf16x2_to_f16x2(qa[kk][i]);
     }
 }
 

@@ -10,15 +10,23 @@
 // (ontq "AI Inference Serving at Scale", section 6, grouped-query attention).
 //
 // Work split.  The (sequence, KV head) pairs are laid end to end, each
-// contributing its blocks; the flattened block list is cut into gridDim.x
-// equal contiguous ranges, one per persistent CTA.  A CTA walks its range as
-// "segments" (the part of one pair that falls in the range).  A pair that lies
-// inside one CTA is finished there; a pair cut by range boundaries leaves a
-// partial softmax state (m, l, unnormalised o) per piece in the workspace, and
-// the last CTA to finish a piece of that pair (arrival counter, zeroed by the
-// host before the launch) merges them with the log-sum-exp rule in CTA order.
-// Everything about the split depends on context lengths only, never on block
-// ids, so results are bitwise independent of block placement.
+// contributing its blocks; the flattened block list is cut into contiguous
+// chunks.  A worker is one warp of a persistent CTA, and works alone: it
+// walks its chunks as "segments" (the part of one pair that falls in a
+// chunk), keeping the online-softmax state of the pair's query rows in its
+// registers.  The first three quarters of the list form one chunk per worker
+// (worker w takes chunk w); the last quarter is cut into `nd` small chunks
+// that workers claim with an atomic counter when they run out, which evens
+// out SMs that get less memory bandwidth or more segment ends than others.
+// A pair that lies inside one chunk is finished by its warp; a pair cut by
+// chunk boundaries leaves a partial state (m, l, unnormalised o) per piece in
+// the workspace, and a post-pass kernel (pa_decode_merge, one warp per pair)
+// merges the pieces with the log-sum-exp rule in chunk order, so no warp ever
+// waits on another.  Chunk boundaries depend on context lengths and the grid only, never
+// on block ids or on which warp took a chunk, so results are bitwise
+// independent of block placement and of timing.  A chunk start is found by a
+// search over per-sequence block prefix sums (written by a pre-pass kernel,
+// copied to shared memory when there are at most CUM_SMEM sequences).
 //
 // Shared prefixes (optional).  With prefix groups, the first first_blocks[s]
 // blocks of a member sequence were already reduced by the prefix kernel into
@@ -26,13 +34,13 @@
 // blocks after the prefix, and the carry joins the final log-sum-exp
 // combination.
 //
-// Inside a CTA.  Warp NC is the producer: it reads block ids from the table
-// (32 at a time, one per lane), and lane 0 issues two-dimensional TMA loads
-// (128-byte swizzle) of each (block, KV head) K chunk and V chunk into a ring
-// of shared-memory stages guarded by full/empty mbarriers.  Warps 0..NC-1 are
-// consumers: block k of the CTA range goes to warp k % NC, which folds it in
-// with consume_block() (mma.sync scores, online softmax, PV).  At the end of a
-// segment the NC warp states are merged through shared memory.
+// Inside a warp.  Each warp owns R shared-memory stages with one mbarrier
+// each.  Lane 0 issues the copies of a stage (two-dimensional TMA loads with
+// 128-byte swizzle for the 16-bit cache, one bulk copy per block piece for the
+// 8-bit cache) R stages ahead of the one being computed, and refills a stage
+// as soon as it has been folded in (consume_block / consume_stage8: mma.sync
+// scores, online softmax, PV).  Block ids come from the table 32 at a time,
+// one per lane.  No warp ever waits for another.
 //
 // Every wait is bounded (PA_DEVERR_TIMEOUT); bad block ids and context lengths
 // set error bits and poison the affected rows with NaN instead of trapping.
@@ -49,14 +57,16 @@ struct DecodeParams {
     const int32_t* block_tables;  // [N][MB]
     const int32_t* context_lens;  // [N]
     uint16_t* out;                // [N][Hq][D]
-    int32_t* counters;            // [N * Hkv], zeroed before each launch
-    float* partials;              // [gridDim.x][2][G][D + 2]
+    float* partials;              // [chunks][2][G][D + 4]
     uint32_t* err;                // may be null
     // shared prefixes (first_blocks == null: none)
     const int32_t* first_blocks;  // [N] blocks already covered by the prefix pass
     const float* carry;           // [N][Hq][D + 2] prefix states (o, m, l)
     const uint8_t* kv8;           // 8-bit cache only: the pool (K rows, then dims-first V, per piece)
     float v_scale;                // multiplies the output (V's cache scale; 1 for 16-bit)
+    const long long* cum;         // [N + 1] blocks of sequences before s (pre-pass)
+    int32_t* chunk_ctr;           // dynamic chunks claimed so far (zeroed by the pre-pass)
+    int32_t nd;                   // dynamic chunks wanted (0: the static split alone)
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
     uint64_t timeout_ns;
@@ -69,42 +79,32 @@ struct DecodeTraits {
     using Gm = std::conditional_t<KV8, Geom8<BS_>, Geom<D_, BS_>>;
     static constexpr int D = D_;
     static constexpr int BS = BS_;
-    static constexpr int UB = Gm::UB;                       // blocks per ring stage
+    static constexpr int UB = Gm::UB;                       // blocks per stage
     static constexpr int G = G_;
     static constexpr bool BF16 = BF16_;
     static constexpr bool E5M2 = KVF_ == 2;
-    static constexpr int NC = 4;                            // consumer warps
-    static constexpr int THREADS = (NC + 1) * 32;
-    static constexpr int MIN_CTAS = 2;
-    static constexpr int RING_TARGET = 64 * 1024;
-    static constexpr int STAGES =
-        ((RING_TARGET / Gm::STAGE_BYTES) > 16 ? 16 : (RING_TARGET / Gm::STAGE_BYTES)) / 4 * 4;
+    // About 192 KiB of stages per SM: stages of up to 8 KiB, two CTAs of four
+    // warps; 16 KiB stages, one CTA of six warps.
+    static constexpr int RING_PER_SM = 192 * 1024;
+    static constexpr int MIN_CTAS = Gm::STAGE_BYTES <= 8192 ? 2 : 1;
+    static constexpr int NW = MIN_CTAS == 2 ? 4 : 6;       // warps (workers) per CTA
+    static constexpr int R_FIT = RING_PER_SM / (MIN_CTAS * NW * Gm::STAGE_BYTES);
+    static constexpr int R = R_FIT > 8 ? 8 : R_FIT;        // stages per warp
+    static constexpr int THREADS = NW * 32;
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
-    static constexpr int OSTRIDE = D_ + 4;                  // padded scratch row (bank spread)
-    static constexpr int PSTRIDE = D_ + 2;                  // state row: o[D], m, l
-    // shared memory carve-up, offsets from a 1024-byte aligned base
-    static constexpr int RING_OFF = 0;
-    static constexpr int SO_OFF = STAGES * Gm::STAGE_BYTES;
-    static constexpr int SO_BYTES = NC * G * OSTRIDE * 4;
-    static constexpr int SM_OFF = SO_OFF + SO_BYTES;        // m per (warp, head)
-    static constexpr int SL_OFF = SM_OFF + NC * G * 4;      // l per (warp, head)
-    static constexpr int SH_OFF = SL_OFF + NC * G * 4;      // per head: M, L, carry factors
-    static constexpr int SP_OFF = SH_OFF + 4 * G * 4;       // poison flag per warp
-    static constexpr int PS_OFF = SP_OFF + NC * 4;          // poison flag per stage
-    static constexpr int BAR_OFF = ((PS_OFF + STAGES * 4) + 7) & ~7;
-    static constexpr int INFO_OFF = BAR_OFF + 2 * STAGES * 8;
-    static constexpr int INFO_BYTES = 64;
-    static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;  // + alignment slack
+    static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad (16-byte rows)
+    static constexpr int CSTRIDE = D_ + 2;                  // carry row (prefix pass): o[D], m, l
+    static constexpr int CUM_SMEM = 1024;                   // sequences whose prefix sums fit in smem
+    static constexpr int QN = 16;                           // open chunks per warp (> R + 1)
+    // shared memory, offsets from a 1024-byte aligned base
+    static constexpr int BAR_OFF = NW * R * Gm::STAGE_BYTES;
+    static constexpr int CUM_OFF = BAR_OFF + NW * R * 8;    // long long [CUM_SMEM + 1]
+    static constexpr int CQ_OFF = CUM_OFF + (CUM_SMEM + 1) * 8;
+    static constexpr int PS_OFF = CQ_OFF + NW * QN * 32;    // poison flag per stage
+    static constexpr int SMEM_BYTES = PS_OFF + NW * R * 4 + 1024;  // + alignment slack
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
-    static_assert(STAGES >= 2 && STAGES % NC == 0, "ring stages are owned by consumer warps");
-};
-
-// Shared CTA bookkeeping written by warp 0 before the roles split.
-struct CtaInfo {
-    long long lo, hi, W, geff;
-    int s0, kvh0, b0;
-    int abort;
-    int last;
+    static_assert(R >= 2, "two stages per warp at least");
+    static_assert(32 % UB == 0, "a batch of 32 table entries holds whole stages");
 };
 
 // Blocks of sequence s in this kernel's work list (and its first block).
@@ -138,289 +138,328 @@ __device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodePa
     }
 }
 
+__device__ __forceinline__ int seg_len(const SegIter& it, long long hi) {
+    return (int)min((long long)(it.nb - it.b0), hi - it.gi);
+}
+
+// Chunks of the flattened list: NS static ones over [0, Ws), then ND over [Ws, W).
+struct Sched {
+    long long W, Ws;
+    int NS, ND;
+    __device__ long long lo(long long c) const {
+        if (c <= NS) return range_lo(c, Ws, NS);
+        return Ws + range_lo(c - NS, W - Ws, ND);
+    }
+    __device__ long long of(long long x) const {   // the chunk holding flattened block x
+        if (x < Ws) return cta_of(x, Ws, NS);
+        return NS + cta_of(x - Ws, W - Ws, ND);
+    }
+};
+
+// The schedule of W flattened blocks over `nworkers` warps with `nd` dynamic
+// chunks wanted: the last quarter goes dynamic when every chunk can hold a
+// few blocks, else the static split alone.
+__device__ __forceinline__ Sched make_sched(long long W, long long nworkers, int nd) {
+    Sched sc;
+    sc.W = W;
+    if (nd > 0 && W >= 64 * nworkers) {
+        sc.Ws = W - W / 4;
+        sc.NS = (int)nworkers;
+        sc.ND = nd;
+    } else {
+        sc.Ws = W;
+        sc.NS = (int)(W < nworkers ? W : nworkers);
+        sc.ND = 0;
+    }
+    return sc;
+}
+
+// An open chunk, queued by the issue side for the compute side of one warp.
+struct ChunkEnt {
+    long long lo, hi;
+    int id, s, kvh, b0;
+};
+static_assert(sizeof(ChunkEnt) <= 32, "chunk queue entry");
+
+// Position of flattened block x (0 <= x < W): the pair (s, kvh) and block b0.
+// cum[s] counts the blocks of sequences before s; a 32-way search, one probe
+// per lane per round.
+__device__ __forceinline__ SegIter locate(const DecodeParams& p, const long long* cum, long long x, int BS,
+                                          int lane) {
+    int a = 0, b = p.N;   // cum[a] * Hkv <= x < cum[b] * Hkv
+    while (b - a > 1) {
+        const int step = (b - a + 31) / 32;
+        const int idx = a + lane * step;
+        const bool le = idx < b && cum[idx] * p.Hkv <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        const int top = 31 - __clz(m);                 // lane 0 always probes a
+        a = a + top * step;
+        b = min(a + step, b);
+    }
+    SegIter it;
+    const long long c0 = cum[a];
+    const int nb = (int)(cum[a + 1] - c0);
+    const long long off = x - c0 * p.Hkv;
+    it.gi = x;
+    it.s = a;
+    it.kvh = (int)(off / nb);
+    it.b0 = (int)(off % nb);
+    it.nb = nb;
+    it.first = p.first_blocks ? __ldg(p.first_blocks + a) : 0;
+    return it;
+}
+
 template <class Tr>
 __global__ void __launch_bounds__(Tr::THREADS, Tr::MIN_CTAS)
 pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const DecodeParams p) {
     using Gm = typename Tr::Gm;
-    constexpr int D = Tr::D, BS = Tr::BS, G = Tr::G, NC = Tr::NC, S = Tr::STAGES;
+    constexpr int D = Tr::D, BS = Tr::BS, G = Tr::G, NW = Tr::NW, R = Tr::R, UB = Tr::UB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring_u32 = smem_u32(smem + Tr::RING_OFF);
-    float* so = reinterpret_cast<float*>(smem + Tr::SO_OFF);
-    float* sm = reinterpret_cast<float*>(smem + Tr::SM_OFF);
-    float* sl = reinterpret_cast<float*>(smem + Tr::SL_OFF);
-    float* sh = reinterpret_cast<float*>(smem + Tr::SH_OFF);
-    int* spois = reinterpret_cast<int*>(smem + Tr::SP_OFF);
-    volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::BAR_OFF);
-    CtaInfo* info = reinterpret_cast<CtaInfo*>(smem + Tr::INFO_OFF);
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = smem_u32(bars + S);
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;       // fragment row group
+    const int t4 = lane & 3;       // fragment column pair
+    const uint32_t ring = smem_u32(smem) + warp * R * Gm::STAGE_BYTES;      // this warp's stages
+    const uint32_t full0 = smem_u32(smem + Tr::BAR_OFF) + warp * R * 8;
+    volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF) + warp * R;
 
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < S; ++st) {
-            mbar_init(full0 + 8 * st, 1);
-            mbar_init(empty0 + 8 * st, 1);
-        }
+    long long* scum = reinterpret_cast<long long*>(smem + Tr::CUM_OFF);
+    ChunkEnt* cq = reinterpret_cast<ChunkEnt*>(smem + Tr::CQ_OFF) + warp * Tr::QN;
+
+    if (lane == 0) {
+        for (int st = 0; st < R; ++st) mbar_init(full0 + 8 * st, 1);
         fence_mbar_init();
-    }
-    if constexpr (!Tr::KV8) {
-        if (warp == NC && lane == 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
-    }
-
-    // ---- work range of this CTA (warp 0) ----
-    if (warp == 0) {
-        long long w = 0;
-        int first = 0;
-        for (int s = lane; s < p.N; s += 32) w += pair_blocks(p, s, BS, first);
-        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        const long long W = w * p.Hkv;
-        const long long geff = W < (long long)gridDim.x ? W : (long long)gridDim.x;
-        long long lo = 0, hi = 0;
-        int s0 = 0, kvh0 = 0, b0 = 0;
-        if ((long long)blockIdx.x < geff) {
-            lo = range_lo(blockIdx.x, W, geff);
-            hi = range_lo(blockIdx.x + 1, W, geff);
-            long long base = 0;
-            for (int sb = 0; sb < p.N; sb += 32) {
-                const int s = sb + lane;
-                const long long v = s < p.N ? (long long)pair_blocks(p, s, BS, first) * p.Hkv : 0;
-                long long incl = v;
-                for (int o = 1; o < 32; o <<= 1) {
-                    const long long t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                const long long total = __shfl_sync(0xffffffffu, incl, 31);
-                if (base + total > lo) {
-                    const unsigned m = __ballot_sync(0xffffffffu, base + incl > lo);
-                    const int firstlane = __ffs(m) - 1;
-                    const long long before = base + __shfl_sync(0xffffffffu, incl - v, firstlane);
-                    s0 = sb + firstlane;
-                    const int nb = pair_blocks(p, s0, BS, first);
-                    const long long off = lo - before;
-                    kvh0 = (int)(off / nb);
-                    b0 = (int)(off % nb);
-                    break;
-                }
-                base += total;
+        if constexpr (!Tr::KV8) {
+            if (warp == 0) {
+                prefetch_tmap(&tmap_k);
+                prefetch_tmap(&tmap_v);
             }
         }
-        if (lane == 0) {
-            info->lo = lo;
-            info->hi = hi;
-            info->W = W;
-            info->geff = geff;
-            info->s0 = s0;
-            info->kvh0 = kvh0;
-            info->b0 = b0;
-            info->abort = 0;
-            info->last = 0;
-        }
     }
+    const bool cum_in_smem = p.N <= Tr::CUM_SMEM;
+    if (cum_in_smem)
+        for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) scum[i] = __ldg(p.cum + i);
+    __syncthreads();
+    const long long* cum = cum_in_smem ? scum : p.cum;
 
     // ---- rows of sequences with no blocks here: zero (ctx == 0), the prefix
     //      state alone (every key in a shared prefix), NaN (bad ctx) ----
-    if (warp < NC) {
-        for (int s = blockIdx.x; s < p.N; s += gridDim.x) {
-            const int ctx = __ldg(p.context_lens + s);
-            int first = 0;
-            if (pair_blocks(p, s, BS, first) > 0) continue;
-            const bool bad = ctx < 0 || ctx > p.MB * BS;
-            if (bad && threadIdx.x == 0) set_err(p.err, PA_DEVERR_CONTEXT);
-            uint16_t* row = p.out + (size_t)s * p.Hq * D;
-            for (int i = threadIdx.x; i < p.Hq * D; i += NC * 32) {
-                uint16_t v = 0;
-                if (bad) {
-                    v = qnan16<Tr::BF16>();
-                } else if (first > 0 && ctx > 0) {
-                    const float* c = p.carry + ((size_t)s * p.Hq + i / D) * Tr::PSTRIDE;
-                    v = f32_to_16<Tr::BF16>(__ldg(c + i % D) / __ldg(c + D + 1) * p.v_scale);
-                }
-                row[i] = v;
+    for (int s = blockIdx.x; s < p.N; s += gridDim.x) {
+        if (cum[s + 1] > cum[s]) continue;
+        const int ctx = __ldg(p.context_lens + s);
+        const int first = p.first_blocks ? __ldg(p.first_blocks + s) : 0;
+        const bool bad = ctx < 0 || ctx > p.MB * BS;
+        if (bad && threadIdx.x == 0) set_err(p.err, PA_DEVERR_CONTEXT);
+        uint16_t* row = p.out + (size_t)s * p.Hq * D;
+        for (int i = threadIdx.x; i < p.Hq * D; i += Tr::THREADS) {
+            uint16_t v = 0;
+            if (bad) {
+                v = qnan16<Tr::BF16>();
+            } else if (first > 0 && ctx > 0) {
+                const float* c = p.carry + ((size_t)s * p.Hq + i / D) * Tr::CSTRIDE;
+                v = f32_to_16<Tr::BF16>(__ldg(c + i % D) / __ldg(c + D + 1) * p.v_scale);
             }
+            row[i] = v;
         }
     }
-    __syncthreads();
 
-    const long long lo = info->lo, hi = info->hi, W = info->W, geff = info->geff;
-    if ((long long)blockIdx.x >= geff) return;
+    // ---- the chunk schedule ----
+    const long long nworkers = (long long)gridDim.x * NW;
+    const long long wid = (long long)blockIdx.x * NW + warp;
+    const Sched sc = make_sched(cum[p.N] * p.Hkv, nworkers, p.nd);
+    const int nchunks = sc.NS + sc.ND;
+    if (nchunks == 0) return;
+    // next chunk for this warp: its static one first, then claims (lane 0's
+    // claim is made one chunk ahead so its latency stays hidden)
+    int claim = 0;
+    auto claim_async = [&]() {
+        if (sc.ND > 0 && lane == 0) claim = sc.NS + atomicAdd(p.chunk_ctr, 1);
+        else claim = nchunks;
+    };
+    int next_id;
+    if (wid < sc.NS) {
+        next_id = (int)wid;
+    } else {
+        claim_async();
+        next_id = __shfl_sync(0xffffffffu, claim, 0);
+    }
+    if (next_id >= nchunks) return;
+    claim_async();
+    int qhead = 0, qtail = 0;   // chunk queue: pushed by the issue side, popped by the compute side
 
-    SegIter it0;
-    it0.gi = lo;
-    it0.s = info->s0;
-    it0.kvh = info->kvh0;
-    it0.b0 = info->b0;
-    it0.nb = pair_blocks(p, it0.s, BS, it0.first);
-
-    if (warp == NC) {
-        // =========================== producer ===========================
-        // One ring stage per UB consecutive blocks of a segment; `issued`
-        // counts stages.  A batch of 32 table entries never splits a stage
-        // (32 is a multiple of UB).  Stages are filled in rounds: lane j
-        // probes (without blocking) whether ring stage issued + j is free,
-        // and the leading run of free stages is filled at once, one stage per
-        // lane; only when the oldest stage is still busy does lane 0 block on
-        // it.  At most S stages are probed per round, so no two lanes touch
-        // the same ring slot.
-        long long issued = 0;
-        bool aborted = false;
-        SegIter it = it0;
-        while (it.gi < hi && !aborted) {
-            const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
-            const int32_t* trow = p.block_tables + (size_t)it.s * p.MB + it.first + it.b0;
-            int tcur = lane < len ? __ldg(trow + lane) : 0;
-            for (int base = 0; base < len && !aborted; base += 32) {
-                const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
-                const int cnt = min(32, len - base);
-                const int nst = (cnt + Tr::UB - 1) / Tr::UB;   // stages in this batch
-                int done = 0;
-                while (done < nst) {
-                    const int want = min(nst - done, S);
-                    const long long my = issued + lane;
-                    bool is_free = false;
-                    if (lane < want)
-                        is_free = my < S || mbar_test_wait(empty0 + 8 * (uint32_t)(my % S),
-                                                           (uint32_t)(((my / S) - 1) & 1));
-                    const unsigned fm = __ballot_sync(0xffffffffu, is_free);
-                    int run = (fm == 0xffffffffu) ? 32 : __ffs(~fm) - 1;
-                    if (run == 0) {
-                        int ok = 1;
-                        if (lane == 0)
-                            ok = mbar_wait_bounded(empty0 + 8 * (uint32_t)(issued % S),
-                                                   (uint32_t)(((issued / S) - 1) & 1), p.timeout_ns) ? 1 : 0;
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) {
-                            if (lane == 0) {
-                                set_err(p.err, PA_DEVERR_TIMEOUT);
-                                *(volatile int*)&info->abort = 1;
-                            }
-                            aborted = true;
-                            break;
-                        }
-                        run = 1;
-                    }
-                    // lane j < run fills stage issued + j with batch entries (done + j) * UB ..
-                    const int first = (done + lane) * Tr::UB;
-                    int ids[Tr::UB];
-#pragma unroll
-                    for (int u = 0; u < Tr::UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, (first + u) & 31);
-                    if (lane < run) {
-                        const int nblk = min(Tr::UB, cnt - first);
-                        const int st = (int)(my % S);
-                        bool bad = false;
-#pragma unroll
-                        for (int u = 0; u < Tr::UB; ++u) {
-                            if (u < nblk && (unsigned)ids[u] >= (unsigned)p.NB) {
-                                bad = true;
-                                ids[u] = 0;
-                            }
-                        }
-                        if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
-                        stage_poison[st] = bad ? 1 : 0;
-                        const uint32_t fb = full0 + 8 * st;
-                        const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
-                        if constexpr (Tr::KV8) {
-                            // each block's piece is one contiguous run in the pool
-                            mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
-#pragma unroll
-                            for (int u = 0; u < Tr::UB; ++u)
-                                if (u < nblk)
-                                    bulk_load(kdst + u * Gm::PIECE_BYTES,
-                                              p.kv8 + ((size_t)ids[u] * p.Hkv + it.kvh) * Gm::PIECE_BYTES,
-                                              Gm::PIECE_BYTES, fb);
-                        } else {
-                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-                            const int y = (ids[0] * p.Hkv + it.kvh) * BS;
-#pragma unroll
-                            for (int h = 0; h < Gm::HALVES; ++h) {
-                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-                            }
-                        }
-                    }
-                    issued += run;
-                    done += run;
-                }
-                tcur = nxt;
-            }
-            if (!aborted) seg_advance(it, len, p, BS);
-        }
-        // Wait until every issued copy has landed before the CTA may exit.
+    // ---- issue side: runs up to R stages ahead of the compute side ----
+    SegIter is;
+    long long ihi = 0;
+    int ilen = 0, ib = 0, tbase = 0;
+    const int32_t* irow = nullptr;
+    int tcur = 0, tnxt = 0;
+    bool idone = false;
+    // open chunk `id`: locate its start, queue it, fetch its first table ids
+    auto open_chunk = [&](int id) {
+        const long long clo = sc.lo(id);
+        ihi = sc.lo(id + 1);
+        is = locate(p, cum, clo, BS, lane);
         if (lane == 0) {
-            const long long nst = issued < S ? issued : S;
-            for (long long st = 0; st < nst; ++st) {
-                const long long klast = st + ((issued - 1 - st) / S) * S;
-                if (!mbar_wait_bounded(full0 + 8 * (uint32_t)st, (uint32_t)((klast / S) & 1), p.timeout_ns))
-                    set_err(p.err, PA_DEVERR_TIMEOUT);
+            ChunkEnt& e = cq[qtail % Tr::QN];
+            e.lo = clo;
+            e.hi = ihi;
+            e.id = id;
+            e.s = is.s;
+            e.kvh = is.kvh;
+            e.b0 = is.b0;
+        }
+        ++qtail;
+        ilen = seg_len(is, ihi);
+        ib = 0;
+        tbase = 0;
+        irow = p.block_tables + (size_t)is.s * p.MB + is.first + is.b0;
+        tcur = lane < ilen ? __ldg(irow + lane) : 0;
+        tnxt = 32 + lane < ilen ? __ldg(irow + 32 + lane) : 0;
+    };
+    open_chunk(next_id);
+    long long nis = 0;        // stages issued
+    bool aborted = false;
+    auto issue = [&]() {
+        if (idone || aborted) return;
+        const int st = (int)(nis % R);
+        const int nblk = min(UB, ilen - ib);
+        int ids[UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, (ib - tbase + u) & 31);
+        if (lane == 0) {
+            bool bad = false;
+#pragma unroll
+            for (int u = 0; u < UB; ++u) {
+                if (u < nblk && (unsigned)ids[u] >= (unsigned)p.NB) {
+                    bad = true;
+                    ids[u] = 0;
+                }
+            }
+            if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
+            stage_poison[st] = bad ? 1 : 0;
+            const uint32_t fb = full0 + 8 * st;
+            const uint32_t dst = ring + st * Gm::STAGE_BYTES;
+            if constexpr (Tr::KV8) {
+                // each block's piece is one contiguous run in the pool
+                mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
+#pragma unroll
+                for (int u = 0; u < UB; ++u)
+                    if (u < nblk)
+                        bulk_load(dst + u * Gm::PIECE_BYTES,
+                                  p.kv8 + ((size_t)ids[u] * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES, fb);
+            } else {
+                mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                const int y = (ids[0] * p.Hkv + is.kvh) * BS;
+#pragma unroll
+                for (int h = 0; h < Gm::HALVES; ++h) {
+                    tma_load_2d(dst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                    tma_load_2d(dst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
+                }
             }
         }
-        return;
-    }
+        ++nis;
+        ib += nblk;
+        if (ib == ilen) {
+            seg_advance(is, ilen, p, BS);
+            if (is.gi < ihi) {
+                ilen = seg_len(is, ihi);
+                ib = 0;
+                tbase = 0;
+                irow = p.block_tables + (size_t)is.s * p.MB + is.first + is.b0;
+                tcur = lane < ilen ? __ldg(irow + lane) : 0;
+                tnxt = 32 + lane < ilen ? __ldg(irow + 32 + lane) : 0;
+            } else {
+                const int nid = __shfl_sync(0xffffffffu, claim, 0);
+                if (nid < nchunks) {
+                    claim_async();
+                    open_chunk(nid);
+                } else {
+                    idone = true;
+                }
+            }
+        } else if (ib - tbase == 32) {
+            tbase += 32;
+            tcur = tnxt;
+            tnxt = tbase + 32 + lane < ilen ? __ldg(irow + tbase + 32 + lane) : 0;
+        }
+    };
+    for (int i = 0; i < R; ++i) issue();
 
-    // ============================ consumers ============================
-    const int tid = threadIdx.x;   // 0 .. NC*32-1
-    const int g = lane >> 2;       // fragment row group
-    const int t4 = lane & 3;       // fragment column pair
-    SegIter it = it0;
-    long long ubase = 0;   // stages of the CTA before this segment
-    WarpAcc<D, Tr::NR> acc;
-    // Q fragments (A operand of S^T = Q K^T), rows = heads of the group
+    // ---- compute side ----
     auto load_q = [&](uint32_t (&qa)[Gm::KD][4], const SegIter& sg) {
         const uint16_t* qrow = p.q + ((size_t)sg.s * p.Hq + (size_t)sg.kvh * G) * D;
         const uint16_t* r0 = g < G ? qrow + g * D : nullptr;
         const uint16_t* r1 = (G > 8) ? qrow + (g + 8) * D : nullptr;
         if constexpr (Tr::KV8) {
-            load_q_frags8<D, Tr::BF16>(qa, r0, r1, t4);
+            load_q_frags8<D>(qa, r0, r1, t4);
         } else {
             load_q_frags<D>(qa, r0, r1, t4);
         }
     };
+    // the compute side's current chunk
+    long long clo = 0, chi = 0;
+    int cid = 0;
+    SegIter it;
+    auto pop_chunk = [&]() {
+        __syncwarp();
+        const ChunkEnt& e = cq[qhead % Tr::QN];
+        clo = e.lo;
+        chi = e.hi;
+        cid = e.id;
+        it.gi = e.lo;
+        it.s = e.s;
+        it.kvh = e.kvh;
+        it.b0 = e.b0;
+        const long long c0 = cum[it.s];
+        it.nb = (int)(cum[it.s + 1] - c0);
+        it.first = p.first_blocks ? __ldg(p.first_blocks + it.s) : 0;
+        ++qhead;
+    };
+    pop_chunk();
+    WarpAcc<D, Tr::NR> acc;
     uint32_t qa[Gm::KD][4];
-    int ctx = 0;
-    if (it.gi < hi) {
-        ctx = __ldg(p.context_lens + it.s);
-        load_q(qa, it);
-    }
-    while (it.gi < hi) {
-        const int len = (int)min((long long)(it.nb - it.b0), hi - it.gi);
+    load_q(qa, it);
+    if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
+    int ctx = __ldg(p.context_lens + it.s);
+    long long ncons = 0;      // stages folded in (or skipped after an abort)
+    long long nwait = 0;      // stages whose copies are known to have landed
+    const float qnan = __int_as_float(0x7fc00000);
+    while (true) {
+        const int len = seg_len(it, chi);
+        // the next segment of this chunk: its position, length and Q fetched
+        // a segment ahead
+        SegIter nx = it;
+        seg_advance(nx, len, p, BS);
+        const bool nx_here = nx.gi < chi;
+        uint32_t qn[Gm::KD][4];
+        int ctx_next = 0;
+        if (nx_here) {
+            ctx_next = __ldg(p.context_lens + nx.s);
+            load_q(qn, nx);
+        }
         acc.reset();
         int poisoned = 0;
-
-        // Stage k of the CTA (k = ubase + u, UB blocks each) goes to warp
-        // k % NC.  With STAGES a multiple of NC every ring stage is owned by one
-        // warp, which consumes its fills strictly in order (no mbarrier phase
-        // aliasing).
-        const int nu = (len + Tr::UB - 1) / Tr::UB;
-        int j0 = warp - (int)(ubase % NC);
-        if (j0 < 0) j0 += NC;
-        for (int u = j0; u < nu; u += NC) {
-            const long long k = ubase + u;
-            const int st = (int)(k % S);
-            const uint32_t par = (uint32_t)((k / S) & 1);
-            if (*(volatile int*)&info->abort) {
-                poisoned = 1;
-                continue;
-            }
-            if (!mbar_wait_bounded(full0 + 8 * st, par, p.timeout_ns)) {
-                if (lane == 0) {
-                    set_err(p.err, PA_DEVERR_TIMEOUT);
-                    *(volatile int*)&info->abort = 1;
+        for (int b = 0; b < len; b += UB) {
+            const int st = (int)(ncons % R);
+            ++ncons;
+            if (!aborted) {
+                if (mbar_wait_bounded(full0 + 8 * st, (uint32_t)(((ncons - 1) / R) & 1), p.timeout_ns)) {
+                    nwait = ncons;
+                } else {
+                    if (lane == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
+                    aborted = true;
                 }
+            }
+            if (aborted) {
                 poisoned = 1;
                 continue;
             }
             poisoned |= stage_poison[st];
-            const int b = u * Tr::UB;
-            const int nblk = min(Tr::UB, len - b);
+            const int nblk = min(UB, len - b);
             const int valid = min(nblk * BS, ctx - (it.first + it.b0 + b) * BS);
-            const uint32_t kb = ring_u32 + st * Gm::STAGE_BYTES;
+            const uint32_t kb = ring + st * Gm::STAGE_BYTES;
             bool zeroed = false;
             if constexpr (Tr::KV8) {
                 if (valid < 32 && (valid & 15)) {
@@ -438,30 +477,60 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 }
                 consume_block<Gm, Tr::NR, Tr::BF16>(kb, vb, valid, qa, acc, p.scale_log2, lane);
             }
+            // the stage's shared memory is read (and any zeroing written)
+            // before the async proxy refills it
             if (zeroed) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * st);
-        }
-        ubase += nu;
-
-        // The next segment's position, length and Q: loaded now so that the
-        // loads overlap the merge below.
-        SegIter nx = it;
-        seg_advance(nx, len, p, BS);
-        int ctx_next = 0;
-        if (nx.gi < hi) {
-            ctx_next = __ldg(p.context_lens + nx.s);
-            load_q(qa, nx);
+            issue();
         }
 
-        // ---- merge the NC warp states of this segment ----
+        // ---- finish the segment: output rows, or this chunk's piece ----
 #pragma unroll
         for (int r = 0; r < Tr::NR; ++r) {
             acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
             acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
         }
-        {
-            float* mine = so + warp * G * Tr::OSTRIDE;
+        const long long P0 = it.gi - it.b0;           // flattened start of this pair
+        const long long cfirst = sc.of(P0);
+        const long long clast = sc.of(P0 + it.nb - 1);
+        const bool complete = cfirst == clast;
+        const bool has_carry = it.first > 0;
+        uint16_t* orow = p.out + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
+        const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::CSTRIDE;
+        if (complete) {
+#pragma unroll
+            for (int r = 0; r < Tr::NR; ++r) {
+                // this lane's o columns are heads 8 r + 2 t4 and 8 r + 2 t4 + 1
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int head = 8 * r + 2 * t4 + c;
+                    float M = __shfl_sync(0xffffffffu, acc.m[r], (2 * t4 + c) * 4);
+                    float L = __shfl_sync(0xffffffffu, acc.l[r], (2 * t4 + c) * 4);
+                    float fa = 1.f, fb = 0.f;
+                    if (has_carry && head < G) {
+                        const float* cr = crow + head * Tr::CSTRIDE;
+                        const float cm = __ldg(cr + D), cl = __ldg(cr + D + 1);
+                        const float Mn = fmaxf(M, cm);
+                        fa = ex2(M - Mn);
+                        fb = ex2(cm - Mn);
+                        L = L * fa + cl * fb;
+                    }
+                    if (head < G) {
+#pragma unroll
+                        for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int dim = 16 * mt + g + 8 * hh;
+                                float O = poisoned ? qnan : acc.o[mt][r][2 * hh + c];
+                                if (has_carry) O = O * fa + __ldg(crow + head * Tr::CSTRIDE + dim) * fb;
+                                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
+                            }
+                    }
+                }
+            }
+        } else {
+            const int slot = (it.gi == clo) ? 0 : 1;
+            float* prow = p.partials + ((size_t)cid * 2 + slot) * G * Tr::PSTRIDE;
 #pragma unroll
             for (int mt = 0; mt < Gm::KD; ++mt)
 #pragma unroll
@@ -470,118 +539,154 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     for (int e = 0; e < 4; ++e) {
                         const int head = 8 * r + 2 * t4 + (e & 1);
                         const int dim = 16 * mt + g + 8 * (e >> 1);
-                        if (head < G) mine[head * Tr::OSTRIDE + dim] = acc.o[mt][r][e];
+                        if (head < G) prow[head * Tr::PSTRIDE + dim] = poisoned ? qnan : acc.o[mt][r][e];
                     }
             if (t4 == 0) {
 #pragma unroll
                 for (int r = 0; r < Tr::NR; ++r) {
                     const int head = g + 8 * r;
                     if (head < G) {
-                        sm[warp * G + head] = acc.m[r];
-                        sl[warp * G + head] = acc.l[r];
+                        prow[head * Tr::PSTRIDE + D] = acc.m[r];
+                        prow[head * Tr::PSTRIDE + D + 1] = acc.l[r];
                     }
-                }
-            }
-            if (lane == 0) spois[warp] = poisoned;
-        }
-        named_bar_sync(1, NC * 32);
-
-        const long long P0 = it.gi - it.b0;           // flattened start of this pair
-        const long long cfirst = cta_of(P0, W, geff);
-        const long long clast = cta_of(P0 + it.nb - 1, W, geff);
-        const bool complete = cfirst == clast;
-        const int slot = (it.gi == lo) ? 0 : 1;
-        const bool has_carry = it.first > 0;
-        int bad = 0;
-#pragma unroll
-        for (int w = 0; w < NC; ++w) bad |= spois[w];
-        const float qnan = __int_as_float(0x7fc00000);
-        uint16_t* orow = p.out + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
-        const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::PSTRIDE;
-        float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * G * Tr::PSTRIDE;
-        // Per head, once: the common max M, each warp's factor exp2(m_w - M)
-        // (in place of m_w), L, and for a finished pair with a prefix state
-        // the factors that fold the carry in (the log-sum-exp rule).
-        if (tid < G) {
-            const int hd = tid;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) M = fmaxf(M, sm[w * G + hd]);
-            float L = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) {
-                const float f = ex2(sm[w * G + hd] - M);
-                sm[w * G + hd] = f;
-                L += sl[w * G + hd] * f;
-            }
-            float fa = 1.f, fb = 0.f;
-            if (complete && has_carry) {
-                const float* c = crow + hd * Tr::PSTRIDE;
-                const float cm = __ldg(c + D), cl = __ldg(c + D + 1);
-                const float Mn = fmaxf(M, cm);
-                fa = ex2(M - Mn);
-                fb = ex2(cm - Mn);
-                L = L * fa + cl * fb;
-                M = Mn;
-            }
-            sh[hd] = M;
-            sh[G + hd] = L;
-            sh[2 * G + hd] = fa;
-            sh[3 * G + hd] = fb;
-        }
-        named_bar_sync(1, NC * 32);
-        for (int idx = tid; idx < G * D; idx += NC * 32) {
-            const int head = idx / D;
-            const int dim = idx - head * D;
-            float O = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) O += so[(w * G + head) * Tr::OSTRIDE + dim] * sm[w * G + head];
-            if (bad) O = qnan;
-            if (complete) {
-                if (has_carry) O = O * sh[2 * G + head] + __ldg(crow + head * Tr::PSTRIDE + dim) * sh[3 * G + head];
-                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / sh[G + head] * p.v_scale);
-            } else {
-                prow[head * Tr::PSTRIDE + dim] = O;
-                if (dim == 0) {
-                    prow[head * Tr::PSTRIDE + D] = sh[head];
-                    prow[head * Tr::PSTRIDE + D + 1] = sh[G + head];
                 }
             }
         }
 
-        if (!complete) {
-            // Publish this piece, count arrivals; the last piece merges.
-            __threadfence();
-            named_bar_sync(1, NC * 32);
-            const int pair = it.s * p.Hkv + it.kvh;
-            if (tid == 0) {
-                const int prev = atomicAdd(p.counters + pair, 1);
-                *(volatile int*)&info->last = (prev == (int)(clast - cfirst)) ? 1 : 0;
-            }
-            named_bar_sync(1, NC * 32);
-            if (*(volatile int*)&info->last) {
-                __threadfence();
-                for (int idx = tid; idx < G * D; idx += NC * 32) {
-                    const int head = idx / D;
-                    const int dim = idx - head * D;
-                    float M = -INFINITY, L = 0.f, O = 0.f;
-                    for (long long c = cfirst; c <= clast; ++c) {
-                        const int sl_c = (c == cfirst && range_lo(c, W, geff) < P0) ? 1 : 0;
-                        const float* pr = p.partials + ((size_t)c * 2 + sl_c) * G * Tr::PSTRIDE + head * Tr::PSTRIDE;
-                        lse_fold(M, L, O, __ldcg(pr + D), __ldcg(pr + D + 1), __ldcg(pr + dim));
-                    }
-                    if (has_carry) {
-                        const float* cr = crow + head * Tr::PSTRIDE;
-                        lse_fold(M, L, O, __ldg(cr + D), __ldg(cr + D + 1), __ldg(cr + dim));
-                    }
-                    orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
-                }
-            }
+        if (nx_here) {
+            it = nx;
+            ctx = ctx_next;
+#pragma unroll
+            for (int kk = 0; kk < Gm::KD; ++kk)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qa[kk][i] = qn[kk][i];
+        } else {
+            // the chunk is done; the next one (if any) was queued by the
+            // issue side, which is always ahead
+            if (qhead == qtail) break;
+            pop_chunk();
+            ctx = __ldg(p.context_lens + it.s);
+            load_q(qa, it);
         }
-        named_bar_sync(1, NC * 32);
-        it = nx;
-        ctx = ctx_next;
+        if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
     }
+
+    // After a timeout, wait (bounded) for the copies still in flight before
+    // the CTA's shared memory is released.
+    if (aborted && lane == 0) {
+        for (long long k = nwait; k < nis; ++k) {
+            if (k < nis - R) continue;   // an older fill of the same stage
+            mbar_wait_bounded(full0 + 8 * (uint32_t)(k % R), (uint32_t)((k / R) & 1), p.timeout_ns);
+        }
+    }
+}
+
+// Post-pass: for every pair cut by chunk boundaries, combine its pieces (in
+// chunk order) and the prefix carry by the log-sum-exp rule and write the
+// output rows.  One warp per (pair, query head) -- two heads per warp when
+// d = 64 -- so the whole merge is a few rounds of independent loads: first
+// the lanes take different pieces to form the common max M and the sum L,
+// then every lane folds 4 dims of every piece.  nworkers and nd are the
+// decode launch's.
+template <int D>
+__global__ void __launch_bounds__(256, 4)
+pa_decode_merge(const long long* __restrict__ cum, const int32_t* __restrict__ first_blocks,
+                const float* __restrict__ carry, const float* __restrict__ partials, uint16_t* __restrict__ out,
+                int N, int Hkv, int G, long long nworkers, int nd, float v_scale, int bf16) {
+    constexpr int PSTRIDE = D + 4, CSTRIDE = D + 2;
+    constexpr int LPH = D / 4;                     // lanes per head
+    constexpr int HPW = 32 / LPH;                  // heads per warp
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPH;
+    const int hgroups = (G + HPW - 1) / HPW;
+    const long long task = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const long long pair = task / hgroups;
+    if (pair >= (long long)N * Hkv) return;
+    const int s = (int)(pair / Hkv), kvh = (int)(pair % Hkv);
+    const long long c0 = cum[s];
+    const int nb = (int)(cum[s + 1] - c0);
+    if (nb == 0) return;
+    const Sched sc = make_sched(cum[N] * Hkv, nworkers, nd);
+    const long long P0 = c0 * Hkv + (long long)kvh * nb;
+    const long long cfirst = sc.of(P0), clast = sc.of(P0 + nb - 1);
+    if (cfirst == clast) return;                                  // written by the decode kernel
+    const int head0 = (int)(task % hgroups) * HPW + lane / LPH;
+    const bool writer = head0 < G;
+    const int head = writer ? head0 : G - 1;
+    const int np = (int)(clast - cfirst) + 1;
+    // piece i = chunk cfirst + i; only the first can sit in slot 1 (when the
+    // pair starts inside that chunk)
+    const size_t cstride = (size_t)2 * G * PSTRIDE;
+    const float* first = partials + (size_t)cfirst * cstride + (sc.lo(cfirst) < P0 ? (size_t)G * PSTRIDE : 0) +
+                         (size_t)head * PSTRIDE;
+    const float* rest = partials + (size_t)cfirst * cstride + (size_t)head * PSTRIDE;
+    auto piece = [&](int i) -> const float* { return i == 0 ? first : rest + (size_t)i * cstride; };
+    const bool has_carry = first_blocks && first_blocks[s] > 0;
+    const int Hq = Hkv * G;
+    const float* cr = carry + ((size_t)s * Hq + (size_t)kvh * G + head) * CSTRIDE;
+
+    const int d0 = sub * 4;
+    // the first pieces' o slices, issued before anything that depends on M
+    constexpr int PB = 8;
+    float4 v[PB];
+#pragma unroll
+    for (int k = 0; k < PB; ++k)
+        if (k < np) v[k] = *reinterpret_cast<const float4*>(piece(k) + d0);
+    // per-piece m and l: lane (i mod LPH) of the head's lane group holds piece i
+    float M = -INFINITY;
+    for (int i = sub; i < np; i += LPH) M = fmaxf(M, piece(i)[D]);
+    for (int o = LPH / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float cm = -INFINITY, cl = 0.f;
+    if (has_carry) {
+        cm = cr[D];
+        cl = cr[D + 1];
+        M = fmaxf(M, cm);
+    }
+    const float fi = sub < np ? ex2(piece(sub)[D] - M) : 0.f;   // factor of piece sub (np <= LPH)
+    float L = 0.f;
+    for (int i = sub; i < np; i += LPH) {
+        const float* pr = piece(i);
+        L += pr[D + 1] * ex2(pr[D] - M);
+    }
+    for (int o = LPH / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int gbase = lane - sub;                                 // first lane of this head's group
+    for (int c0 = 0; c0 < np; c0 += PB) {
+        if (c0 > 0) {
+#pragma unroll
+            for (int k = 0; k < PB; ++k)
+                if (c0 + k < np) v[k] = *reinterpret_cast<const float4*>(piece(c0 + k) + d0);
+        }
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+            const int c = c0 + k;
+            if (c >= np) break;
+            const float f = c < LPH ? __shfl_sync(0xffffffffu, fi, gbase + c) : ex2(piece(c)[D] - M);
+            acc.x += v[k].x * f;
+            acc.y += v[k].y * f;
+            acc.z += v[k].z * f;
+            acc.w += v[k].w * f;
+        }
+    }
+    if (has_carry) {
+        const float f = ex2(cm - M);
+        L += cl * f;
+        acc.x += cr[d0] * f;
+        acc.y += cr[d0 + 1] * f;
+        acc.z += cr[d0 + 2] * f;
+        acc.w += cr[d0 + 3] * f;
+    }
+    if (!writer) return;
+    const float inv = v_scale / L;
+    const float x[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+    uint32_t w[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint16_t h0 = bf16 ? f32_to_16<true>(x[2 * k]) : f32_to_16<false>(x[2 * k]);
+        const uint16_t h1 = bf16 ? f32_to_16<true>(x[2 * k + 1]) : f32_to_16<false>(x[2 * k + 1]);
+        w[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    }
+    *reinterpret_cast<uint2*>(out + ((size_t)s * Hq + (size_t)kvh * G + head) * D + d0) = make_uint2(w[0], w[1]);
 }
 
 // ---------------------------------------------------------------- host side
@@ -591,13 +696,14 @@ struct DecodeLaunch {
     DecodeParams p;
     cudaStream_t stream;
     int grid;
+    bool bf16;   // output type of the merge post-pass
 };
 
 struct DecodeKernelInfo {
     cudaError_t (*launch)(const DecodeLaunch&);
     int (*max_ctas)(int device);   // persistent grid size on that device, <= 0 on error
     int smem_bytes;
-    int stages;
+    int workers;                   // worker warps per CTA (partial-state slots per CTA)
 };
 
 template <class Tr>
@@ -609,7 +715,7 @@ cudaError_t decode_launch(const DecodeLaunch& L) {
 template <class Tr>
 DecodeKernelInfo decode_info() {
     return DecodeKernelInfo{&decode_launch<Tr>, &persistent_ctas<pa_decode_kernel<Tr>, Tr::THREADS, Tr::SMEM_BYTES>,
-                            Tr::SMEM_BYTES, Tr::STAGES};
+                            Tr::SMEM_BYTES, Tr::NW};
 }
 
 // Per-(dtype, head_dim) tables, defined in the instantiation units.

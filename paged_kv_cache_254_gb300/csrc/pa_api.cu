@@ -83,14 +83,118 @@ pa_status pick_decode(const pa_shape* s, const DecodeKernelInfo** out) {
     return PA_OK;
 }
 
-size_t counters_bytes(const pa_shape* s) {
-    const size_t c = (size_t)s->num_seqs * s->num_kv_heads * sizeof(int32_t);
+// ---------------------------------------------------------------- decode scratch
+// One region per decode launch: the dynamic-chunk counter, per-sequence block
+// prefix sums, and two partial states (o[d], m, l per query row of a group,
+// rows of d + 4 floats) per chunk.  Chunks: one per worker warp, plus up to
+// kDynPerWorker per worker claimed at run time.
+constexpr int kDynPerWorker = 4;
+
+size_t counters_bytes(const pa_shape*) { return 256; }
+
+size_t cum_bytes(const pa_shape* s) {
+    const size_t c = ((size_t)s->num_seqs + 1) * sizeof(long long);
     return (c + 255) & ~size_t(255);
 }
 
-size_t partials_bytes(const pa_shape* s, int max_ctas) {
+size_t piece_bytes(const pa_shape* s) {
     const int g = s->num_q_heads / s->num_kv_heads;
-    return (size_t)max_ctas * 2 * g * (s->head_dim + 2) * sizeof(float);
+    return (size_t)2 * g * (s->head_dim + 4) * sizeof(float);
+}
+
+// Region size for `workers` static chunks and `nd` dynamic ones.
+size_t decode_region_bytes(const pa_shape* s, long long workers, long long nd) {
+    return counters_bytes(s) + cum_bytes(s) + (size_t)(workers + nd) * piece_bytes(s);
+}
+
+// Zero the chunk counter; cum[s] = blocks of the
+// sequences before s in the decode work list (with a shared-prefix pass,
+// blocks after each sequence's first_blocks).  One CTA.
+__global__ void __launch_bounds__(1024)
+pa_decode_prepass(const int32_t* __restrict__ context_lens, const int32_t* __restrict__ first_blocks, int N,
+                  int MB, int BS, int32_t* __restrict__ counters, long long n_counters,
+                  long long* __restrict__ cum) {
+    __shared__ long long wsum[32];
+    __shared__ long long carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (long long i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        cum[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int s = base + (int)threadIdx.x;
+        long long v = 0;
+        if (s < N) {
+            const int c = context_lens[s];
+            const int nb = (c > 0 && c <= MB * BS) ? (c + BS - 1) / BS : 0;
+            const int f = first_blocks ? first_blocks[s] : 0;
+            v = nb - f > 0 ? nb - f : 0;
+        }
+        long long x = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long t = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += t;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long w = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long t = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += t;
+            }
+            wsum[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const long long incl = carry + (warp > 0 ? wsum[warp - 1] : 0) + x;
+        if (s < N) cum[s + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+}
+
+template <int D>
+cudaError_t merge_launch(const DecodeLaunch& L, int g, long long nworkers, cudaStream_t st) {
+    constexpr int HPW = 32 / (D / 4);
+    const long long tasks = (long long)L.p.N * L.p.Hkv * ((g + HPW - 1) / HPW);
+    const long long blocks = (tasks + 7) / 8;
+    pa_decode_merge<D><<<(unsigned)blocks, 256, 0, st>>>(L.p.cum, L.p.first_blocks, L.p.carry, L.p.partials,
+                                                         L.p.out, L.p.N, L.p.Hkv, g, nworkers, L.p.nd,
+                                                         L.p.v_scale, L.bf16 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+// Lay out the decode region, run the pre-pass, fill L's scheduling fields,
+// launch the decode and the merge of split pairs.  L's other fields are set
+// by the caller.
+pa_status run_decode(const DecodeKernelInfo* k, int ctas, DecodeLaunch& L, const pa_shape* s, void* region,
+                     size_t region_bytes, const int32_t* first_blocks) {
+    const long long workers = (long long)ctas * k->workers;
+    const size_t fixed = counters_bytes(s) + cum_bytes(s);
+    if (!region || region_bytes < decode_region_bytes(s, workers, 0)) return PA_ERR_WORKSPACE;
+    long long cap = (long long)((region_bytes - fixed) / piece_bytes(s)) - workers;
+    long long nd = kDynPerWorker * workers;
+    if (nd > cap) nd = cap;
+    if (nd > (1ll << 30)) nd = 1ll << 30;
+    uint8_t* base = static_cast<uint8_t*>(region);
+    L.p.chunk_ctr = reinterpret_cast<int32_t*>(base);
+    L.p.cum = reinterpret_cast<const long long*>(base + counters_bytes(s));
+    L.p.partials = reinterpret_cast<float*>(base + fixed);
+    L.p.nd = (int32_t)nd;
+    L.grid = ctas;
+    L.bf16 = s->dtype == PA_BF16;
+    pa_decode_prepass<<<1, 1024, 0, L.stream>>>(L.p.context_lens, first_blocks, s->num_seqs,
+                                                s->max_blocks_per_seq, s->block_size, L.p.chunk_ctr, 1,
+                                                const_cast<long long*>(L.p.cum));
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (k->launch(L) != cudaSuccess) return PA_ERR_CUDA;
+    const int g = s->num_q_heads / s->num_kv_heads;
+    const cudaError_t e = s->head_dim == 128 ? merge_launch<128>(L, g, workers, L.stream)
+                                             : merge_launch<64>(L, g, workers, L.stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -168,18 +272,17 @@ const PrefixKernelInfo& pick_prefix(const pa_shape* s) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace of prefix-aware decode: decode counters, prefix counters, carry
-// states, decode partials, prefix partials (offsets in off[0..4]).
-size_t shared_prefix_layout(const pa_shape* s, int dec_ctas, int pre_ctas, size_t (&off)[6]) {
-    const size_t cb = counters_bytes(s);
-    off[0] = 0;                                   // decode counters
-    off[1] = cb;                                  // prefix counters
-    off[5] = 2 * cb;                              // first block per sequence
-    off[2] = off[5] + align256((size_t)s->num_seqs * sizeof(int32_t));   // carry (after the zeroed part)
+// Workspace of prefix-aware decode (offsets in off[]): [0] prefix counters,
+// [1] first block per sequence (both zeroed before the prefix pass), [2] carry
+// states, [3] prefix partials, [4] the decode region (to the end).
+size_t shared_prefix_layout(const pa_shape* s, long long dec_workers, int pre_ctas, size_t (&off)[5]) {
+    off[0] = 0;
+    off[1] = align256((size_t)s->num_seqs * s->num_kv_heads * sizeof(int32_t));
+    off[2] = off[1] + align256((size_t)s->num_seqs * sizeof(int32_t));
     const size_t carry = align256((size_t)s->num_seqs * s->num_q_heads * (s->head_dim + 2) * sizeof(float));
     off[3] = off[2] + carry;
-    off[4] = off[3] + align256(partials_bytes(s, dec_ctas));
-    return off[4] + (size_t)pre_ctas * 2 * 32 * (s->head_dim + 2) * sizeof(float);
+    off[4] = off[3] + align256((size_t)pre_ctas * 2 * 32 * (s->head_dim + 2) * sizeof(float));
+    return off[4] + decode_region_bytes(s, dec_workers, kDynPerWorker * dec_workers);
 }
 
 }  // namespace
@@ -193,7 +296,8 @@ size_t pa_decode_workspace_bytes(const pa_shape* shape) {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int ctas = k->max_ctas(dev);
     if (ctas <= 0) return 0;
-    return counters_bytes(shape) + partials_bytes(shape, ctas);
+    const long long workers = (long long)ctas * k->workers;
+    return decode_region_bytes(shape, workers, kDynPerWorker * workers);
 }
 
 pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, const void* v_pool,
@@ -212,8 +316,7 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
     const int ctas = k->max_ctas(dev);
     if (ctas <= 0) return PA_ERR_CUDA;
-    const size_t need = counters_bytes(shape) + partials_bytes(shape, ctas);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
     if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
@@ -225,8 +328,6 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     L.p.block_tables = block_tables;
     L.p.context_lens = context_lens;
     L.p.out = static_cast<uint16_t*>(out);
-    L.p.counters = static_cast<int32_t*>(workspace);
-    L.p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counters_bytes(shape));
     L.p.err = err_word;
     L.p.N = shape->num_seqs;
     L.p.Hq = shape->num_q_heads;
@@ -237,11 +338,9 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     L.p.timeout_ns = kTimeoutNs;
     L.p.v_scale = 1.0f;
     L.stream = static_cast<cudaStream_t>(stream);
-    L.grid = ctas;
-    // Arrival counters start at zero for every call (the region may hold
-    // another shape's partial states from an earlier call).
-    if (cudaMemsetAsync(workspace, 0, counters_bytes(shape), L.stream) != cudaSuccess) return PA_ERR_CUDA;
-    return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    // The counters start at zero for every call (the pre-pass clears them;
+    // the region may hold another shape's state from an earlier call).
+    return run_decode(k, ctas, L, shape, workspace, workspace_bytes, nullptr);
 }
 
 size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape) {
@@ -251,8 +350,8 @@ size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape) {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int dec = k->max_ctas(dev), pre = pick_prefix(shape).max_ctas(dev);
     if (dec <= 0 || pre <= 0) return 0;
-    size_t off[6];
-    return shared_prefix_layout(shape, dec, pre, off);
+    size_t off[5];
+    return shared_prefix_layout(shape, (long long)dec * k->workers, pre, off);
 }
 
 pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const void* k_pool, const void* v_pool,
@@ -277,16 +376,18 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     const PrefixKernelInfo& pk = pick_prefix(shape);
     const int dec = k->max_ctas(dev), pre = pk.max_ctas(dev);
     if (dec <= 0 || pre <= 0) return PA_ERR_CUDA;
-    size_t off[6];
-    const size_t need = shared_prefix_layout(shape, dec, pre, off);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    size_t off[5];
+    shared_prefix_layout(shape, (long long)dec * k->workers, pre, off);
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < off[4] + decode_region_bytes(shape, (long long)dec * k->workers, 0))
+        return PA_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
     if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     const float scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
-    // both arrival-counter regions and the first-block array start at zero
+    // the prefix arrival counters and the first-block array start at zero
     if (cudaMemsetAsync(ws, 0, off[2], strm) != cudaSuccess) return PA_ERR_CUDA;
 
     if (num_groups > 0) {
@@ -299,9 +400,9 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
         P.p.grp_starts = group_starts;
         P.p.grp_prefix = group_prefix_blocks;
         P.p.carry = reinterpret_cast<float*>(ws + off[2]);
-        P.p.first_blocks = reinterpret_cast<int32_t*>(ws + off[5]);
-        P.p.counters = reinterpret_cast<int32_t*>(ws + off[1]);
-        P.p.partials = reinterpret_cast<float*>(ws + off[4]);
+        P.p.first_blocks = reinterpret_cast<int32_t*>(ws + off[1]);
+        P.p.counters = reinterpret_cast<int32_t*>(ws + off[0]);
+        P.p.partials = reinterpret_cast<float*>(ws + off[3]);
         P.p.err = err_word;
         P.p.n_groups = num_groups;
         P.p.G = shape->num_q_heads / shape->num_kv_heads;
@@ -324,10 +425,8 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     L.p.block_tables = block_tables;
     L.p.context_lens = context_lens;
     L.p.out = static_cast<uint16_t*>(out);
-    L.p.counters = reinterpret_cast<int32_t*>(ws + off[0]);
-    L.p.partials = reinterpret_cast<float*>(ws + off[3]);
     L.p.err = err_word;
-    L.p.first_blocks = reinterpret_cast<const int32_t*>(ws + off[5]);
+    L.p.first_blocks = reinterpret_cast<const int32_t*>(ws + off[1]);
     L.p.carry = reinterpret_cast<const float*>(ws + off[2]);
     L.p.N = shape->num_seqs;
     L.p.Hq = shape->num_q_heads;
@@ -338,8 +437,7 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
     L.p.timeout_ns = kTimeoutNs;
     L.p.v_scale = 1.0f;
     L.stream = strm;
-    L.grid = dec;
-    return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return run_decode(k, dec, L, shape, ws + off[4], workspace_bytes - off[4], L.p.first_blocks);
 }
 
 size_t pa_decode_fp8_workspace_bytes(const pa_shape* shape, int32_t kv_format) {
@@ -347,9 +445,11 @@ size_t pa_decode_fp8_workspace_bytes(const pa_shape* shape, int32_t kv_format) {
     if (pick_decode(shape, &k16) != PA_OK || check_fp8(shape, kv_format, 1.f, 1.f) != PA_OK) return 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const int ctas = pick_decode8(shape, kv_format)->max_ctas(dev);
+    const DecodeKernelInfo* k8 = pick_decode8(shape, kv_format);
+    const int ctas = k8->max_ctas(dev);
     if (ctas <= 0) return 0;
-    return counters_bytes(shape) + partials_bytes(shape, ctas);
+    const long long workers = (long long)ctas * k8->workers;
+    return decode_region_bytes(shape, workers, kDynPerWorker * workers);
 }
 
 pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q, const void* kv_pool,
@@ -372,8 +472,7 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     const DecodeKernelInfo* k = pick_decode8(shape, kv_format);
     const int ctas = k->max_ctas(dev);
     if (ctas <= 0) return PA_ERR_CUDA;
-    const size_t need = counters_bytes(shape) + partials_bytes(shape, ctas);
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     // every (block, head) piece is bulk-copied from p.kv8; the tensor-map
     // parameters of the kernel go unused
     CUtensorMap unused{};
@@ -385,8 +484,6 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     L.p.block_tables = block_tables;
     L.p.context_lens = context_lens;
     L.p.out = static_cast<uint16_t*>(out);
-    L.p.counters = static_cast<int32_t*>(workspace);
-    L.p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counters_bytes(shape));
     L.p.err = err_word;
     L.p.kv8 = static_cast<const uint8_t*>(kv_pool);
     L.p.v_scale = v_scale;
@@ -399,9 +496,7 @@ pa_status pa_decode_fp8(const pa_shape* shape, int32_t kv_format, const void* q,
     L.p.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
     L.p.timeout_ns = kTimeoutNs;
     L.stream = static_cast<cudaStream_t>(stream);
-    L.grid = ctas;
-    if (cudaMemsetAsync(workspace, 0, counters_bytes(shape), L.stream) != cudaSuccess) return PA_ERR_CUDA;
-    return k->launch(L) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return run_decode(k, ctas, L, shape, workspace, workspace_bytes, nullptr);
 }
 
 pa_status pa_append_kv_fp8(const pa_shape* shape, int32_t kv_format, int32_t num_tokens, const void* k_new,

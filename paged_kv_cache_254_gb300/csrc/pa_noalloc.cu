@@ -50,8 +50,10 @@ extern "C" pa_status pa_decode_noalloc(const pa_shape* shape, const void* q, con
                                        const void* v_pool, const int32_t* block_tables,
                                        const int32_t* context_lens, float scale, void* out,
                                        uint32_t* err_word, void* stream) {
-    const size_t need = pa_decode_workspace_bytes(shape);
-    if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    // pa_decode rejects (PA_ERR_WORKSPACE, nothing enqueued) a buffer below the
+    // shape's minimum scratch, and uses fewer run-time balanced chunks when the
+    // buffer is below its preferred size.
+    if (pa_decode_workspace_bytes(shape) == 0) return PA_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (scratch_on_current_device(&scratch) != cudaSuccess) return PA_ERR_CUDA;
     // pa_decode validates everything else and clears the arrival counters in

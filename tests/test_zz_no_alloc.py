@@ -59,10 +59,12 @@ def test_noalloc_rejects_shapes_beyond_its_buffer():
     import paged_kv_cache_254_gb300 as pa
 
     lib = _lib.load()
-    # 300k sequences x 8 KV heads need ~9.6 MB of counters alone, past the
-    # 8 MiB static buffer; the call must refuse before touching any pointer.
-    shape = pa.make_shape(300_000, 64, 8, 128, 16, 1000, 8, torch.bfloat16)
+    # 5M sequences need 40 MB of per-sequence prefix sums alone, past the
+    # 32 MiB static buffer even at the minimum scratch; the call must refuse
+    # before it enqueues anything (the pointers below are never valid).
+    shape = pa.make_shape(5_000_000, 64, 8, 128, 16, 1000, 8, torch.bfloat16)
     fake = ctypes.c_void_p(1 << 20)
+    assert (5_000_000 + 1) * 8 > _lib.NOALLOC_SCRATCH_BYTES
     assert lib.pa_decode_workspace_bytes(ctypes.byref(shape)) > _lib.NOALLOC_SCRATCH_BYTES
     st = lib.pa_decode_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, ctypes.c_float(0.1), fake,
                                ctypes.c_void_p(0), ctypes.c_void_p(0))
