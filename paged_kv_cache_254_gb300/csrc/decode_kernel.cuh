@@ -94,12 +94,14 @@ struct DecodeTraits {
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
     static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad (16-byte rows)
     static constexpr int CSTRIDE = D_ + 2;                  // carry row (prefix pass): o[D], m, l
-    static constexpr int CUM_SMEM = 1024;                   // sequences whose prefix sums fit in smem
+    static constexpr int CUM_SMEM = 512;                    // sequences whose tables fit in smem
     static constexpr int QN = 16;                           // open chunks per warp (> R + 1)
     // shared memory, offsets from a 1024-byte aligned base
     static constexpr int BAR_OFF = NW * R * Gm::STAGE_BYTES;
     static constexpr int CUM_OFF = BAR_OFF + NW * R * 8;    // long long [CUM_SMEM + 1]
-    static constexpr int CQ_OFF = CUM_OFF + (CUM_SMEM + 1) * 8;
+    static constexpr int CTX_OFF = CUM_OFF + (CUM_SMEM + 1) * 8;   // int [CUM_SMEM] context lengths
+    static constexpr int FST_OFF = CTX_OFF + CUM_SMEM * 4;  // int [CUM_SMEM] first blocks
+    static constexpr int CQ_OFF = FST_OFF + CUM_SMEM * 4;
     static constexpr int PS_OFF = CQ_OFF + NW * QN * 32;    // poison flag per stage
     static constexpr int SMEM_BYTES = PS_OFF + NW * R * 4 + 1024;  // + alignment slack
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
@@ -107,12 +109,16 @@ struct DecodeTraits {
     static_assert(32 % UB == 0, "a batch of 32 table entries holds whole stages");
 };
 
-// Blocks of sequence s in this kernel's work list (and its first block).
-__device__ __forceinline__ int pair_blocks(const DecodeParams& p, int s, int BS, int& first) {
-    first = p.first_blocks ? __ldg(p.first_blocks + s) : 0;
-    const int nb = seq_blocks(__ldg(p.context_lens + s), BS, p.MB) - first;
-    return nb > 0 ? nb : 0;
-}
+// Per-sequence data of the work list (in shared memory for small batches):
+// cum[s] = blocks of the sequences before s, context lengths, first blocks
+// (blocks already covered by a shared-prefix pass; null: none).
+struct SeqTab {
+    const long long* cum;
+    const int* ctx;
+    const int* first;
+    __device__ __forceinline__ int nb(int s) const { return (int)(cum[s + 1] - cum[s]); }
+    __device__ __forceinline__ int fst(int s) const { return first ? first[s] : 0; }
+};
 
 // Position inside the flattened block list, advanced segment by segment.
 struct SegIter {
@@ -120,20 +126,20 @@ struct SegIter {
     int s, kvh, b0, nb, first;
 };
 
-__device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodeParams& p, int BS) {
+__device__ __forceinline__ void seg_advance(SegIter& it, int len, const DecodeParams& p, const SeqTab& tab) {
     it.gi += len;
     it.b0 += len;
     if (it.b0 == it.nb) {
         it.b0 = 0;
         if (++it.kvh == p.Hkv) {
             it.kvh = 0;
-            int nb = 0, first = 0;
+            int nb = 0;
             while (++it.s < p.N) {
-                nb = pair_blocks(p, it.s, BS, first);
+                nb = tab.nb(it.s);
                 if (nb > 0) break;
             }
             it.nb = nb;
-            it.first = first;
+            it.first = it.s < p.N ? tab.fst(it.s) : 0;
         }
     }
 }
@@ -184,8 +190,8 @@ static_assert(sizeof(ChunkEnt) <= 32, "chunk queue entry");
 // Position of flattened block x (0 <= x < W): the pair (s, kvh) and block b0.
 // cum[s] counts the blocks of sequences before s; a 32-way search, one probe
 // per lane per round.
-__device__ __forceinline__ SegIter locate(const DecodeParams& p, const long long* cum, long long x, int BS,
-                                          int lane) {
+__device__ __forceinline__ SegIter locate(const DecodeParams& p, const SeqTab& tab, long long x, int lane) {
+    const long long* cum = tab.cum;
     int a = 0, b = p.N;   // cum[a] * Hkv <= x < cum[b] * Hkv
     while (b - a > 1) {
         const int step = (b - a + 31) / 32;
@@ -205,7 +211,7 @@ __device__ __forceinline__ SegIter locate(const DecodeParams& p, const long long
     it.kvh = (int)(off / nb);
     it.b0 = (int)(off % nb);
     it.nb = nb;
-    it.first = p.first_blocks ? __ldg(p.first_blocks + a) : 0;
+    it.first = tab.fst(a);
     return it;
 }
 
@@ -226,6 +232,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     volatile int* stage_poison = reinterpret_cast<volatile int*>(smem + Tr::PS_OFF) + warp * R;
 
     long long* scum = reinterpret_cast<long long*>(smem + Tr::CUM_OFF);
+    int* sctx = reinterpret_cast<int*>(smem + Tr::CTX_OFF);
+    int* sfst = reinterpret_cast<int*>(smem + Tr::FST_OFF);
     ChunkEnt* cq = reinterpret_cast<ChunkEnt*>(smem + Tr::CQ_OFF) + warp * Tr::QN;
 
     if (lane == 0) {
@@ -238,18 +246,29 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         }
     }
-    const bool cum_in_smem = p.N <= Tr::CUM_SMEM;
-    if (cum_in_smem)
-        for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) scum[i] = __ldg(p.cum + i);
+    const bool in_smem = p.N <= Tr::CUM_SMEM;
+    if (in_smem) {
+        for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) {
+            scum[i] = __ldg(p.cum + i);
+            if (i < p.N) {
+                sctx[i] = __ldg(p.context_lens + i);
+                if (p.first_blocks) sfst[i] = __ldg(p.first_blocks + i);
+            }
+        }
+    }
     __syncthreads();
-    const long long* cum = cum_in_smem ? scum : p.cum;
+    SeqTab tab;
+    tab.cum = in_smem ? scum : p.cum;
+    tab.ctx = in_smem ? sctx : p.context_lens;
+    tab.first = p.first_blocks ? (in_smem ? sfst : p.first_blocks) : nullptr;
+    const long long* cum = tab.cum;
 
     // ---- rows of sequences with no blocks here: zero (ctx == 0), the prefix
     //      state alone (every key in a shared prefix), NaN (bad ctx) ----
     for (int s = blockIdx.x; s < p.N; s += gridDim.x) {
         if (cum[s + 1] > cum[s]) continue;
-        const int ctx = __ldg(p.context_lens + s);
-        const int first = p.first_blocks ? __ldg(p.first_blocks + s) : 0;
+        const int ctx = tab.ctx[s];
+        const int first = tab.fst(s);
         const bool bad = ctx < 0 || ctx > p.MB * BS;
         if (bad && threadIdx.x == 0) set_err(p.err, PA_DEVERR_CONTEXT);
         uint16_t* row = p.out + (size_t)s * p.Hq * D;
@@ -290,17 +309,47 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     int qhead = 0, qtail = 0;   // chunk queue: pushed by the issue side, popped by the compute side
 
     // ---- issue side: runs up to R stages ahead of the compute side ----
+    // Block ids come from the table 32 at a time (one per lane): tcur holds
+    // entries [row_off, row_off + 32) of sequence row_s's row, tnxt the next
+    // 32.  The KV heads of a sequence share its row, so a batch is reused
+    // across them; the first batch of the next sequence is fetched (tpre)
+    // while the current one is in use.
     SegIter is;
     long long ihi = 0;
     int ilen = 0, ib = 0, tbase = 0;
-    const int32_t* irow = nullptr;
-    int tcur = 0, tnxt = 0;
+    int tcur = 0, tnxt = 0, tpre = 0;
+    int row_s = -1, row_off = 0, pre_s = -1;
     bool idone = false;
-    // open chunk `id`: locate its start, queue it, fetch its first table ids
+    auto row_ids = [&](int sq, int off, int navail) -> int {
+        return lane < navail ? __ldg(p.block_tables + (size_t)sq * p.MB + off + lane) : 0;
+    };
+    // the table batch for the segment starting at `is`
+    auto seg_ids = [&]() {
+        const int off = is.first + is.b0;
+        ib = 0;
+        tbase = 0;
+        if (!(is.s == row_s && off == row_off)) {
+            if (is.s == pre_s && is.b0 == 0) {
+                tcur = tpre;
+            } else {
+                tcur = row_ids(is.s, off, is.nb - is.b0);
+            }
+            tnxt = row_ids(is.s, off + 32, is.nb - is.b0 - 32);
+            row_s = is.s;
+            row_off = off;
+            // the next sequence with blocks, from its first entry
+            int sn = is.s + 1;
+            while (sn < p.N && tab.nb(sn) == 0) ++sn;
+            pre_s = sn < p.N ? sn : -1;
+            if (pre_s >= 0) tpre = row_ids(sn, tab.fst(sn), tab.nb(sn));
+        }
+        ilen = seg_len(is, ihi);
+    };
+    // open chunk `id`: locate its start, queue it for the compute side
     auto open_chunk = [&](int id) {
         const long long clo = sc.lo(id);
         ihi = sc.lo(id + 1);
-        is = locate(p, cum, clo, BS, lane);
+        is = locate(p, tab, clo, lane);
         if (lane == 0) {
             ChunkEnt& e = cq[qtail % Tr::QN];
             e.lo = clo;
@@ -311,12 +360,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             e.b0 = is.b0;
         }
         ++qtail;
-        ilen = seg_len(is, ihi);
-        ib = 0;
-        tbase = 0;
-        irow = p.block_tables + (size_t)is.s * p.MB + is.first + is.b0;
-        tcur = lane < ilen ? __ldg(irow + lane) : 0;
-        tnxt = 32 + lane < ilen ? __ldg(irow + 32 + lane) : 0;
+        seg_ids();
     };
     open_chunk(next_id);
     long long nis = 0;        // stages issued
@@ -362,14 +406,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ++nis;
         ib += nblk;
         if (ib == ilen) {
-            seg_advance(is, ilen, p, BS);
+            seg_advance(is, ilen, p, tab);
             if (is.gi < ihi) {
-                ilen = seg_len(is, ihi);
-                ib = 0;
-                tbase = 0;
-                irow = p.block_tables + (size_t)is.s * p.MB + is.first + is.b0;
-                tcur = lane < ilen ? __ldg(irow + lane) : 0;
-                tnxt = 32 + lane < ilen ? __ldg(irow + 32 + lane) : 0;
+                seg_ids();
             } else {
                 const int nid = __shfl_sync(0xffffffffu, claim, 0);
                 if (nid < nchunks) {
@@ -381,8 +420,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         } else if (ib - tbase == 32) {
             tbase += 32;
+            row_off += 32;
             tcur = tnxt;
-            tnxt = tbase + 32 + lane < ilen ? __ldg(irow + tbase + 32 + lane) : 0;
+            tnxt = row_ids(is.s, is.first + is.b0 + tbase + 32, is.nb - is.b0 - tbase - 32);
         }
     };
     for (int i = 0; i < R; ++i) issue();
@@ -412,9 +452,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         it.s = e.s;
         it.kvh = e.kvh;
         it.b0 = e.b0;
-        const long long c0 = cum[it.s];
-        it.nb = (int)(cum[it.s + 1] - c0);
-        it.first = p.first_blocks ? __ldg(p.first_blocks + it.s) : 0;
+        it.nb = tab.nb(it.s);
+        it.first = tab.fst(it.s);
         ++qhead;
     };
     pop_chunk();
@@ -422,7 +461,34 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     uint32_t qa[Gm::KD][4];
     load_q(qa, it);
     if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
-    int ctx = __ldg(p.context_lens + it.s);
+    int ctx = tab.ctx[it.s];
+    // The running state starts empty, or -- for the first suffix segment of
+    // a sequence whose shared prefix was reduced by the prefix pass -- as the
+    // prefix state (the carry), so the carry is folded in exactly once.
+    auto init_acc = [&]() {
+        acc.reset();
+        if (it.first > 0 && it.b0 == 0) {
+            const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::CSTRIDE;
+#pragma unroll
+            for (int r = 0; r < Tr::NR; ++r) {
+                const int head = g + 8 * r;
+                if (head < G) {
+                    acc.m[r] = __ldg(crow + head * Tr::CSTRIDE + D);
+                    if (t4 == 0) acc.l[r] = __ldg(crow + head * Tr::CSTRIDE + D + 1);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < Gm::KD; ++mt)
+#pragma unroll
+                for (int r = 0; r < Tr::NR; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int head = 8 * r + 2 * t4 + (e & 1);
+                        const int dim = 16 * mt + g + 8 * (e >> 1);
+                        if (head < G) acc.o[mt][r][e] = __ldg(crow + head * Tr::CSTRIDE + dim);
+                    }
+        }
+    };
     long long ncons = 0;      // stages folded in (or skipped after an abort)
     long long nwait = 0;      // stages whose copies are known to have landed
     const float qnan = __int_as_float(0x7fc00000);
@@ -431,15 +497,15 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         // the next segment of this chunk: its position, length and Q fetched
         // a segment ahead
         SegIter nx = it;
-        seg_advance(nx, len, p, BS);
+        seg_advance(nx, len, p, tab);
         const bool nx_here = nx.gi < chi;
         uint32_t qn[Gm::KD][4];
         int ctx_next = 0;
         if (nx_here) {
-            ctx_next = __ldg(p.context_lens + nx.s);
+            ctx_next = tab.ctx[nx.s];
             load_q(qn, nx);
         }
-        acc.reset();
+        init_acc();
         int poisoned = 0;
         for (int b = 0; b < len; b += UB) {
             const int st = (int)(ncons % R);
@@ -494,9 +560,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const long long cfirst = sc.of(P0);
         const long long clast = sc.of(P0 + it.nb - 1);
         const bool complete = cfirst == clast;
-        const bool has_carry = it.first > 0;
         uint16_t* orow = p.out + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * D;
-        const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::CSTRIDE;
         if (complete) {
 #pragma unroll
             for (int r = 0; r < Tr::NR; ++r) {
@@ -504,26 +568,16 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int head = 8 * r + 2 * t4 + c;
-                    float M = __shfl_sync(0xffffffffu, acc.m[r], (2 * t4 + c) * 4);
-                    float L = __shfl_sync(0xffffffffu, acc.l[r], (2 * t4 + c) * 4);
-                    float fa = 1.f, fb = 0.f;
-                    if (has_carry && head < G) {
-                        const float* cr = crow + head * Tr::CSTRIDE;
-                        const float cm = __ldg(cr + D), cl = __ldg(cr + D + 1);
-                        const float Mn = fmaxf(M, cm);
-                        fa = ex2(M - Mn);
-                        fb = ex2(cm - Mn);
-                        L = L * fa + cl * fb;
-                    }
+                    const float L = __shfl_sync(0xffffffffu, acc.l[r], (2 * t4 + c) * 4);
                     if (head < G) {
+                        const float inv = p.v_scale / L;
 #pragma unroll
                         for (int mt = 0; mt < Gm::KD; ++mt)
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh) {
                                 const int dim = 16 * mt + g + 8 * hh;
-                                float O = poisoned ? qnan : acc.o[mt][r][2 * hh + c];
-                                if (has_carry) O = O * fa + __ldg(crow + head * Tr::CSTRIDE + dim) * fb;
-                                orow[head * D + dim] = f32_to_16<Tr::BF16>(O / L * p.v_scale);
+                                const float O = poisoned ? qnan : acc.o[mt][r][2 * hh + c];
+                                orow[head * D + dim] = f32_to_16<Tr::BF16>(O * inv);
                             }
                     }
                 }
@@ -565,7 +619,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             // issue side, which is always ahead
             if (qhead == qtail) break;
             pop_chunk();
-            ctx = __ldg(p.context_lens + it.s);
+            ctx = tab.ctx[it.s];
             load_q(qa, it);
         }
         if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
@@ -582,18 +636,17 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 }
 
 // Post-pass: for every pair cut by chunk boundaries, combine its pieces (in
-// chunk order) and the prefix carry by the log-sum-exp rule and write the
-// output rows.  One warp per (pair, query head) -- two heads per warp when
+// chunk order) by the log-sum-exp rule and write the output rows (a prefix
+// carry is already inside the pair's first piece).  One warp per (pair, query head) -- two heads per warp when
 // d = 64 -- so the whole merge is a few rounds of independent loads: first
 // the lanes take different pieces to form the common max M and the sum L,
 // then every lane folds 4 dims of every piece.  nworkers and nd are the
 // decode launch's.
 template <int D>
 __global__ void __launch_bounds__(256, 4)
-pa_decode_merge(const long long* __restrict__ cum, const int32_t* __restrict__ first_blocks,
-                const float* __restrict__ carry, const float* __restrict__ partials, uint16_t* __restrict__ out,
+pa_decode_merge(const long long* __restrict__ cum, const float* __restrict__ partials, uint16_t* __restrict__ out,
                 int N, int Hkv, int G, long long nworkers, int nd, float v_scale, int bf16) {
-    constexpr int PSTRIDE = D + 4, CSTRIDE = D + 2;
+    constexpr int PSTRIDE = D + 4;
     constexpr int LPH = D / 4;                     // lanes per head
     constexpr int HPW = 32 / LPH;                  // heads per warp
     const int lane = threadIdx.x & 31;
@@ -621,9 +674,7 @@ pa_decode_merge(const long long* __restrict__ cum, const int32_t* __restrict__ f
                          (size_t)head * PSTRIDE;
     const float* rest = partials + (size_t)cfirst * cstride + (size_t)head * PSTRIDE;
     auto piece = [&](int i) -> const float* { return i == 0 ? first : rest + (size_t)i * cstride; };
-    const bool has_carry = first_blocks && first_blocks[s] > 0;
     const int Hq = Hkv * G;
-    const float* cr = carry + ((size_t)s * Hq + (size_t)kvh * G + head) * CSTRIDE;
 
     const int d0 = sub * 4;
     // the first pieces' o slices, issued before anything that depends on M
@@ -636,12 +687,6 @@ pa_decode_merge(const long long* __restrict__ cum, const int32_t* __restrict__ f
     float M = -INFINITY;
     for (int i = sub; i < np; i += LPH) M = fmaxf(M, piece(i)[D]);
     for (int o = LPH / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float cm = -INFINITY, cl = 0.f;
-    if (has_carry) {
-        cm = cr[D];
-        cl = cr[D + 1];
-        M = fmaxf(M, cm);
-    }
     const float fi = sub < np ? ex2(piece(sub)[D] - M) : 0.f;   // factor of piece sub (np <= LPH)
     float L = 0.f;
     for (int i = sub; i < np; i += LPH) {
@@ -667,14 +712,6 @@ pa_decode_merge(const long long* __restrict__ cum, const int32_t* __restrict__ f
             acc.z += v[k].z * f;
             acc.w += v[k].w * f;
         }
-    }
-    if (has_carry) {
-        const float f = ex2(cm - M);
-        L += cl * f;
-        acc.x += cr[d0] * f;
-        acc.y += cr[d0 + 1] * f;
-        acc.z += cr[d0 + 2] * f;
-        acc.w += cr[d0 + 3] * f;
     }
     if (!writer) return;
     const float inv = v_scale / L;

@@ -161,9 +161,8 @@ cudaError_t merge_launch(const DecodeLaunch& L, int g, long long nworkers, cudaS
     constexpr int HPW = 32 / (D / 4);
     const long long tasks = (long long)L.p.N * L.p.Hkv * ((g + HPW - 1) / HPW);
     const long long blocks = (tasks + 7) / 8;
-    pa_decode_merge<D><<<(unsigned)blocks, 256, 0, st>>>(L.p.cum, L.p.first_blocks, L.p.carry, L.p.partials,
-                                                         L.p.out, L.p.N, L.p.Hkv, g, nworkers, L.p.nd,
-                                                         L.p.v_scale, L.bf16 ? 1 : 0);
+    pa_decode_merge<D><<<(unsigned)blocks, 256, 0, st>>>(L.p.cum, L.p.partials, L.p.out, L.p.N, L.p.Hkv, g,
+                                                         nworkers, L.p.nd, L.p.v_scale, L.bf16 ? 1 : 0);
     return cudaGetLastError();
 }
 
