@@ -42,13 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic per decode launch (bytes read + written), keyed by a hash
 # of the decode kernel's source; a stale entry reports null.
 TRAFFIC = {
-    ("b01e7ef0750b7170", "llama3_70b_b256"): 4_838_000_000,   # 4.83 GB read + 7.94 MB written
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one pa_decode_kernel launch
+    ("bd2b041a08e61c80", "llama3_70b_b256"): 4_861_687_296,   # 4,829,489,920 read + 32,197,376 written
 }
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "ptx.cuh"):
+    for f in ("decode_kernel.cuh", "decode_common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_254_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
