@@ -221,3 +221,66 @@ def decode_shared_prefix_ref(q, k_pool, v_pool, block_tables, context_lens, scal
                  for lo, hi in ((0, npre), (npre, ctx)) if hi > lo]
         out[b, h] = lse_merge_ref(parts)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Multi-token query: a chunk of new tokens per sequence, causal within it.
+# ---------------------------------------------------------------------------
+
+def decode_multi_ref(q, k_pool, v_pool, block_tables, context_lens, q_start, scale: float) -> np.ndarray:
+    """Paged attention for a chunk of query tokens per sequence, in fp64.
+
+    The pages' chunked prefill (thewebvale section 4: a long prompt is fed in
+    chunks co-scheduled with decode) and speculative verification
+    (letsbuildsolutions "Speculative Decoding", ontq section 7: the target
+    model scores all drafted tokens in one pass) both need attention for
+    several new tokens of one sequence at once.  Reading taken: sequence b's
+    q_len = q_start[b + 1] - q_start[b] query tokens are its last q_len cached
+    tokens (their K/V were appended before the call), at positions
+    ctx - q_len .. ctx - 1, and query token i attends causally to keys
+    t <= ctx - q_len + i.  q [T, Hq, d] with T = q_start[N], sequence b's
+    rows at q_start[b] ..; returns out [T, Hq, d].
+    """
+    qf = f64(q)
+    bt = _i64(block_tables)
+    cl = _i64(context_lens)
+    qs = _i64(q_start)
+    T, Hq, d = qf.shape
+    Hkv, B = k_pool.shape[1], k_pool.shape[2]
+    g = Hq // Hkv
+    out = np.full((T, Hq, d), np.nan)
+    for b in range(len(cl)):
+        ctx, r0, r1 = int(cl[b]), int(qs[b]), int(qs[b + 1])
+        n = r1 - r0
+        assert 0 <= n <= ctx or (n == 0 and ctx == 0), "a chunk longer than its context"
+        for kh in range(Hkv):
+            if n == 0:
+                continue
+            K, V = gather_sequence(k_pool, v_pool, bt[b], ctx, kh, B)
+            for i in range(n):
+                lim = ctx - n + i                          # last key this token sees
+                for h in range(kh * g, (kh + 1) * g):
+                    p = softmax_weights(qf[r0 + i, h], K[:lim + 1], scale)
+                    out[r0 + i, h] = p @ V[:lim + 1]
+    return out
+
+
+def causal_dense_ref(q_all, k_seq, v_seq, scale: float) -> np.ndarray:
+    """Textbook causal self-attention over one contiguous sequence:
+    q_all [ctx, Hq, d], k_seq, v_seq [ctx, Hkv, d]; S = scale Q K^T with
+    S[i, t] = -inf for t > i, row softmax, O = P V.  Returns [ctx, Hq, d]."""
+    qf, kf, vf = f64(q_all), f64(k_seq), f64(v_seq)
+    ctx, Hq, d = qf.shape
+    Hkv = kf.shape[1]
+    g = Hq // Hkv
+    out = np.zeros_like(qf)
+    mask = np.triu(np.ones((ctx, ctx), dtype=bool), k=1)
+    for h in range(Hq):
+        kh = h // g
+        S = scale * qf[:, h, :] @ kf[:, kh, :].T
+        S[mask] = -np.inf
+        S -= S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, h, :] = P @ vf[:, kh, :]
+    return out
