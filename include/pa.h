@@ -125,6 +125,41 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
                     void* stream);
 
 /*
+ * Multi-token query paged attention: a chunk of new tokens per sequence
+ * (chunked prefill -- thewebvale "vLLM & High-Throughput Serving", section 4;
+ * speculative verification -- letsbuildsolutions "How LLM Inference Engines
+ * Work", speculative decoding, where the target model scores every drafted
+ * token in one pass).
+ *
+ * Sequence b brings n_b = q_start[b + 1] - q_start[b] query tokens, its last
+ * n_b cached tokens (their K/V appended before the call), at rows
+ * q_start[b] .. q_start[b + 1] - 1 of q and out.  Query token i of the chunk
+ * attends causally to the keys t <= context_lens[b] - n_b + i:
+ *     s_t  = scale * <q[q_start[b] + i, h, :], K(b, t, h / g)>
+ *     out[q_start[b] + i, h, :] = sum_t softmax(s)_t * V(b, t, h / g)
+ * with K(b, t, kh) = K_pool[table[b][t/B], kh, t%B, :] as in pa_decode.
+ *
+ *   max_q_len     largest n_b of the call, 1..16; max_q_len * g <= 128
+ *   total_q       T: rows of q and out (q_start[N] should equal it)
+ *   q, out        [T][Hq][d], same 16-bit dtype as the pools
+ *   q_start       device int32 [N + 1], non-decreasing
+ *   others        as pa_decode; workspace: pa_decode_multi_workspace_bytes
+ *
+ * A sequence whose chunk is malformed (n_b < 0, n_b > max_q_len, n_b > its
+ * context, rows outside [0, T)) or whose context is invalid sets
+ * PA_DEVERR_CONTEXT; its rows inside [0, T) are NaN.  Supported shapes as
+ * pa_decode (16-bit); larger max_q_len * g: PA_ERR_UNSUPPORTED.  Three
+ * launches on `stream` (pre-pass, attention, merge of split pairs).
+ */
+size_t pa_decode_multi_workspace_bytes(const pa_shape* shape, int32_t max_q_len);
+
+pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t total_q, const void* q,
+                          const int32_t* q_start, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                          void* stream);
+
+/*
  * 8-bit (FP8) KV cache.  Storing keys and values in 8 bits halves the cache
  * (ontq "AI Inference Serving at Scale", section 6; the vLLM deployment
  * script on thewebvale, section 5, names fp8_e5m2 as a cache dtype).

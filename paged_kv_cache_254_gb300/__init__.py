@@ -20,6 +20,7 @@ from .ops import (  # noqa: F401
     pa_decode,
     pa_decode_fp8,
     pa_decode_shared_prefix,
+    pa_decode_multi,
     pa_decode_workspace_bytes,
     pa_read_error,
     workspace_for,

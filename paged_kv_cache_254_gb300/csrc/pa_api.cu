@@ -10,6 +10,7 @@
 #include "../../include/pa.h"
 #include "decode_kernel.cuh"
 #include "kv_ops.cuh"
+#include "multi_kernel.cuh"
 #include "prefix_kernel.cuh"
 
 namespace {
@@ -270,6 +271,35 @@ const PrefixKernelInfo& pick_prefix(const pa_shape* s) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- multi-token query
+// Kernel for a launch whose chunks hold up to max_q tokens: 16-row tiles per
+// CTA = the rows of one (sequence, KV head) pair, max_q * g <= 128.
+pa_status pick_multi(const pa_shape* s, int max_q, const MultiKernelInfo** out) {
+    const DecodeKernelInfo* k16 = nullptr;
+    pa_status st = pick_decode(s, &k16);                  // the same shape rules as decode
+    if (st != PA_OK) return st;
+    if (max_q < 1 || max_q > 16) return PA_ERR_INVALID_ARG;
+    const int rows = max_q * (s->num_q_heads / s->num_kv_heads);
+    if (rows > 128) return PA_ERR_UNSUPPORTED;
+    const int nw = rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 4 : 8;
+    static const auto tab = [] {
+        struct T { MultiKernelInfo t[2][2][2][4]; } x;   // [bf16][d == 128][bs == 32][log2 nw]
+        multi_table_fp16_d64(x.t[0][0]);
+        multi_table_fp16_d128(x.t[0][1]);
+        multi_table_bf16_d64(x.t[1][0]);
+        multi_table_bf16_d128(x.t[1][1]);
+        return x;
+    }();
+    *out = &tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32][log2_exact(nw)];
+    return PA_OK;
+}
+
+// Scratch of a multi-token launch: chunk counter, block prefix sums, two
+// partial states per tile row per CTA.
+size_t multi_region_bytes(const pa_shape* s, int ctas, int rows) {
+    return counters_bytes(s) + cum_bytes(s) + (size_t)ctas * 2 * rows * (s->head_dim + 4) * sizeof(float);
+}
 
 // Workspace of prefix-aware decode (offsets in off[]): [0] prefix counters,
 // [1] first block per sequence (both zeroed before the prefix pass), [2] carry
@@ -616,5 +646,87 @@ const char* pa_status_string(pa_status status) {
 }
 
 int32_t pa_version(void) { return 100; }
+
+
+size_t pa_decode_multi_workspace_bytes(const pa_shape* shape, int32_t max_q_len) {
+    const MultiKernelInfo* k = nullptr;
+    if (pick_multi(shape, max_q_len, &k) != PA_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int ctas = k->max_ctas(dev);
+    if (ctas <= 0) return 0;
+    return multi_region_bytes(shape, ctas, k->rows);
+}
+
+pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t total_q, const void* q,
+                          const int32_t* q_start, const void* k_pool, const void* v_pool,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
+                          void* workspace, size_t workspace_bytes, uint32_t* err_word, void* stream) {
+    const MultiKernelInfo* k = nullptr;
+    pa_status st = pick_multi(shape, max_q_len, &k);
+    if (st != PA_OK) return st;
+    if (total_q < 0) return PA_ERR_INVALID_ARG;
+    if (!q_start || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(q_start, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->num_seqs == 0) return PA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    const int ctas = k->max_ctas(dev);
+    if (ctas <= 0) return PA_ERR_CUDA;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < multi_region_bytes(shape, ctas, k->rows))
+        return PA_ERR_WORKSPACE;
+    CUtensorMap mk, mv;
+    if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    MultiLaunch L{};
+    L.tmap_k = &mk;
+    L.tmap_v = &mv;
+    DecodeParams& d = L.p.d;
+    d.q = static_cast<const uint16_t*>(q);
+    d.block_tables = block_tables;
+    d.context_lens = context_lens;
+    d.out = static_cast<uint16_t*>(out);
+    d.err = err_word;
+    d.chunk_ctr = reinterpret_cast<int32_t*>(base);
+    d.cum = reinterpret_cast<const long long*>(base + counters_bytes(shape));
+    d.partials = reinterpret_cast<float*>(base + counters_bytes(shape) + cum_bytes(shape));
+    d.N = shape->num_seqs;
+    d.Hq = shape->num_q_heads;
+    d.Hkv = shape->num_kv_heads;
+    d.NB = shape->num_blocks;
+    d.MB = shape->max_blocks_per_seq;
+    d.scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
+    d.timeout_ns = kTimeoutNs;
+    d.v_scale = 1.0f;
+    L.p.q_start = q_start;
+    L.p.max_q = max_q_len;
+    L.p.total_q = total_q;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.grid = ctas;
+    pa_decode_prepass<<<1, 1024, 0, L.stream>>>(context_lens, nullptr, shape->num_seqs,
+                                                shape->max_blocks_per_seq, shape->block_size, d.chunk_ctr, 1,
+                                                const_cast<long long*>(d.cum));
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (k->launch(L) != cudaSuccess) return PA_ERR_CUDA;
+    const int g = shape->num_q_heads / shape->num_kv_heads;
+    constexpr int kWarps = 8;
+    const int rpw = shape->head_dim == 128 ? 1 : 2;            // merge rows per warp
+    const long long tasks = (long long)shape->num_seqs * shape->num_kv_heads * ((max_q_len * g + rpw - 1) / rpw);
+    const unsigned blocks = (unsigned)((tasks + kWarps - 1) / kWarps);
+    if (shape->head_dim == 128)
+        pa_multi_merge<128><<<blocks, 32 * kWarps, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out,
+                                                                  d.N, d.Hkv, g, k->rows, ctas, max_q_len, total_q,
+                                                                  shape->dtype == PA_BF16);
+    else
+        pa_multi_merge<64><<<blocks, 32 * kWarps, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out,
+                                                                 d.N, d.Hkv, g, k->rows, ctas, max_q_len, total_q,
+                                                                 shape->dtype == PA_BF16);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 }  // extern "C"

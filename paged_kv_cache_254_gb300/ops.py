@@ -202,6 +202,56 @@ def pa_decode_shared_prefix(q, k_pool, v_pool, block_tables, context_lens, group
     return out
 
 
+def pa_decode_multi(q, k_pool, v_pool, block_tables, context_lens, q_start, scale, max_q_len=None,
+                    out=None, workspace=None, err=None, stream=None):
+    """Multi-token query paged attention (see include/pa.h): q [T, Hq, d]
+    holds each sequence's chunk of new tokens at rows q_start[b] ..
+    q_start[b + 1] - 1 (q_start: int32 CUDA tensor [N + 1]); token i of a
+    chunk attends causally to keys t <= ctx - q_len + i.  max_q_len defaults
+    to the largest chunk (read from q_start on the host)."""
+    _need_cuda("q", q)
+    _need_cuda("k_pool", k_pool, q.dtype)
+    _need_cuda("v_pool", v_pool, q.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("q_start", q_start, torch.int32)
+    T, Hq, d = q.shape
+    N = block_tables.shape[0]
+    if q_start.shape != (N + 1,) or context_lens.shape != (N,):
+        raise ValueError("q_start must have N + 1 entries and context_lens N")
+    if k_pool.shape != v_pool.shape or k_pool.shape[3] != d:
+        raise ValueError("shape mismatch between q and the pools")
+    if max_q_len is None:
+        qs = q_start.cpu()
+        max_q_len = max(1, int((qs[1:] - qs[:-1]).max().item())) if N > 0 else 1
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, q.dtype)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    shape = _pool_shape(k_pool, N, Hq, block_tables.shape[1])
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        need = int(lib.pa_decode_multi_workspace_bytes(ctypes.byref(shape), ctypes.c_int32(max_q_len)))
+        if need == 0 and workspace is None:
+            # an invalid shape or chunk bound: let the call report which
+            workspace = torch.empty(0, dtype=torch.uint8, device=q.device)
+        elif workspace is None:
+            workspace = _shared_workspace(q.device, need, stream)
+        else:
+            _need_cuda("workspace", workspace)
+        if err is not None:
+            _need_cuda("err", err, torch.int32)
+        st = lib.pa_decode_multi(ctypes.byref(shape), ctypes.c_int32(max_q_len), ctypes.c_int32(T), _ptr(q),
+                                 _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                 _ptr(context_lens), ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                                 ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(err),
+                                 _stream(q.device, stream))
+    _lib.check(st, "pa_decode_multi")
+    return out
+
+
 _sp_cache = {}
 
 
