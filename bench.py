@@ -69,6 +69,9 @@ def parse_args(argv=None):
                     help="cache element type (fp8: 8-bit cache, quantising append, 8-bit decode)")
     ap.add_argument("--plain-decode", action="store_true",
                     help="decode shared-prompt batches without the prefix-aware pass")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence per step (> 1: each sequence appends that many tokens and "
+                         "pa_decode_multi attends them causally -- a chunked-prefill / speculative-verify step)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="truncate the batch (small profiling captures); the JSON line says so")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
@@ -76,13 +79,13 @@ def parse_args(argv=None):
 
 
 # --------------------------------------------------------------------------- accounting
-def decode_bytes(ctx, Hq, Hkv, d, B, elem=2, q_elem=2) -> int:
+def decode_bytes(ctx, Hq, Hkv, d, B, elem=2, q_elem=2, q_len=1) -> int:
     """Bytes the method must move for one decode call: every cached K and V
-    element once (elem bytes each), Q and O once, the block-table entries in
-    use and the context lengths."""
+    element once (elem bytes each), Q and O once (q_len rows per sequence),
+    the block-table entries in use and the context lengths."""
     ctx = [int(c) for c in ctx]
     kv = sum(ctx) * Hkv * d * elem * 2
-    qo = 2 * len(ctx) * Hq * d * q_elem
+    qo = 2 * len(ctx) * q_len * Hq * d * q_elem
     tables = sum(-(-c // B) for c in ctx) * 4
     return kv + qo + tables + 4 * len(ctx)
 
@@ -200,7 +203,7 @@ def unique_decode_bytes(tables, ctx, Hq, Hkv, d, B, elem=2, q_elem=2) -> int:
 FP8_SCALE = 0.25
 
 
-def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
+def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16", q_len=1) -> dict:
     """Device tensors of one decode step.  Block tables, lengths, slot mapping
     and copy list come from the host BlockManager (seeded random placement);
     values from the seeded workload generators."""
@@ -237,11 +240,19 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
         bm = BlockManager(case.num_blocks, B, seed=seed + 17)
         seqs = list(range(len(case.context_lens)))
         for s in seqs:
-            if bm.add_sequence(s, int(case.context_lens[s]) - 1) is None:
+            if bm.add_sequence(s, int(case.context_lens[s]) - q_len) is None:
                 raise RuntimeError("pool too small")
         t0 = time.perf_counter()
-        slots = bm.append_slots(seqs)                # the newest token of every sequence
+        # the newest token (or the chunk of q_len new tokens) of every sequence
+        slots = bm.append_slots(seqs if q_len == 1 else [(s, q_len) for s in seqs])
         host_ms = (time.perf_counter() - t0) * 1e3
+        if q_len > 1:
+            from workloads import make_values
+            gq = torch.Generator(device=device).manual_seed((seed or 0) + 77)
+            n = len(seqs)
+            case.q = make_values((n * q_len, cfg.num_q_heads, cfg.head_dim), cfg.dtype, gq, device)
+            case.k_new = make_values((n * q_len, cfg.num_kv_heads, cfg.head_dim), cfg.dtype, gq, device)
+            case.v_new = make_values((n * q_len, cfg.num_kv_heads, cfg.head_dim), cfg.dtype, gq, device)
         max_blocks = cfg.max_blocks_per_seq
         desc, Hq, Hkv, d = cfg.description, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
     copies = bm.take_copies()
@@ -269,6 +280,7 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
         "host_block_manager_ms": host_ms, "bm_stats": bm.stats(),
         "shared": name == SAMPLING.name, "kv_dtype": kv_dtype,
         "group_starts": to(gstarts), "group_prefix": to(gprefix), "n_groups": int(gprefix.size),
+        "q_len": q_len, "q_start": to((np.arange(len(seqs) + 1) * q_len).astype(np.int32)),
     }
 
 
@@ -276,8 +288,9 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16") -> dict:
 def cpu_worker(args):
     """Time the fp64 oracle on the first sequences of the workload (host
     cores, single-threaded BLAS) and print one JSON object."""
-    from oracle.attention import decode_ref
+    from oracle.attention import decode_multi_ref, decode_ref
     from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case, sampling_tables
+    import torch
 
     if args.config == SAMPLING.name:
         cfg = SAMPLING
@@ -290,23 +303,31 @@ def cpu_worker(args):
         tables, ctx_all = case.block_tables, case.context_lens
         n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     n_gen = len(ctx_all)
+    ql = args.q_len
+    if ql > 1:
+        gq = torch.Generator().manual_seed(77)
+        qm = torch.randn((n_gen * ql, Hq, d), generator=gq).to(case.q.dtype)
     done = 0
     t0 = time.perf_counter()
     while done < n_gen and time.perf_counter() - t0 < args.cpu_seconds:
-        rows = [(done, h) for h in range(Hq)]
-        decode_ref(case.q, case.k_pool, case.v_pool, tables, ctx_all, case.scale, rows=rows)
+        if ql > 1:
+            decode_multi_ref(qm[done * ql:(done + 1) * ql], case.k_pool, case.v_pool, tables[done:done + 1],
+                             ctx_all[done:done + 1], [0, ql], case.scale)
+        else:
+            rows = [(done, h) for h in range(Hq)]
+            decode_ref(case.q, case.k_pool, case.v_pool, tables, ctx_all, case.scale, rows=rows)
         done += 1
     dt = time.perf_counter() - t0
     ctx_done = [int(c) for c in ctx_all[:done]]
     if args.config == SAMPLING.name:
         nbytes = unique_decode_bytes(tables[:done], ctx_done, Hq, Hkv, d, B)
     else:
-        nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B)
-    nbytes += append_bytes(done, Hkv, d)
+        nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B, q_len=ql)
+    nbytes += append_bytes(done * ql, Hkv, d)
     print(json.dumps({
-        "value": nbytes / dt / 1e9, "unit": "GB/s", "tokens_per_s": done / dt, "seconds": dt,
+        "value": nbytes / dt / 1e9, "unit": "GB/s", "tokens_per_s": done * ql / dt, "seconds": dt,
         "sample": f"first {done} of {n_total} sequences of {cfg.name} (all {Hq} query heads, "
-                  f"{sum(ctx_done)} cached tokens), fp64 oracle",
+                  f"{ql} query token(s) each, {sum(ctx_done)} cached tokens), fp64 oracle",
         "cores": 1,
     }))
 
@@ -319,7 +340,7 @@ def run_cpu_baseline(args) -> dict:
     env.pop("WORLD_SIZE", None)
     env["CUDA_VISIBLE_DEVICES"] = ""
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--config", args.config,
-           "--cpu-seconds", str(args.cpu_seconds)]
+           "--cpu-seconds", str(args.cpu_seconds), "--q-len", str(args.q_len)]
     if args.seed is not None:
         cmd += ["--seed", str(args.seed)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
@@ -354,7 +375,7 @@ def reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         # one whole step (every sequence of the workload) at the sampled rate
-        "ms_per_step": (1e3 * cfg.num_seqs / tps) if tps else None,
+        "ms_per_step": (1e3 * cfg.num_seqs * args.q_len / tps) if tps else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "tokens_per_s": tps,
@@ -381,7 +402,10 @@ def gpu_arm(args):
     _build.build()
 
     seed = None if args.seed is None and rank == 0 else (args.seed or 0) + 1000 * rank
-    st = make_workload(args.config, device, seed, args.num_seqs, args.kv_dtype)
+    if args.q_len > 1 and (args.kv_dtype != "bf16" or args.config == "parallel_sampling"):
+        raise SystemExit("--q-len > 1 runs the 16-bit cache on the decode workloads")
+    st = make_workload(args.config, device, seed, args.num_seqs, args.kv_dtype, q_len=args.q_len)
+    multi = args.q_len > 1
     Hq, Hkv, d, B = st["Hq"], st["Hkv"], st["d"], st["B"]
     N = len(st["ctx_h"])
     T = int(st["slots_h"].shape[0])
@@ -389,7 +413,7 @@ def gpu_arm(args):
     out = torch.empty_like(st["q"])
     fp8 = args.kv_dtype != "bf16"
     fmt = args.kv_dtype[4:] if fp8 else None
-    ws = None if fp8 else pa.workspace_for(st["q"], st["k_pool"], st["tables"])
+    ws = None if (fp8 or multi) else pa.workspace_for(st["q"], st["k_pool"], st["tables"])
     n_copies = int(st["copies"].shape[0])
     use_prefix = st["n_groups"] > 0 and not args.plain_decode and not fp8
 
@@ -409,6 +433,9 @@ def gpu_arm(args):
             ev[0].record(stream)
         if fp8:
             pa.pa_decode_fp8(q, st["k_pool"], tables, ctx, st["scale"], FP8_SCALE, FP8_SCALE, kv_format=fmt, out=out)
+        elif multi:
+            pa.pa_decode_multi(q, st["k_pool"], st["v_pool"], tables, ctx, st["q_start"], st["scale"],
+                               max_q_len=args.q_len, out=out)
         elif use_prefix:
             pa.pa_decode_shared_prefix(q, st["k_pool"], st["v_pool"], tables, ctx, st["group_starts"],
                                        st["group_prefix"], st["scale"], out=out)
@@ -451,14 +478,18 @@ def gpu_arm(args):
     host["slots"] = torch.from_numpy(st["slots_h"]).pin_memory()
     host["tables"] = torch.from_numpy(st["tables_h"]).pin_memory()
     host["ctx"] = torch.from_numpy(st["ctx_h"]).pin_memory()
+    if multi:
+        host["q_start"] = st["q_start"].cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dbuf = {k: torch.empty_like(v, device=device) for k, v in host.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
-        for k in ("q", "k_new", "v_new", "slots", "tables", "ctx"):
+        for k in host:
             dbuf[k].copy_(host[k], non_blocking=True)
+        if multi:
+            st["q_start"] = dbuf["q_start"]
         step(dbuf["q"], dbuf["k_new"], dbuf["v_new"], dbuf["slots"], dbuf["tables"], dbuf["ctx"])
         out_h.copy_(out, non_blocking=True)
 
@@ -477,12 +508,12 @@ def gpu_arm(args):
 
     # ---- numbers ----
     kv_elem = 1 if fp8 else 2
-    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem)
+    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem, q_len=args.q_len)
     ubytes = unique_decode_bytes(st["tables_h"], st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem) if st["shared"] else dbytes
     extra = append_bytes(T, Hkv, d, elem=kv_elem) + copy_bytes(n_copies, Hkv, B, d, elem=kv_elem)
     step_bytes = ubytes + extra
     value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
-    tokens = world * args.steps * N / (max_ms * 1e-3)
+    tokens = world * args.steps * N * args.q_len / (max_ms * 1e-3)
     e2e_value = world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
@@ -491,7 +522,7 @@ def gpu_arm(args):
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not fp8 else None
+    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not fp8 and not multi else None
 
     if rank != 0:
         return
@@ -504,7 +535,7 @@ def gpu_arm(args):
                "bytes_per_step": step_bytes,
                "l2": "inputs larger than L2 (KV stream %.2f GB per step), no flush" % (dbytes / 1e9),
                "parallelism": f"replicas x{world}", "truncated_batch": args.num_seqs,
-               "kv_cache": args.kv_dtype}
+               "kv_cache": args.kv_dtype, "q_len": args.q_len}
     if st["shared"]:
         cfg_out["bytes_note"] = ("value counts each shared physical block once (unique bytes); "
                                  "logical_gbs counts every sequence's reads")
@@ -519,7 +550,8 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
-                                "pa_decode_kernel (8-bit cache)" if fp8 else "pa_decode_kernel"),
+                                "pa_decode_kernel (8-bit cache)" if fp8 else
+                                "pa_multi_kernel" if multi else "pa_decode_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},

@@ -46,11 +46,14 @@ struct MultiTraits {
     static constexpr int ROWS = 16 * NW;
     static constexpr bool BF16 = BF16_;
     static constexpr int THREADS = 32 * NW;
-    static constexpr int MIN_CTAS = NW <= 4 ? 2 : 1;
-    static constexpr int R_FIT = (96 * 1024) / Gm::STAGE_BYTES;
-    static constexpr int R = R_FIT > 12 ? 12 : R_FIT;       // ring stages of the CTA
+    // about 8 warps per SM: 6 / 4 / 2 / 1 CTAs of 1 / 2 / 4 / 8 warps, sharing
+    // ~190 KiB of stages
+    static constexpr int MIN_CTAS = NW == 1 ? 6 : NW == 2 ? 4 : NW == 4 ? 2 : 1;
+    static constexpr int RING = (NW == 8 ? 192 : 160) * 1024 / MIN_CTAS;
+    static constexpr int R_FIT = RING / Gm::STAGE_BYTES;
+    static constexpr int R = R_FIT > 24 ? 24 : (R_FIT < 2 ? 2 : R_FIT);   // ring stages of the CTA
     static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad
-    static constexpr int CUM_SMEM = 512;
+    static constexpr int CUM_SMEM = 256;
     static constexpr int BAR_OFF = R * Gm::STAGE_BYTES;
     static constexpr int CUM_OFF = BAR_OFF + 2 * R * 8;
     static constexpr int CTX_OFF = CUM_OFF + (CUM_SMEM + 1) * 8;
