@@ -125,6 +125,43 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
                     void* stream);
 
 /*
+ * 4-bit integer (INT4) KV cache.  Compressing keys and values to 4 bits
+ * quadruples the requests that fit (ontq "AI Inference Serving at Scale",
+ * section 6); 4-bit integer formats carry per-group scale factors
+ * (letsbuildsolutions "How LLM Inference Engines Work", quantization).
+ * Format: one group per cached (token, KV head) row of K or of V, scale =
+ * amax / 7 (fp32), code = nearest integer to x / scale (fp32 division, ties to
+ * even) in [-8, 7]; a zero row has scale 0.  Decoding: code * scale.
+ * Layout: ONE pool of bytes [NB][Hkv][P] with P = B * d + 8 * B; each
+ * (block, KV head) piece holds the K codes token-major (B rows of d / 2
+ * bytes), the V codes dims-first (d rows of B / 2 bytes), then B fp32 K
+ * scales and B fp32 V scales.  Codes are stored as nibbles code + 8; in each
+ * little-endian 32-bit word of 8 elements, element 2k is nibble k and element
+ * 2k + 1 is nibble k + 4.  Supported: head_dim 128, B in {16, 32}, g in
+ * {1, 2, 4, 8, 16}; shape->dtype is the 16-bit type of q, out and new K/V.
+ *
+ * pa_append_kv_int4: quantize k_new / v_new ([T][Hkv][d]) into the pool at
+ * slot_mapping (negative skips; past the pool: PA_DEVERR_SLOT).
+ * pa_decode_int4: pa_decode over the 4-bit pool (attention over the decoded
+ * values); fp16 tensor-core arithmetic on the codes, the K scale applied to
+ * each score and the V scale to each softmax weight, fp32 accumulation.
+ * pa_copy_blocks_int4: copy-on-write copies of whole blocks of the pool.
+ */
+size_t pa_decode_int4_workspace_bytes(const pa_shape* shape);
+
+pa_status pa_decode_int4(const pa_shape* shape, const void* q, const void* kv_pool,
+                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                         void* out, void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                         void* stream);
+
+pa_status pa_append_kv_int4(const pa_shape* shape, int32_t num_tokens, const void* k_new,
+                            const void* v_new, const int64_t* slot_mapping, void* kv_pool,
+                            uint32_t* err_word, void* stream);
+
+pa_status pa_copy_blocks_int4(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs,
+                              void* kv_pool, uint32_t* err_word, void* stream);
+
+/*
  * Multi-token query paged attention: a chunk of new tokens per sequence
  * (chunked prefill -- thewebvale "vLLM & High-Throughput Serving", section 4;
  * speculative verification -- letsbuildsolutions "How LLM Inference Engines

@@ -21,6 +21,10 @@ from .ops import (  # noqa: F401
     pa_decode_fp8,
     pa_decode_shared_prefix,
     pa_decode_multi,
+    pa_decode_int4,
+    pa_append_kv_int4,
+    pa_copy_blocks_int4,
+    int4_pool,
     pa_decode_workspace_bytes,
     pa_read_error,
     workspace_for,

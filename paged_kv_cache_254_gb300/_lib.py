@@ -26,7 +26,8 @@ DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, 
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
            "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
            "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8",
-           "pa_copy_blocks_fp8", "pa_decode_multi_workspace_bytes", "pa_decode_multi")
+           "pa_copy_blocks_fp8", "pa_decode_multi_workspace_bytes", "pa_decode_multi",
+           "pa_decode_int4_workspace_bytes", "pa_decode_int4", "pa_append_kv_int4", "pa_copy_blocks_int4")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -105,6 +106,14 @@ def load() -> ctypes.CDLL:
         lib.pa_decode_multi_workspace_bytes.restype = SZ
         lib.pa_decode_multi.argtypes = [SP, I32, I32, P, P, P, P, P, P, ctypes.c_float, P, P, SZ, P, P]
         lib.pa_decode_multi.restype = I32
+        lib.pa_decode_int4_workspace_bytes.argtypes = [SP]
+        lib.pa_decode_int4_workspace_bytes.restype = SZ
+        lib.pa_decode_int4.argtypes = [SP, P, P, P, P, ctypes.c_float, P, P, SZ, P, P]
+        lib.pa_decode_int4.restype = I32
+        lib.pa_append_kv_int4.argtypes = [SP, I32, P, P, P, P, P, P]
+        lib.pa_append_kv_int4.restype = I32
+        lib.pa_copy_blocks_int4.argtypes = [SP, P, I32, P, P, P]
+        lib.pa_copy_blocks_int4.restype = I32
         _lib = lib
         return lib
 

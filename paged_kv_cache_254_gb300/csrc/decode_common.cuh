@@ -397,6 +397,162 @@ __device__ __forceinline__ void consume_stage8(uint32_t kb, int valid, const uin
     }
 }
 
+// The 4-bit cache (head_dim 128): a (block, KV head) piece is the K codes
+// token-major (BS rows of 64 bytes), the V codes dims-first (128 rows of
+// BS / 2 bytes), then BS fp32 K scales and BS fp32 V scales -- one
+// contiguous run of PIECE_BYTES in the pool.  Codes are nibbles code + 8; in
+// each 32-bit word of 8 elements, element 2k sits in nibble k and element
+// 2k + 1 in nibble k + 4.  A ring stage holds UB blocks of one pair: 32 tokens.
+template <int BS_>
+struct Geom4 {
+    static constexpr int D = 128;
+    static constexpr int BS = BS_;
+    static constexpr int VC = BS * 64;                 // V codes offset
+    static constexpr int KS = BS * 128;                // K scales offset
+    static constexpr int VS = KS + 4 * BS;             // V scales offset
+    static constexpr int PIECE_BYTES = VS + 4 * BS;
+    static constexpr int UB = 32 / BS;
+    static constexpr int STAGE_BYTES = UB * PIECE_BYTES;
+    static constexpr int NT = 4;
+    static constexpr int KT = 2;
+    static constexpr int KD = D / 16;
+    static_assert(BS == 16 || BS == 32, "block_size");
+    static_assert(PIECE_BYTES % 16 == 0, "pieces are copied in 16-byte units");
+};
+
+// consume_stage8 for the 4-bit cache.  Scores are sums over all dims of
+// q * code, scaled per token by its K scale; P is multiplied by each token's V
+// scale before the PV product (l keeps the plain weights).  Integer codes are
+// always finite, so masked slots need no zeroing; their scales (which may be
+// garbage) are replaced by 0 / skipped.
+template <class Gm, int NR>
+__device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
+                                               WarpAcc<Gm::D, NR>& acc, float scale_log2, int lane) {
+    constexpr int BS = Gm::BS, PIECE = Gm::PIECE_BYTES;
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    // per-token scales of this lane's columns: tokens 4 t4 .. + 3 and 16 + 4 t4 .. + 3
+    float ksc[2][4], vsc[2][4];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+        const int tok = 16 * hlf + 4 * t4;
+        if (16 * hlf < valid) {
+            const uint32_t pb = kb + (tok / BS) * PIECE + 4 * (tok % BS);
+            uint32_t w[4];
+            lds128(pb + Gm::KS, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ksc[hlf][i] = __uint_as_float(w[i]);
+            lds128(pb + Gm::VS, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vsc[hlf][i] = tok + i < valid ? __uint_as_float(w[i]) : 0.f;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ksc[hlf][i] = vsc[hlf][i] = 0.f;
+        }
+    }
+    float sacc[Gm::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        if (16 * (nt >> 1) < valid) {
+            const int tok = perm_token(nt, g);
+            uint32_t w[4];   // dims 32 t4 .. 32 t4 + 31 of token tok
+            lds128(kb + (tok / BS) * PIECE + (tok % BS) * 64 + 16 * t4, w);
+#pragma unroll
+            for (int kk = 0; kk < Gm::KD; ++kk) {
+                const int sh = 8 * (kk & 1);
+                const uint32_t b0 = i4x2_to_f16x2(w[kk >> 1] >> sh);
+                const uint32_t b1 = i4x2_to_f16x2(w[kk >> 1] >> (sh + 4));
+                mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            }
+        }
+    }
+
+    float mx[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) mx[r] = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tok = perm_token(nt, 2 * t4 + (e & 1));
+            const float ks = ksc[nt >> 1][2 * (nt & 1) + (e & 1)];
+            const float v = tok < valid ? sacc[nt][e] * ks * scale_log2 : -INFINITY;
+            sacc[nt][e] = v;
+            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], v);
+        }
+    float alpha[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float m_new = fmaxf(acc.m[r], mx[r]);
+        alpha[r] = ex2(acc.m[r] - m_new);
+        acc.m[r] = m_new;
+        acc.l[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = e >> 1;
+            if (r < NR) {
+                const float pe = ex2(sacc[nt][e] - acc.m[r]);
+                sacc[nt][e] = pe;
+                acc.l[r] += pe;
+            }
+        }
+    uint32_t pb[Gm::KT][NR][2], pl[Gm::KT][NR][2];
+#pragma unroll
+    for (int kt = 0; kt < Gm::KT; ++kt)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int nt = 2 * kt + h;
+                const float x0 = sacc[nt][2 * r] * vsc[kt][2 * h];
+                const float x1 = sacc[nt][2 * r + 1] * vsc[kt][2 * h + 1];
+                const uint32_t hi = pack2<false>(x0, x1);
+                pb[kt][r][h] = hi;
+                pl[kt][r][h] = pack2<false>(x0 - lo_of<false>(hi), x1 - hi_of<false>(hi));
+            }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
+        const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
+#pragma unroll
+        for (int mt = 0; mt < Gm::KD; ++mt) {
+            acc.o[mt][r][0] *= aa;
+            acc.o[mt][r][1] *= ab;
+            acc.o[mt][r][2] *= aa;
+            acc.o[mt][r][3] *= ab;
+        }
+    }
+#pragma unroll
+    for (int kt = 0; kt < Gm::KT; ++kt) {
+        if (16 * kt >= valid) break;
+        // V nibbles of tokens 16 kt + 4 t4 .. + 3 for dim rows g and g + 8
+        const int loc = (16 * kt) % BS + 4 * t4;
+        const uint32_t vb = kb + ((16 * kt) / BS) * PIECE + Gm::VC + 4 * (loc / 8);
+        const int sh = 8 * ((loc % 8) / 4);
+#pragma unroll
+        for (int mt = 0; mt < Gm::KD; ++mt) {
+            const uint32_t x = lds32(vb + (16 * mt + g) * (BS / 2));
+            const uint32_t y = lds32(vb + (16 * mt + g + 8) * (BS / 2));
+            const uint32_t a0 = i4x2_to_f16x2(x >> sh);
+            const uint32_t a2 = i4x2_to_f16x2(x >> (sh + 4));
+            const uint32_t a1 = i4x2_to_f16x2(y >> sh);
+            const uint32_t a3 = i4x2_to_f16x2(y >> (sh + 4));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
+                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
+            }
+        }
+    }
+}
+
 // Zero, in a 32-token 8-bit stage, the V bytes of tokens valid .. the end of
 // valid's 16-token group (0 < valid < 32; nothing when valid is a multiple
 // of 16, since consume_stage8 skips wholly masked groups).

@@ -72,11 +72,14 @@ struct DecodeParams {
     uint64_t timeout_ns;
 };
 
-// KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2.
+// KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2;
+// 3 = 4-bit integer codes with per-row scales.  KV8: any quantized cache (one
+// contiguous piece per (block, head), fetched by bulk copies).
 template <int D_, int BS_, int G_, bool BF16_, int KVF_ = 0>
 struct DecodeTraits {
     static constexpr bool KV8 = KVF_ != 0;
-    using Gm = std::conditional_t<KV8, Geom8<BS_>, Geom<D_, BS_>>;
+    static constexpr bool I4 = KVF_ == 3;
+    using Gm = std::conditional_t<I4, Geom4<BS_>, std::conditional_t<KV8, Geom8<BS_>, Geom<D_, BS_>>>;
     static constexpr int D = D_;
     static constexpr int BS = BS_;
     static constexpr int UB = Gm::UB;                       // blocks per stage
@@ -527,7 +530,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const int valid = min(nblk * BS, ctx - (it.first + it.b0 + b) * BS);
             const uint32_t kb = ring + st * Gm::STAGE_BYTES;
             bool zeroed = false;
-            if constexpr (Tr::KV8) {
+            if constexpr (Tr::I4) {
+                consume_stage4<Gm, Tr::NR>(kb, valid, qa, acc, p.scale_log2, lane);
+            } else if constexpr (Tr::KV8) {
                 if (valid < 32 && (valid & 15)) {
                     zero_v8_tail<Gm>(kb, valid, lane);
                     __syncwarp();
@@ -759,6 +764,9 @@ DecodeKernelInfo decode_info() {
 // Index: [bs == 32][log2(g)]; the 8-bit tables add [e5m2] in front.
 void decode8_table_bf16(DecodeKernelInfo (&t)[2][2][5]);
 void decode8_table_fp16(DecodeKernelInfo (&t)[2][2][5]);
+// 4-bit cache: [bs == 32][log2(g)]
+void decode4_table_bf16(DecodeKernelInfo (&t)[2][5]);
+void decode4_table_fp16(DecodeKernelInfo (&t)[2][5]);
 void decode_table_bf16_d128(DecodeKernelInfo (&t)[2][5]);
 void decode_table_bf16_d64(DecodeKernelInfo (&t)[2][5]);
 void decode_table_fp16_d128(DecodeKernelInfo (&t)[2][5]);

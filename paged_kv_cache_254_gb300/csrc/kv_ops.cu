@@ -149,6 +149,96 @@ pa_append8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict
     }
 }
 
+// Quantising append for the 4-bit cache (head_dim 128).  One warp per
+// (token, KV head) row; lane L holds dims 4L .. 4L + 3.  Per row: scale =
+// amax / 7 (fp32 division), code = rint(x / scale) clamped to [-8, 7] (0 for a
+// zero row).  K codes fill whole 32-bit words of the token's row; V is stored
+// dims-first, where neighbouring tokens share words, so each V nibble is set
+// with an atomic AND (clear) and OR (set) that touch only its own bits.
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+pa_append4_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                  const int64_t* __restrict__ slots, uint8_t* __restrict__ kv_pool, Append4Args a) {
+    constexpr int D = 128;
+    const int lane = threadIdx.x & 31;
+    const int BS = a.BS;
+    const int VC = BS * 64, KS = BS * 128, VS = KS + 4 * BS;
+    const long long rows = (long long)a.T * a.Hkv;
+    const long long wstride = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += wstride) {
+        const long long i = w / a.Hkv;
+        const int h = (int)(w - i * a.Hkv);
+        const long long slot = __ldg(slots + i);
+        if (slot < 0) continue;
+        if (slot >= a.num_slots) {
+            if (h == 0 && lane == 0 && a.err) atomicOr(a.err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const long long blk = slot / BS;
+        const int off = (int)(slot - blk * BS);
+        uint8_t* piece = kv_pool + (blk * a.Hkv + h) * (long long)a.piece_bytes;
+        const long long src = (i * a.Hkv + h) * D + 4 * lane;
+        auto widen = [](uint16_t x) -> float {
+            if constexpr (BF16) return __uint_as_float((uint32_t)x << 16);
+            return __half2float(__ushort_as_half(x));
+        };
+        const uint2 kw = __ldg(reinterpret_cast<const uint2*>(k_new + src));
+        const uint2 vw = __ldg(reinterpret_cast<const uint2*>(v_new + src));
+        float kx[4] = {widen(kw.x & 0xffffu), widen(kw.x >> 16), widen(kw.y & 0xffffu), widen(kw.y >> 16)};
+        float vx[4] = {widen(vw.x & 0xffffu), widen(vw.x >> 16), widen(vw.y & 0xffffu), widen(vw.y >> 16)};
+        float ka = 0.f, va = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ka = fmaxf(ka, fabsf(kx[e]));
+            va = fmaxf(va, fabsf(vx[e]));
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            ka = fmaxf(ka, __shfl_xor_sync(0xffffffffu, ka, o));
+            va = fmaxf(va, __shfl_xor_sync(0xffffffffu, va, o));
+        }
+        const float ks = __fdiv_rn(ka, 7.f), vs = __fdiv_rn(va, 7.f);
+        auto code = [](float x, float s) -> uint32_t {
+            if (!(s > 0.f)) return 8u;                       // code 0
+            const float q = fminf(fmaxf(rintf(__fdiv_rn(x, s)), -8.f), 7.f);
+            return (uint32_t)((int)q + 8);
+        };
+        auto nib = [](int e) -> int { return (e & 1) ? 4 + (e >> 1) : (e >> 1); };
+        // K: word lane / 2 of the token's row holds dims 8 (lane / 2) .. + 7
+        uint32_t part = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part |= code(kx[e], ks) << (4 * nib(4 * (lane & 1) + e));
+        part |= __shfl_xor_sync(0xffffffffu, part, 1);
+        if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(piece + off * 64 + 4 * (lane >> 1)) = part;
+        // V: dims-first rows of BS nibbles; this token is element off % 8 of word off / 8
+        const int pos = 4 * nib(off & 7);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            unsigned int* wp = reinterpret_cast<unsigned int*>(piece + VC + (4 * lane + e) * (BS / 2) + 4 * (off >> 3));
+            atomicAnd(wp, ~(0xfu << pos));
+            atomicOr(wp, code(vx[e], vs) << pos);
+        }
+        if (lane == 0) {
+            *reinterpret_cast<float*>(piece + KS + 4 * off) = ks;
+            *reinterpret_cast<float*>(piece + VS + 4 * off) = vs;
+        }
+    }
+}
+
+cudaError_t append4_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
+                           const Append4Args& a, bool bf16, cudaStream_t stream, int sms) {
+    const long long rows = (long long)a.T * a.Hkv;
+    long long blocks = (rows + 7) / 8;                    // 8 warps per CTA
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    auto kn = static_cast<const uint16_t*>(k_new);
+    auto vn = static_cast<const uint16_t*>(v_new);
+    auto kv = static_cast<uint8_t*>(kv_pool);
+    if (bf16) pa_append4_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
+    else pa_append4_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slots, kv, a);
+    return cudaGetLastError();
+}
+
 cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
                            const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms) {
     const long long total = (long long)a.T * a.Hkv * (a.D / 16);

@@ -29,6 +29,15 @@ struct Append8Args {
     uint32_t* err;
 };
 
+struct Append4Args {
+    int32_t T, Hkv, BS;
+    int32_t piece_bytes;   // bytes of one (block, head) piece
+    long long num_slots;
+    uint32_t* err;
+};
+
+cudaError_t append4_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
+                           const Append4Args& a, bool bf16, cudaStream_t stream, int sms);
 cudaError_t append8_launch(const void* k_new, const void* v_new, const int64_t* slots, void* kv_pool,
                            const Append8Args& a, bool bf16, bool e5m2, cudaStream_t stream, int sms);
 cudaError_t append_launch(const void* k_new, const void* v_new, const int64_t* slots, void* k_pool,

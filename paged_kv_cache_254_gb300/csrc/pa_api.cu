@@ -252,6 +252,28 @@ const DecodeKernelInfo* pick_decode8(const pa_shape* s, int kv_format) {
     return s->dtype == PA_BF16 ? &tab.bf[f][b][lg] : &tab.fp[f][b][lg];
 }
 
+// 4-bit cache: queries and new values in the shape's 16-bit dtype, head_dim 128.
+pa_status check_int4(const pa_shape* s) {
+    if (s->dtype != PA_FP16 && s->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (s->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (s->block_size != 16 && s->block_size != 32) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+int int4_piece_bytes(const pa_shape* s) { return s->block_size * s->head_dim + 8 * s->block_size; }
+
+const DecodeKernelInfo* pick_decode4(const pa_shape* s) {
+    static const auto tab = [] {
+        struct T { DecodeKernelInfo bf[2][5], fp[2][5]; } x;
+        decode4_table_bf16(x.bf);
+        decode4_table_fp16(x.fp);
+        return x;
+    }();
+    const int lg = log2_exact(s->num_q_heads / s->num_kv_heads);
+    const int b = s->block_size == 32 ? 1 : 0;
+    return s->dtype == PA_BF16 ? &tab.bf[b][lg] : &tab.fp[b][lg];
+}
+
 pa_status check_fp8(const pa_shape* s, int kv_format, float k_scale, float v_scale) {
     if (kv_format != PA_FP8_E4M3 && kv_format != PA_FP8_E5M2) return PA_ERR_INVALID_ARG;
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
@@ -727,6 +749,108 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
                                                                  d.N, d.Hkv, g, k->rows, ctas, max_q_len, total_q,
                                                                  shape->dtype == PA_BF16);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+
+size_t pa_decode_int4_workspace_bytes(const pa_shape* shape) {
+    const DecodeKernelInfo* k16 = nullptr;
+    if (pick_decode(shape, &k16) != PA_OK || check_int4(shape) != PA_OK) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const DecodeKernelInfo* k4 = pick_decode4(shape);
+    const int ctas = k4->max_ctas(dev);
+    if (ctas <= 0) return 0;
+    const long long workers = (long long)ctas * k4->workers;
+    return decode_region_bytes(shape, workers, kDynPerWorker * workers);
+}
+
+pa_status pa_decode_int4(const pa_shape* shape, const void* q, const void* kv_pool, const int32_t* block_tables,
+                         const int32_t* context_lens, float scale, void* out, void* workspace,
+                         size_t workspace_bytes, uint32_t* err_word, void* stream) {
+    const DecodeKernelInfo* k16 = nullptr;
+    pa_status st = pick_decode(shape, &k16);
+    if (st != PA_OK) return st;
+    st = check_int4(shape);
+    if (st != PA_OK) return st;
+    if (!q || !kv_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (shape->num_seqs == 0) return PA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    const DecodeKernelInfo* k = pick_decode4(shape);
+    const int ctas = k->max_ctas(dev);
+    if (ctas <= 0) return PA_ERR_CUDA;
+    if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    CUtensorMap unused{};   // every (block, head) piece is bulk-copied from p.kv8
+    DecodeLaunch L{};
+    L.tmap_k = &unused;
+    L.tmap_v = &unused;
+    L.p.q = static_cast<const uint16_t*>(q);
+    L.p.block_tables = block_tables;
+    L.p.context_lens = context_lens;
+    L.p.out = static_cast<uint16_t*>(out);
+    L.p.err = err_word;
+    L.p.kv8 = static_cast<const uint8_t*>(kv_pool);
+    L.p.v_scale = 1.0f;                              // per-row scales are applied inside
+    L.p.N = shape->num_seqs;
+    L.p.Hq = shape->num_q_heads;
+    L.p.Hkv = shape->num_kv_heads;
+    L.p.NB = shape->num_blocks;
+    L.p.MB = shape->max_blocks_per_seq;
+    L.p.scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
+    L.p.timeout_ns = kTimeoutNs;
+    L.stream = static_cast<cudaStream_t>(stream);
+    return run_decode(k, ctas, L, shape, workspace, workspace_bytes, nullptr);
+}
+
+pa_status pa_append_kv_int4(const pa_shape* shape, int32_t num_tokens, const void* k_new, const void* v_new,
+                            const int64_t* slot_mapping, void* kv_pool, uint32_t* err_word, void* stream) {
+    pa_status st = check_common(shape);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    st = check_int4(shape);
+    if (st != PA_OK) return st;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !kv_pool) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_pool, 16) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    Append4Args a;
+    a.T = num_tokens;
+    a.Hkv = shape->num_kv_heads;
+    a.BS = shape->block_size;
+    a.piece_bytes = int4_piece_bytes(shape);
+    a.num_slots = (long long)shape->num_blocks * shape->block_size;
+    a.err = err_word;
+    return append4_launch(k_new, v_new, slot_mapping, kv_pool, a, shape->dtype == PA_BF16,
+                          static_cast<cudaStream_t>(stream), sms) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks_int4(const pa_shape* shape, const int32_t* src_dst_pairs, int32_t num_pairs,
+                              void* kv_pool, uint32_t* err_word, void* stream) {
+    pa_status st = check_common(shape);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0) return PA_ERR_INVALID_ARG;
+    st = check_int4(shape);
+    if (st != PA_OK) return st;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_dst_pairs || !kv_pool || !aligned(kv_pool, 16) || !aligned(src_dst_pairs, 4)) return PA_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    CopyArgs a;
+    a.n = num_pairs;
+    a.vec_per_block = (long long)shape->num_kv_heads * int4_piece_bytes(shape) / 16;   // bytes / 16
+    a.NB = shape->num_blocks;
+    a.err = err_word;
+    return copy_launch(src_dst_pairs, kv_pool, nullptr, a, static_cast<cudaStream_t>(stream), sms) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -184,6 +184,16 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t v) {
     return r;
 }
 
+// Two 4-bit codes -> f16x2: nibbles at bits 0..3 and 16..19 of x hold
+// code + 8; OR-ing them under the fp16 pattern of 1024 gives 1024 + nibble
+// exactly, and subtracting 1032 leaves the code.
+__device__ __forceinline__ uint32_t i4x2_to_f16x2(uint32_t x) {
+    const uint32_t h = (x & 0x000f000fu) | 0x64006400u;
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
+    return r;
+}
+
 // Two floats -> two 8-bit float codes (low byte = first), round to nearest
 // even, finite values beyond the format's range saturate.
 template <bool E5M2>

@@ -330,3 +330,70 @@ def pa_copy_blocks_fp8(src_dst_pairs, kv_pool, kv_format="e4m3", err=None, strea
                                             ctypes.c_int32(src_dst_pairs.shape[0]), _ptr(kv_pool), _ptr(err),
                                             _stream(kv_pool.device, stream))
     _lib.check(st, "pa_copy_blocks_fp8")
+
+
+# --------------------------------------------------------------------------- 4-bit cache
+def int4_pool(num_blocks, num_kv_heads, block_size, head_dim=128, device="cuda"):
+    """A zeroed 4-bit pool.  Its tensor shape [NB, Hkv, B, d + 8] only sizes
+    the bytes of each (block, head) piece (B * d code nibbles + 8 * B scale
+    bytes); the piece layout itself is the one include/pa.h describes."""
+    return torch.zeros((num_blocks, num_kv_heads, block_size, head_dim + 8), dtype=torch.uint8, device=device)
+
+
+def _need_pool4(kv_pool):
+    _need_cuda("kv_pool", kv_pool, torch.uint8)
+    if kv_pool.dim() != 4:
+        raise ValueError("kv_pool must be uint8 [NB, Hkv, B, d + 8] (see int4_pool)")
+    return kv_pool.shape[0], kv_pool.shape[1], kv_pool.shape[2], kv_pool.shape[3] - 8
+
+
+def pa_decode_int4(q, kv_pool, block_tables, context_lens, scale, out=None, workspace=None, err=None,
+                   stream=None):
+    """Decode over the 4-bit cache (see include/pa.h)."""
+    _need_cuda("q", q)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    NB, Hkv, B, d = _need_pool4(kv_pool)
+    N, Hq, dq = q.shape
+    if dq != d or block_tables.shape[0] != N:
+        raise ValueError("q [N, Hq, d] and kv_pool [NB, Hkv, B, d + 8] disagree")
+    out = torch.empty_like(q) if out is None else out
+    shape = make_shape(N, Hq, Hkv, d, B, NB, block_tables.shape[1], q.dtype)
+    lib = _lib.load()
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            need = int(lib.pa_decode_int4_workspace_bytes(ctypes.byref(shape)))
+            workspace = _shared_workspace(q.device, max(need, 1), stream)
+        st = lib.pa_decode_int4(ctypes.byref(shape), _ptr(q), _ptr(kv_pool), _ptr(block_tables),
+                                _ptr(context_lens), ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                                ctypes.c_size_t(workspace.numel() * workspace.element_size()), _ptr(err),
+                                _stream(q.device, stream))
+    _lib.check(st, "pa_decode_int4")
+    return out
+
+
+def pa_append_kv_int4(k_new, v_new, slot_mapping, kv_pool, err=None, stream=None):
+    """Quantize k_new / v_new [T, Hkv, d] (fp16/bf16) into the 4-bit pool."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new, k_new.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    NB, Hkv, B, d = _need_pool4(kv_pool)
+    T = slot_mapping.shape[0]
+    shape = make_shape(0, 1, Hkv, d, B, NB, 1, k_new.dtype)
+    with torch.cuda.device(kv_pool.device):
+        st = _lib.load().pa_append_kv_int4(ctypes.byref(shape), ctypes.c_int32(T), _ptr(k_new), _ptr(v_new),
+                                           _ptr(slot_mapping), _ptr(kv_pool), _ptr(err),
+                                           _stream(kv_pool.device, stream))
+    _lib.check(st, "pa_append_kv_int4")
+
+
+def pa_copy_blocks_int4(src_dst_pairs, kv_pool, dtype=torch.bfloat16, err=None, stream=None):
+    """Copy-on-write copies of whole blocks of the 4-bit pool."""
+    _need_cuda("src_dst_pairs", src_dst_pairs, torch.int32)
+    NB, Hkv, B, d = _need_pool4(kv_pool)
+    shape = make_shape(0, 1, Hkv, d, B, NB, 1, dtype)
+    with torch.cuda.device(kv_pool.device):
+        st = _lib.load().pa_copy_blocks_int4(ctypes.byref(shape), _ptr(src_dst_pairs),
+                                             ctypes.c_int32(src_dst_pairs.shape[0]), _ptr(kv_pool), _ptr(err),
+                                             _stream(kv_pool.device, stream))
+    _lib.check(st, "pa_copy_blocks_int4")

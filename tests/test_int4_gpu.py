@@ -1,0 +1,131 @@
+"""The 4-bit cache on the GPU: the quantising append is byte-exact against the
+oracle's quantiser; decode over random 4-bit pools matches the fp64 oracle on
+the decoded values; whole-block copies are byte-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import decode_ref
+from oracle.int4 import append_int4_ref, dequantize_rows, dequantized_pools, split_piece
+from tests.gpu_util import assert_close, dev_case, need_gpu
+from workloads import CONFIGS, DecodeConfig, make_decode_case, make_int4_pool, make_values
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def pa():
+    import paged_kv_cache_254_gb300 as m
+    return m
+
+
+def flat(pool):
+    NB, Hkv = pool.shape[0], pool.shape[1]
+    return pool.reshape(NB, Hkv, -1).cpu().numpy()
+
+
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_append_is_byte_exact(B, dtype):
+    NB, Hkv, d, T = 12, 3, 128, 40
+    g = torch.Generator(device="cuda").manual_seed(B)
+    pool = torch.randint(0, 256, (NB, Hkv, B, d + 8), generator=g, device="cuda", dtype=torch.int32).to(torch.uint8)
+    kn = make_values((T, Hkv, d), dtype, g, "cuda") * 3
+    vn = make_values((T, Hkv, d), dtype, g, "cuda")
+    kn[0, 0] = 0                                         # a zero row: scale 0, codes 0
+    r = np.random.Generator(np.random.PCG64(B + 1))
+    slots = r.permutation(NB * B)[:T].astype(np.int64)
+    slots[3] = -1                                        # skipped
+    want = append_int4_ref(flat(pool), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, B)
+    pa().pa_append_kv_int4(kn, vn, torch.from_numpy(slots).cuda(), pool)
+    got = flat(pool)
+    assert (got == want).all(), f"{int((got != want).sum())} bytes differ"
+
+
+def int4_case(ctx, Hq, Hkv, B, dtype, seed):
+    cfg = DecodeConfig(name="int4", num_seqs=len(ctx), num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,
+                       block_size=B, dtype=dtype, seed=seed, ctx_fixed=tuple(ctx), pool_factor=1.3)
+    case = make_decode_case(cfg, device="cuda", values=False)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    case.q = make_values((len(ctx), Hq, 128), dtype, g, "cuda")
+    pool = make_int4_pool(case.num_blocks, Hkv, B, 128, g, "cuda")
+    return case, pool
+
+
+def decode(case, pool, **kw):
+    bt, cl = dev_case(case)
+    return pa().pa_decode_int4(case.q, pool, bt, cl, case.scale, **kw)
+
+
+EDGE = [1, 2, 15, 16, 17, 31, 32, 33, 48, 100, 513]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("g", [1, 4, 8, 16])
+def test_decode_matches_oracle(dtype, B, g):
+    Hkv = 2
+    case, pool = int4_case(EDGE, Hkv * g, Hkv, B, dtype, seed=100 + B + g)
+    kf, vf = dequantized_pools(flat(pool), B, 128)
+    want = decode_ref(case.q, kf, vf, case.block_tables, case.context_lens, case.scale)
+    assert_close(decode(case, pool), want, what=f"int4 {dtype} B{B} g{g}")
+
+
+def test_long_contexts_and_splits():
+    ctx = [30000, 5, 12000, 800]
+    case, pool = int4_case(ctx, 8, 1, 16, "bf16", seed=7)
+    kf, vf = dequantized_pools(flat(pool), 16, 128)
+    want = decode_ref(case.q, kf, vf, case.block_tables, case.context_lens, case.scale)
+    assert_close(decode(case, pool), want, what="long int4")
+
+
+def test_copy_blocks_is_byte_exact():
+    NB, Hkv, B = 16, 4, 16
+    g = torch.Generator(device="cuda").manual_seed(3)
+    pool = make_int4_pool(NB, Hkv, B, 128, g, "cuda")
+    before = pool.clone()
+    pairs = torch.tensor([[1, 9], [4, 2], [7, 7]], dtype=torch.int32, device="cuda")
+    pa().pa_copy_blocks_int4(pairs, pool)
+    want = before.clone()
+    want[9] = before[1]
+    want[2] = before[4]
+    assert torch.equal(pool, want)
+
+
+def test_full_size_batch_sampled():
+    # the 70B-shaped batch over a 4-bit pool, checked on sampled sequences
+    cfg = CONFIGS["llama3_70b_b256"]
+    case = make_decode_case(cfg, device="cuda", values=False)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    case.q = make_values((cfg.num_seqs, cfg.num_q_heads, 128), cfg.dtype, g, "cuda")
+    pool = make_int4_pool(case.num_blocks, cfg.num_kv_heads, cfg.block_size, 128, g, "cuda")
+    out = decode(case, pool)
+    assert torch.isfinite(out.float()).all()
+    seqs = [0, 77, 255]
+    B = cfg.block_size
+    for s in seqs:
+        nb = -(-int(case.context_lens[s]) // B)
+        ids = case.block_tables[s, :nb]
+        sub = pool[torch.from_numpy(ids.astype(np.int64)).cuda()]
+        kf, vf = dequantized_pools(flat(sub), B, 128)
+        want = decode_ref(case.q[s:s + 1], kf, vf, np.arange(nb)[None, :], case.context_lens[s:s + 1], case.scale)
+        assert_close(out[s:s + 1], want, what=f"sequence {s}")
+
+
+def test_dequantized_values_round_trip_through_append():
+    # appended rows decode (oracle side) to code * scale of the pages' rule
+    from oracle.int4 import quantize_rows
+    NB, Hkv, B, d = 4, 2, 16, 128
+    pool = pa().int4_pool(NB, Hkv, B, d)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    kn = make_values((2, Hkv, d), "bf16", g, "cuda")
+    vn = make_values((2, Hkv, d), "bf16", g, "cuda")
+    pa().pa_append_kv_int4(kn, vn, torch.tensor([5, 40], dtype=torch.int64, device="cuda"), pool)
+    K, V, ks, vs = split_piece(flat(pool)[40 // B, 1], B, d)
+    kq, ksc = quantize_rows(kn[1, 1].float().cpu().numpy())
+    np.testing.assert_array_equal(dequantize_rows(K[40 % B], ks[40 % B]), dequantize_rows(kq, ksc))

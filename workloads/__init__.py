@@ -15,6 +15,7 @@ from .synth import (  # noqa: F401
     SamplingConfig,
     SamplingCase,
     make_codes,
+    make_int4_pool,
     make_decode_case,
     make_sampling_case,
     make_values,

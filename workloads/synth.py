@@ -326,3 +326,24 @@ def make_codes(shape, gen: torch.Generator, device, below: int = 0x50) -> torch.
     mag = torch.randint(0, below, shape, generator=gen, device=device, dtype=torch.int32)
     sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32)
     return (mag | (sign << 7)).to(torch.uint8)
+
+
+def make_int4_pool(num_blocks, num_kv_heads, block_size, head_dim, gen: torch.Generator, device,
+                   scale_range=(0.05, 0.4)) -> torch.Tensor:
+    """Random contents for a 4-bit pool (uint8 [NB, Hkv, B, d + 8]): each piece
+    is B * d random code bytes followed by 2 * B fp32 scales drawn uniformly
+    from scale_range.  Any nibble is a valid code, so every piece decodes to
+    finite values."""
+    NB, Hkv, B, d = num_blocks, num_kv_heads, block_size, head_dim
+    pool = torch.empty((NB, Hkv, B * (d + 8)), dtype=torch.uint8, device=device)
+    codes = B * d
+    step = max(1, (1 << 26) // max(1, Hkv * B * (d + 8)))
+    lo, hi = scale_range
+    for b0 in range(0, NB, step):
+        b1 = min(NB, b0 + step)
+        pool[b0:b1, :, :codes] = torch.randint(0, 256, (b1 - b0, Hkv, codes), generator=gen, device=device,
+                                               dtype=torch.int32).to(torch.uint8)
+        sc = torch.rand((b1 - b0, Hkv, 2 * B), generator=gen, device=device) * (hi - lo) + lo
+        pool[b0:b1, :, codes:] = sc.contiguous().view(torch.uint8).view(b1 - b0, Hkv, 8 * B)
+    return pool.view(NB, Hkv, B, d + 8)
+
