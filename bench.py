@@ -65,8 +65,9 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3", "fp8_e5m2"], default="bf16",
-                    help="cache element type (fp8: 8-bit cache, quantising append, 8-bit decode)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3", "fp8_e5m2", "int4"], default="bf16",
+                    help="cache element type (fp8: 8-bit cache, int4: 4-bit cache with per-row scales; "
+                         "quantising append, quantized decode)")
     ap.add_argument("--plain-decode", action="store_true",
                     help="decode shared-prompt batches without the prefix-aware pass")
     ap.add_argument("--q-len", type=int, default=1,
@@ -79,25 +80,26 @@ def parse_args(argv=None):
 
 
 # --------------------------------------------------------------------------- accounting
-def decode_bytes(ctx, Hq, Hkv, d, B, elem=2, q_elem=2, q_len=1) -> int:
+def decode_bytes(ctx, Hq, Hkv, d, B, elem=2, q_elem=2, q_len=1, row_extra=0) -> int:
     """Bytes the method must move for one decode call: every cached K and V
-    element once (elem bytes each), Q and O once (q_len rows per sequence),
-    the block-table entries in use and the context lengths."""
+    element once (elem bytes each, plus row_extra bytes of scales per cached
+    (token, head)), Q and O once (q_len rows per sequence), the block-table
+    entries in use and the context lengths."""
     ctx = [int(c) for c in ctx]
-    kv = sum(ctx) * Hkv * d * elem * 2
+    kv = int(sum(ctx) * Hkv * (d * elem * 2 + row_extra))
     qo = 2 * len(ctx) * q_len * Hq * d * q_elem
     tables = sum(-(-c // B) for c in ctx) * 4
     return kv + qo + tables + 4 * len(ctx)
 
 
-def append_bytes(T, Hkv, d, elem=2, new_elem=2) -> int:
+def append_bytes(T, Hkv, d, elem=2, new_elem=2, row_extra=0) -> int:
     """K and V rows read (new_elem bytes each) and written to the cache (elem
-    bytes each), plus the int64 slots."""
-    return T * Hkv * d * (elem + new_elem) * 2 + 8 * T
+    bytes each, plus row_extra bytes of scales), plus the int64 slots."""
+    return int(T * Hkv * (d * (elem + new_elem) * 2 + row_extra)) + 8 * T
 
 
-def copy_bytes(n, Hkv, B, d, elem=2) -> int:
-    return 2 * n * Hkv * B * d * elem * 2
+def copy_bytes(n, Hkv, B, d, elem=2, row_extra=0) -> int:
+    return int(2 * n * Hkv * B * (d * elem * 2 + row_extra))
 
 
 def measured_peaks() -> dict:
@@ -261,7 +263,17 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16", q_len=1) -
     gstarts, gprefix = bm.shared_prefix_groups(seqs)
     slots = slots.astype(np.int64)
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
-    if kv_dtype != "bf16":
+    if kv_dtype == "int4":
+        # a 4-bit cache of random codes and scales, one piece per (block, head)
+        from workloads import make_int4_pool
+        g4 = torch.Generator(device=device).manual_seed((seed or 0) + 99)
+        NB, Hkv_, B_, d_ = case.k_pool.shape
+        case.k_pool = None
+        case.v_pool = None
+        torch.cuda.empty_cache()
+        case.k_pool = make_int4_pool(NB, Hkv_, B_, d_, g4, device)
+        case.v_pool = None
+    elif kv_dtype != "bf16":
         # an 8-bit cache of random codes: per (block, head) K rows, then V dims-first
         from workloads import make_codes
         g8 = torch.Generator(device=device).manual_seed((seed or 0) + 99)
@@ -411,27 +423,35 @@ def gpu_arm(args):
     T = int(st["slots_h"].shape[0])
     stream = torch.cuda.current_stream(device)
     out = torch.empty_like(st["q"])
-    fp8 = args.kv_dtype != "bf16"
+    quant = args.kv_dtype != "bf16"
+    int4 = args.kv_dtype == "int4"
+    fp8 = quant and not int4
     fmt = args.kv_dtype[4:] if fp8 else None
-    ws = None if (fp8 or multi) else pa.workspace_for(st["q"], st["k_pool"], st["tables"])
+    ws = None if (quant or multi) else pa.workspace_for(st["q"], st["k_pool"], st["tables"])
     n_copies = int(st["copies"].shape[0])
-    use_prefix = st["n_groups"] > 0 and not args.plain_decode and not fp8
+    use_prefix = st["n_groups"] > 0 and not args.plain_decode and not quant
 
     def step(q, k_new, v_new, slots, tables, ctx, ev=None):
         launches = 0
         if n_copies:
-            if fp8:
+            if int4:
+                pa.pa_copy_blocks_int4(st["copies"], st["k_pool"])
+            elif fp8:
                 pa.pa_copy_blocks_fp8(st["copies"], st["k_pool"], kv_format=fmt)
             else:
                 pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
             launches += 1
-        if fp8:
+        if int4:
+            pa.pa_append_kv_int4(k_new, v_new, slots, st["k_pool"])
+        elif fp8:
             pa.pa_append_kv_fp8(k_new, v_new, slots, st["k_pool"], FP8_SCALE, FP8_SCALE, kv_format=fmt)
         else:
             pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
             ev[0].record(stream)
-        if fp8:
+        if int4:
+            pa.pa_decode_int4(q, st["k_pool"], tables, ctx, st["scale"], out=out)
+        elif fp8:
             pa.pa_decode_fp8(q, st["k_pool"], tables, ctx, st["scale"], FP8_SCALE, FP8_SCALE, kv_format=fmt, out=out)
         elif multi:
             pa.pa_decode_multi(q, st["k_pool"], st["v_pool"], tables, ctx, st["q_start"], st["scale"],
@@ -507,10 +527,12 @@ def gpu_arm(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, device)
 
     # ---- numbers ----
-    kv_elem = 1 if fp8 else 2
-    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem, q_len=args.q_len)
+    kv_elem = 0.5 if int4 else 1 if fp8 else 2
+    rx = 8 if int4 else 0                          # fp32 K and V scale per cached (token, head)
+    dbytes = decode_bytes(st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem, q_len=args.q_len, row_extra=rx)
     ubytes = unique_decode_bytes(st["tables_h"], st["ctx_h"], Hq, Hkv, d, B, elem=kv_elem) if st["shared"] else dbytes
-    extra = append_bytes(T, Hkv, d, elem=kv_elem) + copy_bytes(n_copies, Hkv, B, d, elem=kv_elem)
+    extra = (append_bytes(T, Hkv, d, elem=kv_elem, row_extra=rx) +
+             copy_bytes(n_copies, Hkv, B, d, elem=kv_elem, row_extra=rx))
     step_bytes = ubytes + extra
     value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
     tokens = world * args.steps * N * args.q_len / (max_ms * 1e-3)
@@ -522,7 +544,7 @@ def gpu_arm(args):
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not fp8 and not multi else None
+    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not quant and not multi else None
 
     if rank != 0:
         return
@@ -542,7 +564,7 @@ def gpu_arm(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not fp8 else f"bf16 q/out, {fmt} cache",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not quant else f"bf16 q/out, {args.kv_dtype} cache",
         "data": "synthetic (seeded N(0,1) values, random block placement)",
         "config": cfg_out,
         "tokens_per_s": round(tokens, 1),
@@ -550,6 +572,7 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
+                                "pa_decode_kernel (4-bit cache)" if int4 else
                                 "pa_decode_kernel (8-bit cache)" if fp8 else
                                 "pa_multi_kernel" if multi else "pa_decode_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs",
