@@ -251,6 +251,10 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
     if (warp == NC) {
         // =========================== producer ===========================
+        // Stages are filled in rounds: lane j probes (without blocking)
+        // whether ring stage issued + j is free, and the leading run of free
+        // stages is filled at once, one stage per lane; lane 0 blocks only when
+        // the oldest stage is still in use.
         long long issued = 0;
         bool aborted = false;
         ItemIter it = it0;
@@ -261,42 +265,53 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             for (int base = 0; base < len && !aborted; base += 32) {
                 const int nxt = base + 32 + lane < len ? __ldg(trow + base + 32 + lane) : 0;
                 const int cnt = min(32, len - base);
-                for (int i = 0; i < cnt; ++i) {
-                    int id = __shfl_sync(0xffffffffu, tcur, i);
-                    int ok = 1;
-                    if (lane == 0) {
-                        const int st = (int)(issued % S);
-                        if (issued >= S) {
-                            const uint32_t par = (uint32_t)(((issued / S) - 1) & 1);
-                            if (!mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns)) ok = 0;
-                        }
-                        if (ok) {
-                            const bool bad = (unsigned)id >= (unsigned)p.NB;
-                            if (bad) {
-                                set_err(p.err, PA_DEVERR_BLOCK_ID);
-                                id = 0;
+                int done = 0;
+                while (done < cnt) {
+                    const int want = min(cnt - done, S);
+                    const long long my = issued + lane;
+                    bool is_free = false;
+                    if (lane < want)
+                        is_free = my < S || mbar_test_wait(empty0 + 8 * (uint32_t)(my % S),
+                                                           (uint32_t)(((my / S) - 1) & 1));
+                    const unsigned fm = __ballot_sync(0xffffffffu, is_free);
+                    int run = (fm == 0xffffffffu) ? 32 : __ffs(~fm) - 1;
+                    if (run == 0) {
+                        int ok = 1;
+                        if (lane == 0)
+                            ok = mbar_wait_bounded(empty0 + 8 * (uint32_t)(issued % S),
+                                                   (uint32_t)(((issued / S) - 1) & 1), p.timeout_ns) ? 1 : 0;
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) {
+                            if (lane == 0) {
+                                set_err(p.err, PA_DEVERR_TIMEOUT);
+                                *(volatile int*)&info->abort = 1;
                             }
-                            stage_poison[st] = bad ? 1 : 0;
-                            const uint32_t fb = full0 + 8 * st;
-                            mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-                            const int y = (id * p.Hkv + it.kvh) * BS;
-                            const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
+                            aborted = true;
+                            break;
+                        }
+                        run = 1;
+                    }
+                    int id = __shfl_sync(0xffffffffu, tcur, (done + lane) & 31);
+                    if (lane < run) {
+                        const int st = (int)(my % S);
+                        const bool bad = (unsigned)id >= (unsigned)p.NB;
+                        if (bad) {
+                            set_err(p.err, PA_DEVERR_BLOCK_ID);
+                            id = 0;
+                        }
+                        stage_poison[st] = bad ? 1 : 0;
+                        const uint32_t fb = full0 + 8 * st;
+                        mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                        const int y = (id * p.Hkv + it.kvh) * BS;
+                        const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
 #pragma unroll
-                            for (int h = 0; h < Gm::HALVES; ++h) {
-                                tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                                tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-                            }
-                        } else {
-                            set_err(p.err, PA_DEVERR_TIMEOUT);
-                            *(volatile int*)&info->abort = 1;
+                        for (int h = 0; h < Gm::HALVES; ++h) {
+                            tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
+                            tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
                         }
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) {
-                        aborted = true;
-                        break;
-                    }
-                    ++issued;
+                    issued += run;
+                    done += run;
                 }
                 tcur = nxt;
             }
