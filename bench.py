@@ -574,7 +574,8 @@ def gpu_arm(args):
                      "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
                                 "pa_decode_kernel (4-bit cache)" if int4 else
                                 "pa_decode_kernel (8-bit cache)" if fp8 else
-                                "pa_multi_kernel" if multi else "pa_decode_kernel"),
+                                ("pa_multi_tc_kernel (tcgen05)" if args.q_len * Hq // Hkv >= 33 else
+                                 "pa_multi_kernel (mma.sync)") if multi else "pa_decode_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},

@@ -178,6 +178,7 @@ struct MultiParams {
     const int32_t* q_start;       // [N + 1] first query row of each sequence
     int32_t max_q;                // the launch's largest chunk (q_len above it is an error)
     int32_t total_q;              // T: rows of q and out
+    int32_t q_box;                // tokens per Q tile copy (tensor-core kernel: min(max_q, T))
 };
 
 template <class Tr>
@@ -526,6 +527,7 @@ pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_
 }
 
 struct MultiLaunch {
+    const CUtensorMap* tmap_q;   // tensor-core kernel only: q as [T][Hq][D]
     const CUtensorMap* tmap_k;
     const CUtensorMap* tmap_v;
     MultiParams p;

@@ -3,6 +3,7 @@
 // allocates device memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -11,6 +12,7 @@
 #include "decode_kernel.cuh"
 #include "kv_ops.cuh"
 #include "multi_kernel.cuh"
+#include "multi_tc_kernel.cuh"
 #include "prefix_kernel.cuh"
 
 namespace {
@@ -231,6 +233,23 @@ bool pool_map(CUtensorMap* m, const void* pool, const pa_shape* s) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [T][Hq][D] as a 3-D tensor (head_dim, heads, tokens): boxes of 64
+// columns x g heads x q_box tokens land as rows i * g + hh, 128-byte swizzled.
+bool q_map(CUtensorMap* m, const void* q, const pa_shape* s, int total_q, int q_box) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int g = s->num_q_heads / s->num_kv_heads;
+    const cuuint64_t dims[3] = {(cuuint64_t)s->head_dim, (cuuint64_t)s->num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {(cuuint64_t)s->head_dim * 2, (cuuint64_t)s->num_q_heads * s->head_dim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)q_box};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_sms() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -315,6 +334,22 @@ pa_status pick_multi(const pa_shape* s, int max_q, const MultiKernelInfo** out) 
     }();
     *out = &tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32][log2_exact(nw)];
     return PA_OK;
+}
+
+// Launches whose pairs carry at least this many query rows run on the
+// tensor-core (tcgen05) kernel: 128-row MMA tiles, one CTA per SM.
+constexpr int kTcMinRows = 33;
+
+const MultiKernelInfo* pick_multi_tc(const pa_shape* s) {
+    static const auto tab = [] {
+        struct T { MultiKernelInfo t[2][2][2]; } x;      // [bf16][d == 128][bs == 32]
+        multi_tc_table_fp16_d64(x.t[0][0]);
+        multi_tc_table_fp16_d128(x.t[0][1]);
+        multi_tc_table_bf16_d64(x.t[1][0]);
+        multi_tc_table_bf16_d128(x.t[1][1]);
+        return x;
+    }();
+    return &tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32];
 }
 
 // Scratch of a multi-token launch: chunk counter, block prefix sums, two
@@ -677,7 +712,14 @@ size_t pa_decode_multi_workspace_bytes(const pa_shape* shape, int32_t max_q_len)
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int ctas = k->max_ctas(dev);
     if (ctas <= 0) return 0;
-    return multi_region_bytes(shape, ctas, k->rows);
+    size_t need = multi_region_bytes(shape, ctas, k->rows);
+    if (max_q_len * (shape->num_q_heads / shape->num_kv_heads) >= kTcMinRows) {
+        const MultiKernelInfo* t = pick_multi_tc(shape);
+        const int tctas = t->max_ctas(dev);
+        if (tctas <= 0) return 0;
+        need = std::max(need, multi_region_bytes(shape, tctas, t->rows));
+    }
+    return need;
 }
 
 pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t total_q, const void* q,
@@ -688,6 +730,9 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     pa_status st = pick_multi(shape, max_q_len, &k);
     if (st != PA_OK) return st;
     if (total_q < 0) return PA_ERR_INVALID_ARG;
+    const int g_rows = max_q_len * (shape->num_q_heads / shape->num_kv_heads);
+    const bool tc = g_rows >= kTcMinRows && total_q > 0;
+    if (tc) k = pick_multi_tc(shape);
     if (!q_start || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
@@ -701,11 +746,14 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     if (ctas <= 0) return PA_ERR_CUDA;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < multi_region_bytes(shape, ctas, k->rows))
         return PA_ERR_WORKSPACE;
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, mq;
     if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+    const int q_box = std::min(max_q_len, total_q);
+    if (tc && !q_map(&mq, q, shape, total_q, q_box)) return PA_ERR_CUDA;
 
     uint8_t* base = static_cast<uint8_t*>(workspace);
     MultiLaunch L{};
+    L.tmap_q = tc ? &mq : nullptr;
     L.tmap_k = &mk;
     L.tmap_v = &mv;
     DecodeParams& d = L.p.d;
@@ -728,6 +776,7 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     L.p.q_start = q_start;
     L.p.max_q = max_q_len;
     L.p.total_q = total_q;
+    L.p.q_box = q_box;
     L.stream = static_cast<cudaStream_t>(stream);
     L.grid = ctas;
     pa_decode_prepass<<<1, 1024, 0, L.stream>>>(context_lens, nullptr, shape->num_seqs,
