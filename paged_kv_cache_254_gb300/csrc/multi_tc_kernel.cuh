@@ -13,20 +13,24 @@
 //   S  = Q K^T   M 128, N 64, K = head_dim   (Q, K: K-major swizzled tiles)
 //   O += P V     M 128, N = head_dim, K 64   (P: K-major; V: MN-major tile)
 //
-// with S (two 64-column buffers) and O (fp32) in tensor memory.  P enters as
-// a hi + lo pair of 16-bit values (two MMAs), keeping ~16 bits of each weight
-// as the mma.sync kernels do.
+// with S (two 64-column fp32 buffers), P (two buffers of 16-bit weights, the
+// A operand of the PV product) and O (fp32) all in tensor memory.  P enters
+// as a hi + lo pair of 16-bit values (two MMAs), keeping ~16 bits of each
+// weight as the mma.sync kernels do.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warps 0-3  softmax: thread = query row = TMEM lane.  Loads the stage's
-//              scores, masks per row (causal limit), runs the online softmax
-//              and writes P to shared memory; zeroes the V rows of a stage
-//              past the context; at a segment end loads O and writes the
-//              output rows or the partial state.
-//   warp 4     copies: per segment the Q tile (one 3-D TMA per 64-column
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-7  softmax: warp w handles rows 32 (w % 4) .. + 31 (its TMEM lane
+//              quarter; thread = query row) and keys 32 (w / 4) .. + 31 of
+//              each stage; the two warps of a row quarter exchange their
+//              partial row maxima through shared memory.  Masks per row
+//              (causal limit), runs the online softmax and writes P to
+//              TMEM; zeroes the V rows of a stage past the context; at a
+//              segment end loads its half of O and writes the output rows or
+//              the partial state.
+//   warp 8     copies: per segment the Q tile (one 3-D TMA per 64-column
 //              half: box = g heads x max_q tokens, landing as rows i * g + hh),
 //              per stage the K and V boxes of its blocks (2-D TMA).
-//   warp 5     MMA: allocates TMEM; issues S of stage j + 1 before PV of
+//   warp 9     MMA: allocates TMEM; issues S of stage j + 1 before PV of
 //              stage j so the softmax of one stage overlaps the tensor core.
 //
 // Lazy rescaling.  A row keeps the reference maximum m_ref used for its
@@ -60,46 +64,73 @@ struct TcTraits {
     static constexpr int HALF_BYTES = KEYS * 128;            // one column half of a stage's K or V
     static constexpr int KV_BYTES = HALVES * HALF_BYTES;
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;         // K, then V
-    static constexpr int P_TILE = ROWS * 128;                // 64 16-bit weights per row
-    static constexpr int P_OFF = Q_BYTES;                    // [buffer][hi, lo] tiles
-    static constexpr int RING_OFF = P_OFF + 4 * P_TILE;
+    static constexpr int RING_OFF = Q_BYTES;
     static constexpr int SMEM_CAP = 227 * 1024;
     static constexpr int REC_BYTES = 48;
-    static constexpr int NBAR_FIXED = 11;                    // s_full[2] s_free[2] p_full[2] pv_done[2] q_full q_empty fin
-    static constexpr int R_FIT = (SMEM_CAP - 1024 - RING_OFF - 8 * (16 + NBAR_FIXED) - 8 * REC_BYTES - 16) /
-                                 STAGE_BYTES;
-    static constexpr int R = R_FIT > 8 ? 8 : R_FIT;
+    static constexpr int NBAR_FIXED = 12;    // s_full[2] s_free[2] p_full[2] pv_done[2] q_full q_empty fin o_free
+    // tagged cells per row: softmax references along a segment's stages [4],
+    // and the partial row sums handed to a segment's last stage [4] (value, reference)
+    static constexpr int XCH_BYTES = (4 + 2 * 4) * ROWS * 8;
+    static constexpr int R_FIT = (SMEM_CAP - 1024 - RING_OFF - 8192) / STAGE_BYTES;
+    static constexpr int R = R_FIT > 12 ? 12 : R_FIT;
     static constexpr int BAR_OFF = RING_OFF + R * STAGE_BYTES;
     static constexpr int REC_OFF = (BAR_OFF + 8 * (2 * R + NBAR_FIXED) + 15) / 16 * 16;
-    static constexpr int MISC_OFF = REC_OFF + R * REC_BYTES;  // TMEM base, abort flag
+    static constexpr int XCH_OFF = REC_OFF + R * REC_BYTES;
+    static constexpr int MISC_OFF = XCH_OFF + XCH_BYTES;      // TMEM base, abort flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;   // + alignment slack
-    static constexpr int THREADS = 192;
-    static constexpr int TMEM_COLS = 256;                    // S buffers at columns 0 and 64, O at 128
-    static constexpr int O_COL = 128;
+    static constexpr int SOFT_WARPS = 8;
+    static constexpr int THREADS = 32 * (SOFT_WARPS + 2);
+    static constexpr int COPY_WARP = SOFT_WARPS, MMA_WARP = SOFT_WARPS + 1;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int O_COL = 128;                        // S buffers at columns 0 and 64
+    static constexpr int P_COL = 256;                        // P buffer b at P_COL + 64 b: hi, then lo
     static constexpr int PSTRIDE = D + 4;
     static constexpr float TAU = 8.f;                        // lazy-rescale threshold (log2 units)
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(R >= 2, "two ring stages at least");
+    static_assert(R >= 3, "three ring stages at least (the MMA issue order relies on it)");
     static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
-    static_assert(O_COL + D <= TMEM_COLS, "tensor memory");
+    static_assert(O_COL + D <= P_COL && P_COL + 128 <= TMEM_COLS, "tensor memory");
 };
 
 // One ring stage as the copy warp describes it to the consumers.
 struct alignas(16) TcStage {
     int s, kvh, t0, nkeys;       // sequence, KV head, first key, keys copied (blocks x B)
     int n, ctx, q0, flags;       // chunk length, context, first query row of the sequence
-    int poison, pad0, pad1, pad2;
+    int poison, seg, pad1, pad2;  // bad block id seen; segment number within the CTA
 };
 static_assert(sizeof(TcStage) == 48, "stage record");
 
-enum : int { TC_FIRST = 1, TC_LAST = 2, TC_COMPLETE = 4, TC_SLOT1 = 8, TC_END = 16 };
+enum : int { TC_FIRST = 1, TC_LAST = 2, TC_COMPLETE = 4, TC_SLOT1 = 8, TC_END = 16, TC_PENULT = 32 };
+
+// A value handed to the other warp of a row quarter: one 64-bit shared word
+// holding the value and a tag naming the stage it belongs to, so the reader
+// waits (bounded) for that stage's value and never for a barrier.
+__device__ __forceinline__ void xch_put(volatile unsigned long long* cell, float v, uint32_t tag) {
+    *cell = ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ bool xch_get(const volatile unsigned long long* cell, uint32_t tag, uint64_t limit_ns,
+                                        float& v) {
+    unsigned long long x = *cell;
+    if ((uint32_t)(x >> 32) != tag) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t i = 1;; ++i) {
+            x = *cell;
+            if ((uint32_t)(x >> 32) == tag) break;
+            if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+    v = __uint_as_float((uint32_t)x);
+    return true;
+}
 
 template <class Tr>
 __global__ void __launch_bounds__(Tr::THREADS, 1)
 pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const MultiParams mp) {
     constexpr int D = Tr::D, BS = Tr::BS, R = Tr::R, SB = Tr::SB, HALVES = Tr::HALVES, KEYS = Tr::KEYS;
+    constexpr int SW = Tr::SOFT_WARPS;
     constexpr uint32_t IDESC_S = idesc_f16<Tr::BF16>(128, KEYS, false, false);
     constexpr uint32_t IDESC_O = idesc_f16<Tr::BF16>(128, D, false, true);
     const DecodeParams& p = mp.d;
@@ -110,14 +141,14 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int G = p.Hq / p.Hkv;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t q_tile = sbase;
-    const uint32_t p_tiles = sbase + Tr::P_OFF;
     const uint32_t ring = sbase + Tr::RING_OFF;
     const uint32_t bars = sbase + Tr::BAR_OFF;
     auto full = [&](int st) -> uint32_t { return bars + 8 * st; };
     auto empty = [&](int st) -> uint32_t { return bars + 8 * (R + st); };
     const uint32_t s_full = bars + 16 * R, s_free = s_full + 16, p_full = s_free + 16, pv_done = p_full + 16;
-    const uint32_t q_full = pv_done + 16, q_empty = q_full + 8, fin = q_empty + 8;
+    const uint32_t q_full = pv_done + 16, q_empty = q_full + 8, fin = q_empty + 8, o_free = fin + 8;
     TcStage* recs = reinterpret_cast<TcStage*>(smem + Tr::REC_OFF);
+    volatile unsigned long long* xch = reinterpret_cast<volatile unsigned long long*>(smem + Tr::XCH_OFF);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Tr::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::MISC_OFF + 4);
 
@@ -128,21 +159,23 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + 8 * b, 1);
-            mbar_init(s_free + 8 * b, 4);
-            mbar_init(p_full + 8 * b, 4);
+            mbar_init(s_free + 8 * b, SW / 2);      // the four warps of the stage's stream
+            mbar_init(p_full + 8 * b, SW / 2);
             mbar_init(pv_done + 8 * b, 1);
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         mbar_init(fin, 1);
+        mbar_init(o_free, SW / 2);              // a segment's output read: the four warps of its last stage
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    for (int i = threadIdx.x; i < Tr::XCH_BYTES / 8; i += Tr::THREADS) xch[i] = 0ull;   // tag 0: nothing yet
+    if (warp == Tr::MMA_WARP) {
         tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), Tr::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == Tr::COPY_WARP && lane == 0) {
         prefetch_tmap(&tmap_q);
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
@@ -182,13 +215,13 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const bool has_work = (int)blockIdx.x < sc.NS;
     const long long lo = has_work ? sc.lo(blockIdx.x) : 0, hi = has_work ? sc.lo(blockIdx.x + 1) : 0;
 
-    if (warp == 4) {
+    if (warp == Tr::COPY_WARP) {
         // ================================================================ copies
-        long long j = 0;
-        int nseg = 0;
+        int j = 0, st = 0, nseg = 0;            // stage, its ring slot and phase
+        uint32_t ph = 0;
         bool ok = true;
-        auto claim = [&](int st) -> bool {      // lane 0: slot st free for stage j
-            return j < R || mbar_wait_bounded(empty(st), (uint32_t)(((j / R) - 1) & 1), p.timeout_ns);
+        auto claim = [&]() -> bool {            // lane 0: slot st free for stage j (its last use done)
+            return j < R || mbar_wait_bounded(empty(st), ph ^ 1u, p.timeout_ns);
         };
         if (has_work) {
             SegIter it = locate(p, tab, lo, lane);
@@ -227,9 +260,8 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         int idv[SB];
 #pragma unroll
                         for (int i = 0; i < SB; ++i) idv[i] = __shfl_sync(0xffffffffu, ids, (bb + i) & 31);
-                        const int st = (int)(j % R);
                         if (lane == 0) {
-                            if (!claim(st)) {
+                            if (!claim()) {
                                 ok = false;
                             } else {
                                 int poison = 0;
@@ -248,8 +280,10 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                 rc.n = n;
                                 rc.ctx = ctx;
                                 rc.q0 = q0;
-                                rc.flags = seg_flags | (k == 0 ? TC_FIRST : 0) | (k == nst - 1 ? TC_LAST : 0);
+                                rc.flags = seg_flags | (k == 0 ? TC_FIRST : 0) | (k == nst - 1 ? TC_LAST : 0) |
+                                           (k == nst - 2 ? TC_PENULT : 0);
                                 rc.poison = poison;
+                                rc.seg = nseg;
                                 const uint32_t dst = ring + st * Tr::STAGE_BYTES;
                                 mbar_arrive_expect_tx(full(st), (uint32_t)(nbs * BS * 128 * HALVES * 2));
 #pragma unroll
@@ -267,17 +301,26 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         ++j;
+                        if (++st == R) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
                 seg_advance(it, len, p, tab);
             }
         }
         if (lane == 0) {
-            if (ok) {
-                const int st = (int)(j % R);
-                if (claim(st)) {
+            // the end record, twice: each softmax stream takes every other stage
+            for (int e = 0; e < 2 && ok; ++e) {
+                if (claim()) {
                     recs[st].flags = TC_END;
                     mbar_arrive(full(st));
+                    ++j;
+                    if (++st == R) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 } else {
                     ok = false;
                 }
@@ -286,81 +329,101 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 set_err(p.err, PA_DEVERR_TIMEOUT);
                 *abort_flag = 1;
                 // copies still in flight land before the CTA's shared memory is released
-                for (long long k = j - R > 0 ? j - R : 0; k < j; ++k)
-                    mbar_wait_bounded(full((int)(k % R)), (uint32_t)((k / R) & 1), p.timeout_ns);
+                for (int k = j - R > 0 ? j - R : 0; k < j; ++k)
+                    mbar_wait_bounded(full(k % R), (uint32_t)((k / R) & 1), p.timeout_ns);
                 if (nseg > 0) mbar_wait_bounded(q_full, (uint32_t)((nseg - 1) & 1), p.timeout_ns);
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == Tr::MMA_WARP) {
         // ================================================================ MMA
+        // Issue order S_0, S_1, then (S_{j+2}, PV_j) for j = 0, 1, ...: the
+        // scores run two stages ahead of the PV products, so the softmax of one
+        // stage never waits for its scores; PVs go in stage order (O accumulates
+        // in order).  Every wait blocks in the barrier (bounded).  Deadlock-free:
+        // S_{j+2} needs only the copy of stage j + 2 (its slot was freed by
+        // PV_{j+2-R}, R >= 3), the scores of stage j read (s_free) and at a
+        // segment start the Q tile; PV_j needs P_j and, at a segment start, the
+        // previous segment's output read, all issued or produced before it.
         if (lane == 0) {
-            long long j = 0, pend = -1;
-            int nseg = 0, pend_st = 0, pend_first = 0;
-            bool ok = true;
-            auto issue_pv = [&]() -> bool {
-                const int b = (int)(pend & 1);
-                if (!mbar_wait_bounded(p_full + 8 * b, (uint32_t)((pend >> 1) & 1), p.timeout_ns)) return false;
+            int js = 0, jp = 0, nseg = 0, pv_seg = 0;    // next S, next PV, Q tiles consumed, segments begun
+            int s_st = 0;                                // ring slot and phase of stage js
+            uint32_t s_ph = 0;
+            uint32_t meta = 0;                           // per stage in flight (js % 4): slot | first << 7
+            bool end_seen = false, ok = true;
+            // 0: the end record, 1: issued, -1: a wait timed out
+            auto issue_s = [&]() -> int {
+                if (!mbar_wait_bounded(full(s_st), s_ph, p.timeout_ns)) return -1;
+                const int flags = recs[s_st].flags;
+                if (flags & TC_END) return 0;
+                if ((flags & TC_FIRST) && !mbar_wait_bounded(q_full, (uint32_t)(nseg & 1), p.timeout_ns)) return -1;
+                const int b = js & 1;
+                if (js >= 2 && !mbar_wait_bounded(s_free + 8 * b, (uint32_t)(((js - 2) >> 1) & 1), p.timeout_ns))
+                    return -1;
+                if (flags & TC_FIRST) ++nseg;
                 tc_fence_after();
-                const uint32_t pa = p_tiles + b * 2 * Tr::P_TILE;
-                const uint32_t vb = ring + pend_st * Tr::STAGE_BYTES + Tr::KV_BYTES;
+                const uint64_t qd = sdesc_sw128(q_tile, 16, 1024);
+                const uint64_t kd = sdesc_sw128(ring + s_st * Tr::STAGE_BYTES, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < KEYS / 16; ++k) {
-                    const uint64_t bv = sdesc_sw128(vb + k * 16 * 128, Tr::HALF_BYTES, 1024);
-                    mma_f16(tmem + Tr::O_COL, sdesc_sw128(pa + k * 32, 16, 1024), bv, IDESC_O,
-                            (pend_first && k == 0) ? 0u : 1u);
-                    mma_f16(tmem + Tr::O_COL, sdesc_sw128(pa + Tr::P_TILE + k * 32, 16, 1024), bv, IDESC_O, 1u);
-                }
-                mma_commit(pv_done + 8 * b);
-                mma_commit(empty(pend_st));
-                pend = -1;
-                return true;
-            };
-            while (true) {
-                if (*abort_flag) break;
-                const int st = (int)(j % R);
-                if (!mbar_wait_bounded(full(st), (uint32_t)((j / R) & 1), p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const int flags = recs[st].flags;
-                if (flags & TC_END) break;
-                if (flags & TC_FIRST) {
-                    if (pend >= 0 && !issue_pv()) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait_bounded(q_full, (uint32_t)(nseg & 1), p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    ++nseg;
-                }
-                const int b = (int)(j & 1);
-                if (j >= 2 && !mbar_wait_bounded(s_free + 8 * b, (uint32_t)(((j - 2) >> 1) & 1), p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t kb = ring + st * Tr::STAGE_BYTES;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t a = sdesc_sw128(q_tile + (k / 4) * Tr::Q_HALF + (k % 4) * 32, 16, 1024);
-                    const uint64_t bk = sdesc_sw128(kb + (k / 4) * Tr::HALF_BYTES + (k % 4) * 32, 16, 1024);
-                    mma_f16(tmem + 64 * b, a, bk, IDESC_S, k > 0 ? 1u : 0u);
+                for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step, +a half tile per 4 (address >> 4)
+                    mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (Tr::Q_HALF >> 4) + (k % 4) * 2),
+                            kd + (uint64_t)((k / 4) * (Tr::HALF_BYTES >> 4) + (k % 4) * 2), IDESC_S, k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full + 8 * b);
                 if (flags & TC_LAST) mma_commit(q_empty);
-                if (pend >= 0 && !issue_pv()) {
+                const uint32_t sh = 8u * (uint32_t)(js & 3);
+                meta = (meta & ~(0xffu << sh)) | ((uint32_t)s_st | ((flags & TC_FIRST) ? 0x80u : 0u)) << sh;
+                ++js;
+                if (++s_st == R) {
+                    s_st = 0;
+                    s_ph ^= 1u;
+                }
+                return 1;
+            };
+            auto issue_pv = [&]() -> bool {
+                const uint32_t m8 = (meta >> (8u * (uint32_t)(jp & 3))) & 0xffu;
+                const int st = (int)(m8 & 0x7fu);
+                const bool first = (m8 & 0x80u) != 0;
+                const int b = jp & 1;
+                if (!mbar_wait_bounded(p_full + 8 * b, (uint32_t)((jp >> 1) & 1), p.timeout_ns)) return false;
+                // a segment's first PV overwrites O: the previous segment's output must have been read
+                if (first && pv_seg > 0 && !mbar_wait_bounded(o_free, (uint32_t)((pv_seg - 1) & 1), p.timeout_ns))
+                    return false;
+                if (first) ++pv_seg;
+                tc_fence_after();
+                const uint32_t pt = tmem + Tr::P_COL + 64 * b;
+                const uint64_t vd = sdesc_sw128(ring + st * Tr::STAGE_BYTES + Tr::KV_BYTES, Tr::HALF_BYTES, 1024);
+#pragma unroll
+                for (int k = 0; k < KEYS / 16; ++k) {
+                    const uint64_t bv = vd + (uint64_t)(k * ((16 * 128) >> 4));
+                    mma_f16_ts(tmem + Tr::O_COL, pt + 8 * k, bv, IDESC_O, (first && k == 0) ? 0u : 1u);
+                    mma_f16_ts(tmem + Tr::O_COL, pt + 32 + 8 * k, bv, IDESC_O, 1u);
+                }
+                mma_commit(pv_done + 8 * b);
+                mma_commit(empty(st));
+                ++jp;
+                return true;
+            };
+            for (int i = 0; i < 2 && ok && !end_seen; ++i) {
+                const int r = issue_s();
+                if (r < 0) ok = false;
+                if (r == 0) end_seen = true;
+            }
+            while (ok && jp < js) {
+                if (*abort_flag) {
                     ok = false;
                     break;
                 }
-                pend = j;
-                pend_st = st;
-                pend_first = (flags & TC_FIRST) != 0;
-                ++j;
+                if (!end_seen) {
+                    const int r = issue_s();
+                    if (r < 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (r == 0) end_seen = true;
+                }
+                if (!issue_pv()) ok = false;
             }
-            if (ok && pend >= 0 && !issue_pv()) ok = false;
             if (!ok) {
                 set_err(p.err, PA_DEVERR_TIMEOUT);
                 *abort_flag = 1;
@@ -372,35 +435,66 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         __syncwarp();
     } else {
         // ================================================================ softmax
-        const int r = warp * 32 + lane;                        // query row = TMEM lane
+        // Warp w takes rows 32 (w % 4) .. + 31 (its TMEM lane quarter; thread =
+        // query row) of every other stage: stream w / 4 takes the stages of its
+        // parity, so the two warps of a lane quarter work on consecutive stages
+        // at once.  Per row, the softmax reference is handed along a segment's
+        // stages (a tagged cell, written once the stage's maximum is known); each
+        // stream keeps its own partial row sum, and the segment's last stage adds
+        // the other stream's.  O is one accumulator: a stage that moves the
+        // reference rescales it after the previous stage's PV has completed.
+        const int quarter = warp & 3, stream = warp >> 2;
+        const int r = quarter * 32 + lane;                      // query row = TMEM lane
+        const int stid = quarter * 32 + lane;                   // thread index within the stream
         // bounded wait whose outcome is the same on every lane of the warp
         auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, p.timeout_ns));
         };
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        auto get_all = [&](const volatile unsigned long long* cell, uint32_t tag, float& v) -> bool {
+            return __all_sync(0xffffffffu, xch_get(cell, tag, p.timeout_ns, v));
+        };
+        volatile unsigned long long* ref_cell = xch;                      // [4][ROWS] by tag % 4
+        volatile unsigned long long* sum_cell = xch + 4 * Tr::ROWS;       // [4][ROWS] partial sums by segment % 4
+        volatile unsigned long long* sref_cell = xch + 8 * Tr::ROWS;      // [4][ROWS] their references
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t o_addr = lane_addr + Tr::O_COL;
         const float qnan = __int_as_float(0x7fc00000);
-        long long j = 0;
-        float m_ref = -INFINITY, l = 0.f;
-        int pois = 0, lim = -1;
+        int j = stream, st = stream;                            // this stream's stage, its ring slot and phase
+        uint32_t ph = 0;
+        float m_mine = -INFINITY, l = 0.f;                      // reference of this stream's sum, the sum
+        int pois = 0, lim = -1, cur_seg = -1, seg_kvh = 0, seg_q0 = 0;
         bool wact = false, ok = true;
         while (true) {
             if (*abort_flag) break;
-            const int st = (int)(j % R);
-            if (!wait_all(full(st), (uint32_t)((j / R) & 1))) {
+            if (!wait_all(full(st), ph)) {
                 ok = false;
                 break;
             }
-            const TcStage rc = recs[st];
-            if (rc.flags & TC_END) break;
-            if (rc.flags & TC_FIRST) {
-                m_ref = -INFINITY;
+            const int flags = recs[st].flags;
+            if (flags & TC_END) break;
+            const int t0 = recs[st].t0, nkeys = recs[st].nkeys, ctx = recs[st].ctx, seg = recs[st].seg;
+            if (seg != cur_seg) {
+                const int n = recs[st].n;
+                cur_seg = seg;
+                seg_kvh = recs[st].kvh;
+                seg_q0 = recs[st].q0;
+                m_mine = -INFINITY;
                 l = 0.f;
                 pois = 0;
-                lim = r < rc.n * G ? rc.ctx - rc.n + r / G : -1;
+                lim = r < n * G ? ctx - n + r / G : -1;
                 wact = __any_sync(0xffffffffu, lim >= 0);
             }
-            pois |= rc.poison;
-            const int b = (int)(j & 1);
+            pois |= recs[st].poison;
+            const int b = j & 1;
+            // P buffer b is free once this stream's previous PV is done.  Every warp
+            // of the stream waits for it before arriving for this stage, active or
+            // not: a warp that skipped ahead could otherwise count toward the
+            // previous stage's P-ready phase before that stage's P was written.
+            bool p_free = j < 2;
+            auto p_buffer_free = [&]() -> bool {
+                if (!p_free) p_free = wait_all(pv_done + 8 * b, (uint32_t)(((j - 2) >> 1) & 1));
+                return p_free;
+            };
             if (!wait_all(s_full + 8 * b, (uint32_t)((j >> 1) & 1))) {
                 ok = false;
                 break;
@@ -422,18 +516,40 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free + 8 * b);
             if (wact) {
-                const int kv = min(rc.nkeys, max(0, lim - rc.t0 + 1));    // keys this row sees here
-                float mx = -INFINITY;
+                const int kv = min(nkeys, max(0, lim - t0 + 1));   // keys this row sees here
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (__all_sync(0xffffffffu, kv >= KEYS)) {
 #pragma unroll
-                for (int k = 0; k < KEYS; ++k) {
-                    x[k] = k < kv ? x[k] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[k]);
+                    for (int k = 0; k < KEYS; ++k) {
+                        x[k] *= p.scale_log2;
+                        m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < KEYS; ++k) {
+                        x[k] = k < kv ? x[k] * p.scale_log2 : -INFINITY;
+                        m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+                    }
                 }
-                const float m_new = fmaxf(m_ref, mx);
-                const bool need = m_new > m_ref + Tr::TAU;
-                const float alpha = need ? ex2(m_ref - m_new) : 1.f;      // m_ref = -inf: 0
-                if (!(rc.flags & TC_FIRST) && __any_sync(0xffffffffu, need)) {
-                    // O holds the earlier stages once their PV is done
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                // the reference after the previous stage of the segment (other stream)
+                float m_prev = -INFINITY;
+                if (!(flags & TC_FIRST) && !get_all(ref_cell + (j & 3) * Tr::ROWS + r, (uint32_t)j, m_prev)) {
+                    ok = false;
+                    break;
+                }
+                if (m_prev != m_mine) {                      // references only grow along a segment
+                    l *= m_mine == -INFINITY ? 0.f : ex2(m_mine - m_prev);
+                    m_mine = m_prev;
+                }
+                const float m_new = fmaxf(m_prev, mx);
+                const bool need = m_new > m_prev + Tr::TAU;
+                if (need) m_mine = m_new;
+                if (!(flags & TC_LAST)) xch_put(ref_cell + ((j + 1) & 3) * Tr::ROWS + r, m_mine, (uint32_t)(j + 1));
+                const float alpha = need ? ex2(m_prev - m_new) : 1.f;      // m_prev = -inf: 0
+                if (need) l *= alpha;
+                if (!(flags & TC_FIRST) && __any_sync(0xffffffffu, need)) {
+                    // O holds the earlier stages once the previous stage's PV is done
                     if (!wait_all(pv_done + 8 * (b ^ 1), (uint32_t)(((j - 1) >> 1) & 1))) {
                         ok = false;
                         break;
@@ -442,72 +558,96 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t u[32];
-                        tmem_ld32(lane_addr + Tr::O_COL + 32 * c, u);
+                        tmem_ld32(o_addr + 32 * c, u);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k = 0; k < 32; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-                        tmem_st32(lane_addr + Tr::O_COL + 32 * c, u);
+                        tmem_st32(o_addr + 32 * c, u);
                     }
                     tmem_st_wait();
                 }
-                if (need) {
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-                const float mref = m_ref == -INFINITY ? 0.f : m_ref;      // no visible key yet: weights 0
-                // P buffer b is free once the PV of stage j - 2 is done
-                if (j >= 2 && !wait_all(pv_done + 8 * b, (uint32_t)(((j - 2) >> 1) & 1))) {
+                const float mref = m_mine == -INFINITY ? 0.f : m_mine;      // no visible key yet: weights 0
+                if (!p_buffer_free()) {
                     ok = false;
                     break;
                 }
-                uint8_t* prow = smem + Tr::P_OFF + b * 2 * Tr::P_TILE + r * 128;
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < KEYS / 8; ++c) {
-                    uint32_t hw[4], lw[4];
+                for (int c = 0; c < 2; ++c) {            // 32 keys at a time: hi, lo columns 16 c ..
+                    uint32_t hw[16], lw[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = ex2(x[8 * c + 2 * e] - mref), p1 = ex2(x[8 * c + 2 * e + 1] - mref);
-                        l += p0 + p1;
-                        const uint32_t h = pack2<Tr::BF16>(p0, p1);
-                        hw[e] = h;
-                        lw[e] = pack2<Tr::BF16>(p0 - lo_of<Tr::BF16>(h), p1 - hi_of<Tr::BF16>(h));
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(x[32 * c + 2 * e] - mref), p1 = ex2(x[32 * c + 2 * e + 1] - mref);
+                        s4[e & 3] += p0 + p1;
+                        if constexpr (Tr::BF16) {
+                            // hi: the weights cut to bf16 (their top 16 bits); lo: the exact
+                            // remainders, cut the same way (relative error < 2^-14 in all)
+                            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                            hw[e] = __byte_perm(u0, u1, 0x7632);
+                            const float r0 = p0 - __uint_as_float(u0 & 0xffff0000u);
+                            const float r1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+                            lw[e] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+                        } else {
+                            const uint32_t hv = pack2<false>(p0, p1);
+                            hw[e] = hv;
+                            lw[e] = pack2<false>(p0 - lo_of<false>(hv), p1 - hi_of<false>(hv));
+                        }
                     }
-                    const int off = (c ^ (r & 7)) << 4;
-                    *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(prow + Tr::P_TILE + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    tmem_st16(lane_addr + Tr::P_COL + 64 * b + 16 * c, hw);
+                    tmem_st16(lane_addr + Tr::P_COL + 64 * b + 32 + 16 * c, lw);
                 }
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
             // V rows past the context or past the blocks copied are zero for the PV product
-            const int vvalid = max(0, min(rc.nkeys, rc.ctx - rc.t0));
+            const int vvalid = max(0, min(nkeys, ctx - t0));
             if (vvalid < KEYS) {
                 uint8_t* vt = smem + Tr::RING_OFF + st * Tr::STAGE_BYTES + Tr::KV_BYTES;
                 const int nz = (KEYS - vvalid) * HALVES * 8;
-                for (int i = threadIdx.x; i < nz; i += 128) {
+                for (int i = stid; i < nz; i += 128) {
                     const int row = vvalid + i / (HALVES * 8), part = i % (HALVES * 8);
                     *reinterpret_cast<uint4*>(vt + (part / 8) * Tr::HALF_BYTES + row * 128 + (part % 8) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            if (!p_buffer_free()) {
+                ok = false;
+                break;
+            }
+            if (wact) tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + 8 * b);
-            if (rc.flags & TC_LAST) {
+            if ((flags & TC_PENULT) && wact) {
+                // this stream's share of the row sums, for the segment's last stage
+                xch_put(sum_cell + (seg & 3) * Tr::ROWS + r, l, (uint32_t)(seg + 1));
+                xch_put(sref_cell + (seg & 3) * Tr::ROWS + r, m_mine, (uint32_t)(seg + 1));
+            }
+            if (flags & TC_LAST) {
                 if (!wait_all(pv_done + 8 * b, (uint32_t)((j >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (wact) {
+                    float L = l;
+                    if (!(flags & TC_FIRST)) {
+                        float l2 = 0.f, m2 = -INFINITY;
+                        if (!get_all(sum_cell + (seg & 3) * Tr::ROWS + r, (uint32_t)(seg + 1), l2) ||
+                            !get_all(sref_cell + (seg & 3) * Tr::ROWS + r, (uint32_t)(seg + 1), m2)) {
+                            ok = false;
+                            break;
+                        }
+                        if (m2 != -INFINITY) L += l2 * ex2(m2 - m_mine);
+                    }
                     const bool live = lim >= 0;
-                    if (rc.flags & TC_COMPLETE) {
-                        uint16_t* orow =
-                            p.out + ((size_t)(rc.q0 + r / G) * p.Hq + (size_t)rc.kvh * G + r % G) * D;
-                        const float inv = 1.f / l;
+                    if (flags & TC_COMPLETE) {
+                        uint16_t* orow = p.out + ((size_t)(seg_q0 + r / G) * p.Hq + (size_t)seg_kvh * G + r % G) * D;
+                        const float inv = 1.f / L;
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t u[32];
-                            tmem_ld32(lane_addr + Tr::O_COL + 32 * c, u);
+                            tmem_ld32(o_addr + 32 * c, u);
                             tmem_ld_wait();
                             uint32_t w[16];
 #pragma unroll
@@ -525,12 +665,12 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         }
                     } else {
                         float* prow = p.partials +
-                                      (((size_t)blockIdx.x * 2 + ((rc.flags & TC_SLOT1) ? 1 : 0)) * Tr::ROWS + r) *
+                                      (((size_t)blockIdx.x * 2 + ((flags & TC_SLOT1) ? 1 : 0)) * Tr::ROWS + r) *
                                           Tr::PSTRIDE;
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t u[32];
-                            tmem_ld32(lane_addr + Tr::O_COL + 32 * c, u);
+                            tmem_ld32(o_addr + 32 * c, u);
                             tmem_ld_wait();
                             if (live) {
                                 float4* dst = reinterpret_cast<float4*>(prow + 32 * c);
@@ -546,14 +686,21 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             }
                         }
                         if (live) {
-                            prow[D] = m_ref;
-                            prow[D + 1] = l;
+                            prow[D] = m_mine;
+                            prow[D + 1] = L;
                         }
                     }
                 }
                 tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
             }
-            ++j;
+            j += 2;
+            st += 2;
+            if (st >= R) {
+                st -= R;
+                ph ^= 1u;
+            }
         }
         if (!ok) {
             if (lane == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
@@ -563,7 +710,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == Tr::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, Tr::TMEM_COLS);
     }
