@@ -457,8 +457,10 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
 }
 
 // Post-pass: rows of pairs cut by chunk boundaries, combined in chunk order
-// by the log-sum-exp rule.  One warp per (pair, query row); D / 4 lanes per
-// row, 4 dims each.
+// by the log-sum-exp rule.  A pair is cut where a chunk boundary falls
+// strictly inside it; one CTA per boundary, and the first boundary inside a
+// pair merges it (the others return), so only cut pairs cost work.  Each warp
+// merges rows of the pair: D / 4 lanes per row, 4 dims each.
 template <int D>
 __global__ void __launch_bounds__(256)
 pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_start,
@@ -468,62 +470,70 @@ pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_
     constexpr int PSTRIDE = D + 4;
     constexpr int LPR = D / 4;                    // lanes per row
     constexpr int RPW = 32 / LPR;                 // rows per warp
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int sub = lane % LPR;
-    const int rpp = max_q * G;                    // row slots per pair
-    const int rgroups = (rpp + RPW - 1) / RPW;
-    const long long task = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const long long pair = task / rgroups;
-    if (pair >= (long long)N * Hkv) return;
-    const int s = (int)(pair / Hkv), kvh = (int)(pair % Hkv);
+    const long long W = cum[N] * Hkv;
+    const Sched sc = make_sched(W, nchunks_hint, 0);
+    const int c = (int)blockIdx.x + 1;            // boundary between chunks c - 1 and c
+    if (c >= sc.NS) return;
+    const long long x = sc.lo(c);
+    // the pair holding flattened block x: sequence s with cum[s] Hkv <= x < cum[s + 1] Hkv
+    int a = 0, b = N;
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (cum[m] * Hkv <= x) a = m; else b = m;
+    }
+    const int s = a;
     const int nb = (int)(cum[s + 1] - cum[s]);
     if (nb == 0) return;
-    const int a = q_start[s], b = q_start[s + 1];
-    const int n = b - a;
-    const int ctx = context_lens[s];
-    if (a < 0 || b > total_q || n < 0 || n > max_q || n > ctx) return;    // reported by the kernel
-    const int rr = (int)(task % rgroups) * RPW + lane / LPR;
-    const bool writer = rr < n * G;
-    const int row = writer ? rr : 0;
-    const Sched sc = make_sched(cum[N] * Hkv, nchunks_hint, 0);
+    const int kvh = (int)((x - cum[s] * Hkv) / nb);
     const long long P0 = cum[s] * Hkv + (long long)kvh * nb;
+    if (P0 == x || sc.lo(c - 1) > P0) return;     // not cut here, or cut first by an earlier boundary
+    const int qa = q_start[s], qb = q_start[s + 1];
+    const int n = qb - qa;
+    const int ctx = context_lens[s];
+    if (qa < 0 || qb > total_q || n < 0 || n > max_q || n > ctx) return;    // reported by the kernel
     const long long cfirst = sc.of(P0), clast = sc.of(P0 + nb - 1);
-    if (cfirst == clast) return;
     const size_t cstride = (size_t)2 * rows_per_chunk * PSTRIDE;
-    const float* first = partials + (size_t)cfirst * cstride + (sc.lo(cfirst) < P0 ? (size_t)rows_per_chunk * PSTRIDE : 0) +
-                         (size_t)row * PSTRIDE;
-    const float* rest = partials + (size_t)cfirst * cstride + (size_t)row * PSTRIDE;
     const int np = (int)(clast - cfirst) + 1;
-    auto piece = [&](int i) -> const float* { return i == 0 ? first : rest + (size_t)i * cstride; };
-    float M = -INFINITY;
-    for (int i = 0; i < np; ++i) M = fmaxf(M, piece(i)[D]);
-    const float Mref = M == -INFINITY ? 0.f : M;
     const int d0 = sub * 4;
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < np; ++i) {
-        const float* pr = piece(i);
-        const float f = ex2(pr[D] - Mref);
-        L += pr[D + 1] * f;
-        const float4 v = *reinterpret_cast<const float4*>(pr + d0);
-        acc.x += v.x * f;
-        acc.y += v.y * f;
-        acc.z += v.z * f;
-        acc.w += v.w * f;
-    }
-    if (!writer) return;
-    const float inv = 1.f / L;
-    const float x[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-    uint32_t w[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const uint16_t h0 = bf16 ? f32_to_16<true>(x[2 * k]) : f32_to_16<false>(x[2 * k]);
-        const uint16_t h1 = bf16 ? f32_to_16<true>(x[2 * k + 1]) : f32_to_16<false>(x[2 * k + 1]);
-        w[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-    }
     const int Hq = Hkv * G;
-    uint16_t* dst = out + ((size_t)(a + rr / G) * Hq + (size_t)kvh * G + rr % G) * D + d0;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    for (int base = warp * RPW; base < n * G; base += nwarps * RPW) {
+        const int rr = base + lane / LPR;
+        const bool writer = rr < n * G;
+        const int row = writer ? rr : 0;
+        const float* first = partials + (size_t)cfirst * cstride +
+                             (sc.lo(cfirst) < P0 ? (size_t)rows_per_chunk * PSTRIDE : 0) + (size_t)row * PSTRIDE;
+        const float* rest = partials + (size_t)cfirst * cstride + (size_t)row * PSTRIDE;
+        auto piece = [&](int i) -> const float* { return i == 0 ? first : rest + (size_t)i * cstride; };
+        float M = -INFINITY;
+        for (int i = 0; i < np; ++i) M = fmaxf(M, piece(i)[D]);
+        const float Mref = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < np; ++i) {
+            const float* pr = piece(i);
+            const float f = ex2(pr[D] - Mref);
+            L += pr[D + 1] * f;
+            const float4 v = *reinterpret_cast<const float4*>(pr + d0);
+            acc.x += v.x * f;
+            acc.y += v.y * f;
+            acc.z += v.z * f;
+            acc.w += v.w * f;
+        }
+        if (!writer) continue;
+        const float inv = 1.f / L;
+        const float xv[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+        uint32_t w[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint16_t h0 = bf16 ? f32_to_16<true>(xv[2 * k]) : f32_to_16<false>(xv[2 * k]);
+            const uint16_t h1 = bf16 ? f32_to_16<true>(xv[2 * k + 1]) : f32_to_16<false>(xv[2 * k + 1]);
+            w[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        }
+        uint16_t* dst = out + ((size_t)(qa + rr / G) * Hq + (size_t)kvh * G + rr % G) * D + d0;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    }
 }
 
 struct MultiLaunch {

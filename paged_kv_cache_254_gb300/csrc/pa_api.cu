@@ -785,18 +785,16 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     if (k->launch(L) != cudaSuccess) return PA_ERR_CUDA;
     const int g = shape->num_q_heads / shape->num_kv_heads;
-    constexpr int kWarps = 8;
-    const int rpw = shape->head_dim == 128 ? 1 : 2;            // merge rows per warp
-    const long long tasks = (long long)shape->num_seqs * shape->num_kv_heads * ((max_q_len * g + rpw - 1) / rpw);
-    const unsigned blocks = (unsigned)((tasks + kWarps - 1) / kWarps);
-    if (shape->head_dim == 128)
-        pa_multi_merge<128><<<blocks, 32 * kWarps, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out,
-                                                                  d.N, d.Hkv, g, k->rows, ctas, max_q_len, total_q,
-                                                                  shape->dtype == PA_BF16);
-    else
-        pa_multi_merge<64><<<blocks, 32 * kWarps, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out,
-                                                                 d.N, d.Hkv, g, k->rows, ctas, max_q_len, total_q,
-                                                                 shape->dtype == PA_BF16);
+    if (ctas > 1) {   // one CTA per chunk boundary: the pairs cut there
+        if (shape->head_dim == 128)
+            pa_multi_merge<128><<<ctas - 1, 256, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
+                                                                d.Hkv, g, k->rows, ctas, max_q_len, total_q,
+                                                                shape->dtype == PA_BF16);
+        else
+            pa_multi_merge<64><<<ctas - 1, 256, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
+                                                               d.Hkv, g, k->rows, ctas, max_q_len, total_q,
+                                                               shape->dtype == PA_BF16);
+    }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
