@@ -87,10 +87,12 @@ struct DecodeTraits {
     static constexpr bool BF16 = BF16_;
     static constexpr bool E5M2 = KVF_ == 2;
     // About 192 KiB of stages per SM: stages of up to 8 KiB, two CTAs of four
-    // warps; 16 KiB stages, one CTA of six warps.
+    // warps; 16 KiB stages, one CTA of six warps.  The 4-bit cache (4.3 KiB
+    // stages, more arithmetic per byte) runs three CTAs of four warps: more
+    // warps to hide each stage's latency, at 168 registers.
     static constexpr int RING_PER_SM = 192 * 1024;
-    static constexpr int MIN_CTAS = Gm::STAGE_BYTES <= 8192 ? 2 : 1;
-    static constexpr int NW = MIN_CTAS == 2 ? 4 : 6;       // warps (workers) per CTA
+    static constexpr int MIN_CTAS = I4 ? 3 : Gm::STAGE_BYTES <= 8192 ? 2 : 1;
+    static constexpr int NW = MIN_CTAS == 1 ? 6 : 4;       // warps (workers) per CTA
     static constexpr int R_FIT = RING_PER_SM / (MIN_CTAS * NW * Gm::STAGE_BYTES);
     static constexpr int R = R_FIT > 8 ? 8 : R_FIT;        // stages per warp
     static constexpr int THREADS = NW * 32;
