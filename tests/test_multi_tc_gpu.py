@@ -166,3 +166,24 @@ def test_verify_batch_16_token_chunks_sampled():
         ref = decode_multi_ref(q[16 * s:16 * s + 16], case.k_pool, case.v_pool, case.block_tables[s:s + 1],
                                case.context_lens[s:s + 1], np.array([0, 16], dtype=np.int32), case.scale)
         assert_close(got[16 * s:16 * s + 16], ref, what=f"sequence {s}")
+
+
+@pytest.mark.parametrize("max_q", [4, 8])     # 32 rows per pair: mma.sync kernel; 64 rows: tcgen05
+def test_bad_context_length_poisons_its_rows(max_q):
+    ctx = [300, 500, 77, 1000]
+    qlens = [max_q, 2, 3, max_q]
+    case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=53)
+    cl = case.context_lens.copy()
+    cl[1] = case.block_tables.shape[1] * case.cfg.block_size + 5      # longer than its table can hold
+    err = pa().new_error_word("cuda")
+    bt = torch.from_numpy(case.block_tables).cuda()
+    got = pa().pa_decode_multi(q, case.k_pool, case.v_pool, bt, torch.from_numpy(cl).cuda(),
+                               torch.from_numpy(qs).cuda(), case.scale, max_q_len=max_q, err=err)
+    assert int(err.item()) & 2
+    assert torch.isnan(got[qs[1]:qs[2]].float()).all()
+    keep = [i for s in (0, 2, 3) for i in range(qs[s], qs[s + 1])]
+    sub = [0, 2, 3]
+    sub_qs = np.concatenate([[0], np.cumsum([qlens[s] for s in sub])]).astype(np.int32)
+    ref = decode_multi_ref(q[keep], case.k_pool, case.v_pool, case.block_tables[sub], case.context_lens[sub],
+                           sub_qs, case.scale)
+    assert_close(got[keep], ref, what=f"well-formed sequences, max_q {max_q}")
