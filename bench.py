@@ -340,7 +340,7 @@ def cpu_worker(args):
         "value": nbytes / dt / 1e9, "unit": "GB/s", "tokens_per_s": done * ql / dt, "seconds": dt,
         "sample": f"first {done} of {n_total} sequences of {cfg.name} (all {Hq} query heads, "
                   f"{ql} query token(s) each, {sum(ctx_done)} cached tokens), fp64 oracle",
-        "cores": 1,
+        "cores": 1, "host_cores": len(os.sched_getaffinity(0)), "blas_threads": 1,
     }))
 
 
@@ -360,7 +360,8 @@ def run_cpu_baseline(args) -> dict:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     out = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": out["value"], "unit": "GB/s", "cores": out["cores"], "kind": "oracle",
-            "sample": out["sample"], "tokens_per_s": out["tokens_per_s"]}
+            "sample": out["sample"], "tokens_per_s": out["tokens_per_s"],
+            "host_cores": out.get("host_cores"), "blas_threads": out.get("blas_threads")}
 
 
 def reference_arm(args):
@@ -401,6 +402,21 @@ def reference_arm(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def timed_rows(decode_ms, append_ms, copy_ms, dec_bytes, app_bytes, cp_bytes) -> dict:
+    """Per-call device times of the step's three parts over the timed steps
+    (CUDA events on the launching stream): median with p10 / p90, and the
+    algorithmic GB/s at the median."""
+    def row(ms, nbytes):
+        if not ms:
+            return None
+        qs = statistics.quantiles(ms, n=10, method="inclusive") if len(ms) > 1 else [ms[0]] * 9
+        med = statistics.median(ms)
+        return {"ms_p50": round(med, 5), "ms_p10": round(qs[0], 5), "ms_p90": round(qs[8], 5),
+                "bytes": nbytes, "gbs_at_p50": round(nbytes / (med * 1e-3) / 1e9, 2) if med > 0 else None}
+    return {"decode": row(decode_ms, dec_bytes), "append": row(append_ms, app_bytes),
+            "copy": row(copy_ms, cp_bytes) if copy_ms else None}
+
+
 def gpu_arm(args):
     import numpy as np
     import torch
@@ -432,7 +448,10 @@ def gpu_arm(args):
     use_prefix = st["n_groups"] > 0 and not args.plain_decode and not quant
 
     def step(q, k_new, v_new, slots, tables, ctx, ev=None):
+        # ev: four events around the copies, the append and the decode call
         launches = 0
+        if ev is not None:
+            ev[0].record(stream)
         if n_copies:
             if int4:
                 pa.pa_copy_blocks_int4(st["copies"], st["k_pool"])
@@ -441,6 +460,8 @@ def gpu_arm(args):
             else:
                 pa.pa_copy_blocks(st["copies"], st["k_pool"], st["v_pool"])
             launches += 1
+        if ev is not None:
+            ev[1].record(stream)
         if int4:
             pa.pa_append_kv_int4(k_new, v_new, slots, st["k_pool"])
         elif fp8:
@@ -448,7 +469,7 @@ def gpu_arm(args):
         else:
             pa.pa_append_kv(k_new, v_new, slots, st["k_pool"], st["v_pool"])
         if ev is not None:
-            ev[0].record(stream)
+            ev[2].record(stream)
         if int4:
             pa.pa_decode_int4(q, st["k_pool"], tables, ctx, st["scale"], out=out)
         elif fp8:
@@ -463,7 +484,7 @@ def gpu_arm(args):
         else:
             pa.pa_decode(q, st["k_pool"], st["v_pool"], tables, ctx, st["scale"], out=out, workspace=ws)
         if ev is not None:
-            ev[1].record(stream)
+            ev[3].record(stream)
         return launches + 4   # append, and the decode call's pre-pass, attention and merge kernels
 
     dev_args = (st["q"], st["k_new"], st["v_new"], st["slots"], st["tables"], st["ctx"])
@@ -475,7 +496,7 @@ def gpu_arm(args):
     if local == 0:
         clocks.start()
         time.sleep(0.05)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
@@ -490,7 +511,9 @@ def gpu_arm(args):
         dist.barrier()
     clk = clocks.stop() if local == 0 else None
     total_ms = t_start.elapsed_time(t_end)
-    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    decode_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    append_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    copy_ms = [e[0].elapsed_time(e[1]) for e in evs] if n_copies else None
     max_ms = max_over_ranks(total_ms, dist, device)
 
     # ---- end to end through the public API from pinned host buffers ----
@@ -536,6 +559,7 @@ def gpu_arm(args):
     step_bytes = ubytes + extra
     value = world * args.steps * step_bytes / (max_ms * 1e-3) / 1e9
     tokens = world * args.steps * N * args.q_len / (max_ms * 1e-3)
+    kv_tokens = world * args.steps * float(np.sum(st["ctx_h"])) / (max_ms * 1e-3)
     e2e_value = world * args.steps * step_bytes / (e2e_ms * 1e-3) / 1e9
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
@@ -568,6 +592,10 @@ def gpu_arm(args):
         "data": "synthetic (seeded N(0,1) values, random block placement)",
         "config": cfg_out,
         "tokens_per_s": round(tokens, 1),
+        "kv_tokens_per_s": round(kv_tokens, 1),
+        "timed_rows": timed_rows(decode_ms, append_ms, copy_ms, ubytes,
+                                 append_bytes(T, Hkv, d, elem=kv_elem, row_extra=rx),
+                                 copy_bytes(n_copies, Hkv, B, d, elem=kv_elem, row_extra=rx)),
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

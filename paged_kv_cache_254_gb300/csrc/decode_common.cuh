@@ -432,6 +432,7 @@ __device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uin
     const int g = lane >> 2;
     const int t4 = lane & 3;
     // per-token scales of this lane's columns: tokens 4 t4 .. + 3 and 16 + 4 t4 .. + 3
+    // (K's folded with scale_log2)
     float ksc[2][4], vsc[2][4];
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
@@ -441,14 +442,22 @@ __device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uin
             uint32_t w[4];
             lds128(pb + Gm::KS, w);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ksc[hlf][i] = __uint_as_float(w[i]);
+            for (int i = 0; i < 4; ++i) ksc[hlf][i] = __uint_as_float(w[i]) * scale_log2;
             lds128(pb + Gm::VS, w);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vsc[hlf][i] = tok + i < valid ? __uint_as_float(w[i]) : 0.f;
+            for (int i = 0; i < 4; ++i) vsc[hlf][i] = __uint_as_float(w[i]);
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) ksc[hlf][i] = vsc[hlf][i] = 0.f;
         }
+    }
+    // a partial stage (the last of a segment): masked slots get no V weight
+    if (valid < 32) {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (16 * hlf + 4 * t4 + i >= valid) vsc[hlf][i] = 0.f;
     }
     float sacc[Gm::NT][4];
 #pragma unroll
@@ -460,11 +469,13 @@ __device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uin
             uint32_t w[4];   // dims 32 t4 .. 32 t4 + 31 of token tok
             lds128(kb + (tok / BS) * PIECE + (tok % BS) * 64 + 16 * t4, w);
 #pragma unroll
-            for (int kk = 0; kk < Gm::KD; ++kk) {
-                const int sh = 8 * (kk & 1);
-                const uint32_t b0 = i4x2_to_f16x2(w[kk >> 1] >> sh);
-                const uint32_t b1 = i4x2_to_f16x2(w[kk >> 1] >> (sh + 4));
-                mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            for (int i = 0; i < 4; ++i) {
+                // k-step 2 i takes pairs 0, 1 of word i; k-step 2 i + 1 pairs 2, 3
+                uint32_t b[4];
+                i4x8_to_f16x2(w[i], b);
+                mma16816<false>(sacc[nt], qa[2 * i][0], qa[2 * i][1], qa[2 * i][2], qa[2 * i][3], b[0], b[1]);
+                mma16816<false>(sacc[nt], qa[2 * i + 1][0], qa[2 * i + 1][1], qa[2 * i + 1][2], qa[2 * i + 1][3],
+                                b[2], b[3]);
             }
         }
     }
@@ -475,13 +486,19 @@ __device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uin
 #pragma unroll
     for (int nt = 0; nt < Gm::NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tok = perm_token(nt, 2 * t4 + (e & 1));
-            const float ks = ksc[nt >> 1][2 * (nt & 1) + (e & 1)];
-            const float v = tok < valid ? sacc[nt][e] * ks * scale_log2 : -INFINITY;
-            sacc[nt][e] = v;
-            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], v);
-        }
+        for (int e = 0; e < 4; ++e) sacc[nt][e] *= ksc[nt >> 1][2 * (nt & 1) + (e & 1)];
+    if (valid < 32) {
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (perm_token(nt, 2 * t4 + (e & 1)) >= valid) sacc[nt][e] = -INFINITY;
+    }
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
     float alpha[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -538,12 +555,12 @@ __device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uin
         const int sh = 8 * ((loc % 8) / 4);
 #pragma unroll
         for (int mt = 0; mt < Gm::KD; ++mt) {
-            const uint32_t x = lds32(vb + (16 * mt + g) * (BS / 2));
-            const uint32_t y = lds32(vb + (16 * mt + g + 8) * (BS / 2));
-            const uint32_t a0 = i4x2_to_f16x2(x >> sh);
-            const uint32_t a2 = i4x2_to_f16x2(x >> (sh + 4));
-            const uint32_t a1 = i4x2_to_f16x2(y >> sh);
-            const uint32_t a3 = i4x2_to_f16x2(y >> (sh + 4));
+            const uint32_t x = lds32(vb + (16 * mt + g) * (BS / 2)) >> sh;
+            const uint32_t y = lds32(vb + (16 * mt + g + 8) * (BS / 2)) >> sh;
+            const uint32_t a0 = i4_pair_lo(x);
+            const uint32_t a2 = i4_pair_hi(x);
+            const uint32_t a1 = i4_pair_lo(y);
+            const uint32_t a3 = i4_pair_hi(y);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);

@@ -32,6 +32,19 @@ def test_unique_bytes_count_shared_blocks_once():
     assert u < bench.decode_bytes(ctx, 2, 1, 8, B)
 
 
+def test_timed_rows_quantiles_and_rates():
+    ms = [float(x) for x in range(1, 12)]          # 1 .. 11 ms
+    rows = bench.timed_rows(ms, [0.5, 0.5], None, 6_000_000, 1_000_000, 0)
+    d = rows["decode"]
+    assert d["ms_p50"] == 6.0 and d["ms_p10"] == 2.0 and d["ms_p90"] == 10.0
+    assert d["gbs_at_p50"] == 1.0                  # 6 MB in 6 ms
+    assert rows["append"]["ms_p50"] == 0.5 and rows["append"]["gbs_at_p50"] == 2.0
+    assert rows["copy"] is None
+    one = bench.timed_rows([2.0], [1.0], [4.0], 2e6, 1e6, 4e6)
+    assert one["decode"]["ms_p10"] == one["decode"]["ms_p90"] == 2.0
+    assert one["copy"]["gbs_at_p50"] == 1.0
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
