@@ -324,12 +324,20 @@ __device__ __forceinline__ void consume_stage8(uint32_t kb, int valid, const uin
 #pragma unroll
     for (int nt = 0; nt < Gm::NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tok = perm_token(nt, 2 * t4 + (e & 1));
-            const float v = tok < valid ? sacc[nt][e] * scale_log2 : -INFINITY;
-            sacc[nt][e] = v;
-            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], v);
-        }
+        for (int e = 0; e < 4; ++e) sacc[nt][e] *= scale_log2;
+    // only a partial stage (the last of a segment) has slots to mask
+    if (valid < 32) {
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (perm_token(nt, 2 * t4 + (e & 1)) >= valid) sacc[nt][e] = -INFINITY;
+    }
+#pragma unroll
+    for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
     float alpha[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {

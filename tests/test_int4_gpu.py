@@ -129,3 +129,27 @@ def test_dequantized_values_round_trip_through_append():
     K, V, ks, vs = split_piece(flat(pool)[40 // B, 1], B, d)
     kq, ksc = quantize_rows(kn[1, 1].float().cpu().numpy())
     np.testing.assert_array_equal(dequantize_rows(K[40 % B], ks[40 % B]), dequantize_rows(kq, ksc))
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_masked_slots_with_non_finite_scales(B):
+    # slots past a context hold scales that are NaN or inf; the kernel must
+    # give them no weight whether the partial stage is in its first or
+    # second 16-token half
+    from oracle.int4 import _offsets
+    ctx = [1, 15, 17, 31, 33, 100, 250]
+    case, pool = int4_case(ctx, 16, 2, B, "bf16", seed=60 + B)
+    kf, vf = dequantized_pools(flat(pool), B, 128)
+    want = decode_ref(case.q, kf, vf, case.block_tables, case.context_lens, case.scale)
+    _, _, ks, vs = _offsets(B, 128)
+    bad = np.array([np.nan, np.inf, -np.inf], dtype=np.float32).view(np.uint8).reshape(3, 4)
+    raw = pool.view(pool.shape[0], pool.shape[1], -1)
+    for s, c in enumerate(ctx):
+        blk = int(case.block_tables[s, (c - 1) // B])
+        for off in range(c - ((c - 1) // B) * B, B):
+            for base in (ks, vs):
+                v = torch.from_numpy(bad[(s + off + base) % 3].copy()).cuda()
+                raw[blk, :, base + 4 * off:base + 4 * off + 4] = v
+    got = decode(case, pool)
+    assert torch.isfinite(got.float()).all()
+    assert_close(got, want, what=f"non-finite masked scales B{B}")
