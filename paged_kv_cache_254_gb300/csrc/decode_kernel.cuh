@@ -369,10 +369,12 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     };
     open_chunk(next_id);
     long long nis = 0;        // stages issued
+    int ist = 0;              // ring stage of the next fill (nis % R, kept without a division)
     bool aborted = false;
     auto issue = [&]() {
         if (idone || aborted) return;
-        const int st = (int)(nis % R);
+        const int st = ist;
+        if (++ist == R) ist = 0;
         const int nblk = min(UB, ilen - ib);
         int ids[UB];
 #pragma unroll
@@ -496,6 +498,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     };
     long long ncons = 0;      // stages folded in (or skipped after an abort)
     long long nwait = 0;      // stages whose copies are known to have landed
+    int cst = 0;              // ring stage of the next stage to fold in (ncons % R)
+    uint32_t cph = 0;         // and the parity of its fill ((ncons / R) & 1)
     const float qnan = __int_as_float(0x7fc00000);
     while (true) {
         const int len = seg_len(it, chi);
@@ -513,10 +517,15 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         init_acc();
         int poisoned = 0;
         for (int b = 0; b < len; b += UB) {
-            const int st = (int)(ncons % R);
+            const int st = cst;
+            const uint32_t par = cph;
+            if (++cst == R) {
+                cst = 0;
+                cph ^= 1u;
+            }
             ++ncons;
             if (!aborted) {
-                if (mbar_wait_bounded(full0 + 8 * st, (uint32_t)(((ncons - 1) / R) & 1), p.timeout_ns)) {
+                if (mbar_wait_bounded(full0 + 8 * st, par, p.timeout_ns)) {
                     nwait = ncons;
                 } else {
                     if (lane == 0) set_err(p.err, PA_DEVERR_TIMEOUT);

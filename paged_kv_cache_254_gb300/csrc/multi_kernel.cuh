@@ -272,10 +272,12 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         tnxt = row_ids(irow, 32, ilen - 32);
     }
     long long nis = 0;
+    int ist = 0;               // nis % R, kept without a division
     bool idone = false;
     auto issue_one = [&]() {   // warp 0 only; the stage's slot is known to be free
         if (idone) return;
-        const int st = (int)(nis % R);
+        const int st = ist;
+        if (++ist == R) ist = 0;
         int id = __shfl_sync(0xffffffffu, tcur, (ib - tbase) & 31);
         if (lane == 0) {
             const bool bad = (unsigned)id >= (unsigned)p.NB;
@@ -332,6 +334,8 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     int nq = max(0, chunk_len(it.s));
     load_q(qa, it, nq);
     long long ncons = 0;
+    int cst = 0;               // ncons % R
+    uint32_t cph = 0;          // (ncons / R) & 1
     while (it.gi < hi) {
         const int len = seg_len(it, hi);
         const int ctx = tab.ctx[it.s];
@@ -353,8 +357,12 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         acc.reset();
         int poisoned = seq_bad ? 1 : 0;
         for (int b = 0; b < len; ++b) {
-            const int st = (int)(ncons % R);
-            const uint32_t par = (uint32_t)((ncons / R) & 1);
+            const int st = cst;
+            const uint32_t par = cph;
+            if (++cst == R) {
+                cst = 0;
+                cph ^= 1u;
+            }
             ++ncons;
             if (*abort_flag) {
                 poisoned = 1;
