@@ -65,10 +65,15 @@ struct PrefixTraits : Geom<D_, BS_> {
     static constexpr int SP_OFF = SL_OFF + NC * RPW * 4;
     static constexpr int PS_OFF = SP_OFF + NC * 4;
     static constexpr int BAR_OFF = ((PS_OFF + STAGES * 4) + 7) & ~7;
-    static constexpr int INFO_OFF = BAR_OFF + 2 * STAGES * 8;
+    static constexpr int RF_OFF = BAR_OFF + 2 * STAGES * 8;   // per row: lane factors f0, f1, then M, L
+    static constexpr int RP_OFF = RF_OFF + RC * 4 * 4;        // per row: destination row pointer
+    static constexpr int MAXP = 8;                            // pieces merged through shared memory
+    static constexpr int INFO_OFF = RP_OFF + RC * 8;
     static constexpr int INFO_BYTES = 64;
     static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;
     static_assert(STAGES >= 2 && STAGES % BL == 0, "each ring stage belongs to one block lane");
+    static_assert(RC * MAXP <= NC * RPW * OSTRIDE, "piece factors fit in the lane-state area");
+    static_assert(D_ % 2 == 0 && PSTRIDE % 2 == 0 && OSTRIDE % 2 == 0, "rows hold whole float2 pairs");
 };
 
 struct PrefixInfo {
@@ -376,15 +381,18 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
 
         // ---- the group must really share these blocks ----
+        // (a thread per table column; the members' entries are independent loads)
         {
             const int members = it.s1 - it.s0;
             const int32_t* first_row = p.block_tables + (size_t)it.s0 * p.MB;
             int bad = 0;
-            for (int e = tid; e < members * it.pb; e += NC * 32) {
-                const int m = e / it.pb, i = e - m * it.pb;
-                const int s = it.s0 + m;
-                if (i == 0 && __ldg(p.context_lens + s) < it.pb * BS) bad = 1;
-                if (__ldg(p.block_tables + (size_t)s * p.MB + i) != __ldg(first_row + i)) bad = 1;
+            for (int m = tid; m < members; m += NC * 32)
+                if (__ldg(p.context_lens + it.s0 + m) < it.pb * BS) bad = 1;
+            for (int i = tid; i < it.pb; i += NC * 32) {
+                const int f = __ldg(first_row + i);
+#pragma unroll 4
+                for (int m = 1; m < members; ++m)
+                    if (__ldg(first_row + (size_t)m * p.MB + i) != f) bad = 1;
             }
             if (bad) atomicOr(&info->bad, 1);
         }
@@ -427,24 +435,37 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const int slot = (it.gi_flat == lo) ? 0 : 1;
         const int rows = min(RC, R - it.ch * RC);
         float* prow = p.partials + ((size_t)blockIdx.x * 2 + slot) * RC * Tr::PSTRIDE;
-        for (int idx = tid; idx < rows * D; idx += NC * 32) {
-            const int rloc = idx / D;
-            const int dim = idx - rloc * D;
-            const int rr = rloc % RPW;
-            const int w0 = rloc / RPW, w1 = w0 + RG;          // the two lanes of this row group
+        // per row, once: the factors that merge the two block lanes of its
+        // row group, the merged m and l, and where the row goes
+        float* rowf = reinterpret_cast<float*>(smem + Tr::RF_OFF);
+        float** rowp = reinterpret_cast<float**>(smem + Tr::RP_OFF);
+        if (tid < rows) {
+            const int rr = tid % RPW;
+            const int w0 = tid / RPW, w1 = w0 + RG;           // the two lanes of this row group
             const float m0 = sm[w0 * RPW + rr], m1 = sm[w1 * RPW + rr];
             const float M = fmaxf(m0, m1);
             const float f0 = ex2(m0 - M), f1 = ex2(m1 - M);
-            const float L = sl[w0 * RPW + rr] * f0 + sl[w1 * RPW + rr] * f1;
-            float O = so[(w0 * RPW + rr) * Tr::OSTRIDE + dim] * f0 + so[(w1 * RPW + rr) * Tr::OSTRIDE + dim] * f1;
-            if (anybad) O = qnan;
-            float* dst = complete ? carry_row(p, it.s0, it.kvh, it.ch * RC + rloc, Tr::PSTRIDE)
-                                  : prow + rloc * Tr::PSTRIDE;
-            dst[dim] = O;
-            if (dim == 0) {
-                dst[D] = M;
-                dst[D + 1] = L;
-            }
+            float* dst = complete ? carry_row(p, it.s0, it.kvh, it.ch * RC + tid, Tr::PSTRIDE)
+                                  : prow + tid * Tr::PSTRIDE;
+            rowf[4 * tid] = f0;
+            rowf[4 * tid + 1] = f1;
+            dst[D] = M;
+            dst[D + 1] = sl[w0 * RPW + rr] * f0 + sl[w1 * RPW + rr] * f1;
+            rowp[tid] = dst;
+        }
+        named_bar_sync(1, NC * 32);
+        // o of every row, two dims per thread and pass
+        for (int idx = tid; idx < rows * (D / 2); idx += NC * 32) {
+            const int rloc = idx / (D / 2);
+            const int c2 = 2 * (idx - rloc * (D / 2));
+            const int rr = rloc % RPW;
+            const int w0 = rloc / RPW, w1 = w0 + RG;
+            const float f0 = rowf[4 * rloc], f1 = rowf[4 * rloc + 1];
+            const float2 a = *reinterpret_cast<const float2*>(so + (w0 * RPW + rr) * Tr::OSTRIDE + c2);
+            const float2 b = *reinterpret_cast<const float2*>(so + (w1 * RPW + rr) * Tr::OSTRIDE + c2);
+            float2 o = make_float2(a.x * f0 + b.x * f1, a.y * f0 + b.y * f1);
+            if (anybad) o = make_float2(qnan, qnan);
+            *reinterpret_cast<float2*>(rowp[rloc] + c2) = o;
         }
 
         if (!complete) {
@@ -456,7 +477,57 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 *(volatile int*)&info->last = (prev == (int)(clast - cfirst)) ? 1 : 0;
             }
             named_bar_sync(1, NC * 32);
-            if (*(volatile int*)&info->last) {
+            const int np = (int)(clast - cfirst + 1);
+            if (*(volatile int*)&info->last && np <= Tr::MAXP) {
+                // the item's pieces, in CTA order; the first CTA's piece is in
+                // its second slot when its range starts inside the item
+                __threadfence();
+                const int sl0 = range_lo(cfirst, W, geff) < P0 ? 1 : 0;
+                auto piece = [&](int k) -> const float* {
+                    return p.partials + ((size_t)(cfirst + k) * 2 + (k == 0 ? sl0 : 0)) * RC * Tr::PSTRIDE;
+                };
+                float* fct = so;                               // [RC][MAXP], the lane states are consumed
+                if (tid < rows) {
+                    float mk[Tr::MAXP];
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < Tr::MAXP; ++k) {
+                        mk[k] = k < np ? __ldcg(piece(k) + tid * Tr::PSTRIDE + D) : -INFINITY;
+                        M = fmaxf(M, mk[k]);
+                    }
+                    float L = 0.f;
+#pragma unroll
+                    for (int k = 0; k < Tr::MAXP; ++k) {
+                        if (k < np) {
+                            const float f = ex2(mk[k] - M);
+                            L += __ldcg(piece(k) + tid * Tr::PSTRIDE + D + 1) * f;
+                            fct[tid * Tr::MAXP + k] = f;
+                        }
+                    }
+                    float* dst = carry_row(p, it.s0, it.kvh, it.ch * RC + tid, Tr::PSTRIDE);
+                    dst[D] = M;
+                    dst[D + 1] = L;
+                    rowp[tid] = dst;
+                }
+                named_bar_sync(1, NC * 32);
+                for (int idx = tid; idx < rows * (D / 2); idx += NC * 32) {
+                    const int rloc = idx / (D / 2);
+                    const int c2 = 2 * (idx - rloc * (D / 2));
+                    float2 o = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < Tr::MAXP; ++k) {
+                        if (k < np) {
+                            const float f = fct[rloc * Tr::MAXP + k];
+                            const float2 v = __ldcg(reinterpret_cast<const float2*>(piece(k) + rloc * Tr::PSTRIDE + c2));
+                            o.x += v.x * f;
+                            o.y += v.y * f;
+                        }
+                    }
+                    *reinterpret_cast<float2*>(rowp[rloc] + c2) = o;
+                }
+            } else if (*(volatile int*)&info->last) {
+                // more pieces than the shared-memory path holds: fold them in
+                // order, element by element
                 __threadfence();
                 for (int idx = tid; idx < rows * (D + 2); idx += NC * 32) {
                     const int rloc = idx / (D + 2);

@@ -153,3 +153,26 @@ def test_parallel_sampling_full_size():
                            torch.from_numpy(ctx).cuda(), case.scale)
     a, b = out.double(), plain.double()
     assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
+
+
+@pytest.mark.parametrize("groups,what", [
+    # 30 groups x 2 KV heads of 12 shared blocks: each item is cut across
+    # several CTA ranges (a few pieces, merged through shared memory)
+    ([(4, 12, None)] * 30, "few pieces"),
+    # one group with a 400-block prompt: its items span far more CTA ranges
+    # than the shared-memory merge holds (the in-order fold)
+    ([(4, 400, None)], "many pieces"),
+])
+def test_prefix_items_split_across_many_ctas(groups, what):
+    q, kp, vp, tables, ctx, starts, prefix = grouped_case(77, groups, 8, 2, 128, 16, "bf16", solo=(5,))
+    scale = float(np.float32(128 ** -0.5))
+    err = pa().new_error_word("cuda")
+    out = run_sp(q, kp, vp, tables, ctx, starts, prefix, scale, err=err)
+    assert pa().pa_read_error(err) == 0
+    r = np.random.Generator(np.random.PCG64(3))
+    rows = sorted({(int(s), int(h)) for s in r.integers(0, len(ctx), size=10) for h in r.integers(0, 8, size=2)})
+    ref = decode_shared_prefix_ref(q, kp, vp, tables, ctx, scale, starts, prefix, rows=rows)
+    assert_close(out, ref, rows=rows, what=f"shared prefix, {what}")
+    plain = pa().pa_decode(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(), scale)
+    a, b = out.double(), plain.double()
+    assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
