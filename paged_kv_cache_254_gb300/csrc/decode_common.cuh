@@ -201,17 +201,20 @@ __device__ __forceinline__ void consume_block(uint32_t kb, uint32_t vb, int vali
                 pl[kt][r][h] = pack2<BF16>(x0 - lo_of<BF16>(hi), x1 - hi_of<BF16>(hi));
             }
 
-    // rescale the running O^T by exp2(m_old - m_new) of each row
+    // rescale the running O^T by exp2(m_old - m_new) of each row; skipped
+    // (a multiplication by exactly 1) when no row's maximum moved
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-        const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
-        const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
+        if (__any_sync(0xffffffffu, alpha[r] != 1.f)) {
+            const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
+            const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
 #pragma unroll
-        for (int mt = 0; mt < Gm::KD; ++mt) {
-            acc.o[mt][r][0] *= aa;
-            acc.o[mt][r][1] *= ab;
-            acc.o[mt][r][2] *= aa;
-            acc.o[mt][r][3] *= ab;
+            for (int mt = 0; mt < Gm::KD; ++mt) {
+                acc.o[mt][r][0] *= aa;
+                acc.o[mt][r][1] *= ab;
+                acc.o[mt][r][2] *= aa;
+                acc.o[mt][r][3] *= ab;
+            }
         }
     }
 
