@@ -68,11 +68,14 @@ struct PrefixTraits : Geom<D_, BS_> {
     static constexpr int RF_OFF = BAR_OFF + 2 * STAGES * 8;   // per row: lane factors f0, f1, then M, L
     static constexpr int RP_OFF = RF_OFF + RC * 4 * 4;        // per row: destination row pointer
     static constexpr int MAXP = 8;                            // pieces merged through shared memory
+    static constexpr int RSTEP = NC * 32 / (D_ / 2);          // rows apart of one thread's float2 pairs
+    static constexpr int EPT = RC / RSTEP;                    // float2 pairs of the row block per thread
     static constexpr int INFO_OFF = RP_OFF + RC * 8;
     static constexpr int INFO_BYTES = 64;
     static constexpr int SMEM_BYTES = INFO_OFF + INFO_BYTES + 1024;
     static_assert(STAGES >= 2 && STAGES % BL == 0, "each ring stage belongs to one block lane");
     static_assert(RC * MAXP <= NC * RPW * OSTRIDE, "piece factors fit in the lane-state area");
+    static_assert((NC * 32) % (D_ / 2) == 0 && RC % RSTEP == 0, "the row block splits evenly over the threads");
     static_assert(D_ % 2 == 0 && PSTRIDE % 2 == 0 && OSTRIDE % 2 == 0, "rows hold whole float2 pairs");
 };
 
@@ -454,18 +457,26 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             rowp[tid] = dst;
         }
         named_bar_sync(1, NC * 32);
-        // o of every row, two dims per thread and pass
-        for (int idx = tid; idx < rows * (D / 2); idx += NC * 32) {
-            const int rloc = idx / (D / 2);
-            const int c2 = 2 * (idx - rloc * (D / 2));
-            const int rr = rloc % RPW;
-            const int w0 = rloc / RPW, w1 = w0 + RG;
-            const float f0 = rowf[4 * rloc], f1 = rowf[4 * rloc + 1];
-            const float2 a = *reinterpret_cast<const float2*>(so + (w0 * RPW + rr) * Tr::OSTRIDE + c2);
-            const float2 b = *reinterpret_cast<const float2*>(so + (w1 * RPW + rr) * Tr::OSTRIDE + c2);
-            float2 o = make_float2(a.x * f0 + b.x * f1, a.y * f0 + b.y * f1);
-            if (anybad) o = make_float2(qnan, qnan);
-            *reinterpret_cast<float2*>(rowp[rloc] + c2) = o;
+        // o of every row: thread tid owns dims c2, c2 + 1 of rows tid / (D / 2) + j * RSTEP,
+        // all read before any is written
+        const int c2 = 2 * (tid % (D / 2));
+        {
+            float2 o[Tr::EPT];
+#pragma unroll
+            for (int j = 0; j < Tr::EPT; ++j) {
+                const int rloc = tid / (D / 2) + j * Tr::RSTEP;
+                const int rr = rloc % RPW;
+                const int w0 = rloc / RPW, w1 = w0 + RG;
+                const float f0 = rowf[4 * rloc], f1 = rowf[4 * rloc + 1];
+                const float2 a = *reinterpret_cast<const float2*>(so + (w0 * RPW + rr) * Tr::OSTRIDE + c2);
+                const float2 b = *reinterpret_cast<const float2*>(so + (w1 * RPW + rr) * Tr::OSTRIDE + c2);
+                o[j] = anybad ? make_float2(qnan, qnan) : make_float2(a.x * f0 + b.x * f1, a.y * f0 + b.y * f1);
+            }
+#pragma unroll
+            for (int j = 0; j < Tr::EPT; ++j) {
+                const int rloc = tid / (D / 2) + j * Tr::RSTEP;
+                if (rloc < rows) *reinterpret_cast<float2*>(rowp[rloc] + c2) = o[j];
+            }
         }
 
         if (!complete) {
@@ -510,20 +521,28 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     rowp[tid] = dst;
                 }
                 named_bar_sync(1, NC * 32);
-                for (int idx = tid; idx < rows * (D / 2); idx += NC * 32) {
-                    const int rloc = idx / (D / 2);
-                    const int c2 = 2 * (idx - rloc * (D / 2));
-                    float2 o = make_float2(0.f, 0.f);
+                // piece by piece, each thread's rows at once (loads of one
+                // piece are independent), then the writes
+                float2 o[Tr::EPT];
 #pragma unroll
-                    for (int k = 0; k < Tr::MAXP; ++k) {
-                        if (k < np) {
+                for (int j = 0; j < Tr::EPT; ++j) o[j] = make_float2(0.f, 0.f);
+                for (int k = 0; k < np; ++k) {
+                    const float* pk = piece(k);
+#pragma unroll
+                    for (int j = 0; j < Tr::EPT; ++j) {
+                        const int rloc = tid / (D / 2) + j * Tr::RSTEP;
+                        if (rloc < rows) {
                             const float f = fct[rloc * Tr::MAXP + k];
-                            const float2 v = __ldcg(reinterpret_cast<const float2*>(piece(k) + rloc * Tr::PSTRIDE + c2));
-                            o.x += v.x * f;
-                            o.y += v.y * f;
+                            const float2 v = __ldcg(reinterpret_cast<const float2*>(pk + rloc * Tr::PSTRIDE + c2));
+                            o[j].x += v.x * f;
+                            o[j].y += v.y * f;
                         }
                     }
-                    *reinterpret_cast<float2*>(rowp[rloc] + c2) = o;
+                }
+#pragma unroll
+                for (int j = 0; j < Tr::EPT; ++j) {
+                    const int rloc = tid / (D / 2) + j * Tr::RSTEP;
+                    if (rloc < rows) *reinterpret_cast<float2*>(rowp[rloc] + c2) = o[j];
                 }
             } else if (*(volatile int*)&info->last) {
                 // more pieces than the shared-memory path holds: fold them in
