@@ -251,6 +251,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         }
     }
+    // Everything above is CTA-local; the pre-pass's outputs (and whatever the
+    // stream wrote before it) are read only after the previous kernel is done.
+    griddep_wait();
     const bool in_smem = p.N <= Tr::CUM_SMEM;
     if (in_smem) {
         for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) {
@@ -761,8 +764,19 @@ struct DecodeKernelInfo {
 
 template <class Tr>
 cudaError_t decode_launch(const DecodeLaunch& L) {
-    pa_decode_kernel<Tr><<<L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream>>>(*L.tmap_k, *L.tmap_v, L.p);
-    return cudaGetLastError();
+    // launched with programmatic stream serialization: the CTAs' set-up
+    // overlaps the pre-pass, and the kernel waits for it (griddep_wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.grid);
+    cfg.blockDim = dim3(Tr::THREADS);
+    cfg.dynamicSmemBytes = Tr::SMEM_BYTES;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pa_decode_kernel<Tr>, *L.tmap_k, *L.tmap_v, L.p);
 }
 
 template <class Tr>

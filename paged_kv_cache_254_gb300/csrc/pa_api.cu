@@ -119,6 +119,7 @@ pa_decode_prepass(const int32_t* __restrict__ context_lens, const int32_t* __res
                   long long* __restrict__ cum) {
     __shared__ long long wsum[32];
     __shared__ long long carry;
+    griddep_launch_dependents();   // the attention kernel may set up meanwhile; it waits for this grid
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (long long i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
     if (threadIdx.x == 0) {

@@ -102,6 +102,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel of the
+// stream (launched with programmatic stream serialization) may start now;
+// wait: block until the previous kernel of the stream has completed and its
+// memory operations are visible (returns at once when there is none).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
