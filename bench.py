@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # of the decode kernel's source; a stale entry reports null.
 TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of one pa_decode_kernel launch
-    ("75f948cbe7ee7555", "llama3_70b_b256"): 4_862_185_472,   # 4,829,689,344 read + 32,496,128 written
+    ("3adccd1ff002d487", "llama3_70b_b256"): 4_861_767_680,   # 4,829,669,632 read + 32,098,048 written
 }
 
 
