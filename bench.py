@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # of the decode kernel's source; a stale entry reports null.
 TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of one pa_decode_kernel launch
-    ("3adccd1ff002d487", "llama3_70b_b256"): 4_861_767_680,   # 4,829,669,632 read + 32,098,048 written
+    ("b9279b1ffad2199e", "llama3_70b_b256"): 4_861_498_112,   # 4,829,106,432 read + 32,391,680 written
 }
 
 

@@ -322,7 +322,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // 32.  The KV heads of a sequence share its row, so a batch is reused
     // across them; the first batch of the next sequence is fetched (tpre)
     // while the current one is in use.
-    SegIter is;
+    SegIter is{};             // set by open_chunk before the first issue
     long long ihi = 0;
     int ilen = 0, ib = 0, tbase = 0;
     int tcur = 0, tnxt = 0, tpre = 0;
