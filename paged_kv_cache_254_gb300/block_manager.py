@@ -214,9 +214,14 @@ class BlockManager:
                     self._copies.append((last, new))
             for _ in range(-(-(t + n) // B) - len(blocks)):
                 blocks.append(self._pop())
-            tt = np.arange(t, t + n, dtype=np.int64)
-            tbl = np.asarray(blocks, dtype=np.int64)
-            out[pos:pos + n] = tbl[tt // B] * B + tt % B
+            # only the blocks the new tokens land in: O(n), not O(context)
+            if n == 1:
+                out[pos] = blocks[t // B] * B + t % B
+            else:
+                b0 = t // B
+                tt = np.arange(t, t + n, dtype=np.int64)
+                tbl = np.asarray(blocks[b0:(t + n - 1) // B + 1], dtype=np.int64)
+                out[pos:pos + n] = tbl[tt // B - b0] * B + tt % B
             pos += n
             self._len[seq] = t + n
         return out
