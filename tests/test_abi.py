@@ -133,3 +133,57 @@ def test_fp8_entry_point_checks(lib):
     assert lib.pa_copy_blocks_fp8(ctypes.byref(shape(dtype=2)), FAKE, -1, FAKE, NULL, NULL) == 1
     assert lib.pa_copy_blocks_fp8(ctypes.byref(shape(dtype=2)), NULL, 0, NULL, NULL, NULL) == 0
     assert lib.pa_copy_blocks(ctypes.byref(shape(dtype=2)), FAKE, 1, FAKE, FAKE, NULL, NULL) == 1
+
+
+def test_int4_entry_point_checks(lib):
+    s = shape(head_dim=128, num_q_heads=8, num_kv_heads=2)
+    f = ctypes.c_float
+
+    def dec(sh, q=FAKE, scale=0.1):
+        return lib.pa_decode_int4(ctypes.byref(sh), q, FAKE, FAKE, FAKE, f(scale), FAKE, FAKE,
+                                  ctypes.c_size_t(1 << 30), NULL, NULL)
+    assert dec(shape(head_dim=64)) == 2                     # the 4-bit layout is for head_dim 128
+    assert dec(shape(head_dim=128, block_size=8)) == 2
+    assert dec(s, q=NULL) == 1 and dec(s, scale=float("nan")) == 1
+    assert dec(shape(head_dim=128, num_seqs=0)) == 0
+    assert lib.pa_append_kv_int4(ctypes.byref(s), -1, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_append_kv_int4(ctypes.byref(s), 0, NULL, NULL, NULL, NULL, NULL, NULL) == 0
+    assert lib.pa_append_kv_int4(ctypes.byref(s), 3, NULL, FAKE, FAKE, FAKE, NULL, NULL) == 1
+    assert lib.pa_append_kv_int4(ctypes.byref(shape(head_dim=64)), 3, FAKE, FAKE, FAKE, FAKE, NULL, NULL) == 2
+    assert lib.pa_copy_blocks_int4(ctypes.byref(s), FAKE, -1, FAKE, NULL, NULL) == 1
+    assert lib.pa_copy_blocks_int4(ctypes.byref(s), NULL, 0, NULL, NULL, NULL) == 0
+    assert lib.pa_copy_blocks_int4(ctypes.byref(s), NULL, 2, FAKE, NULL, NULL) == 1
+    assert lib.pa_decode_int4_workspace_bytes(ctypes.byref(shape(head_dim=64))) == 0
+
+
+def test_multi_token_entry_point_checks(lib):
+    s = shape(head_dim=128, num_q_heads=8, num_kv_heads=2)
+
+    def dec(sh, max_q=4, total=8, q=FAKE, q_start=FAKE, scale=0.1):
+        return lib.pa_decode_multi(ctypes.byref(sh), max_q, total, q, q_start, FAKE, FAKE, FAKE, FAKE,
+                                   ctypes.c_float(scale), FAKE, FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+    assert dec(s, max_q=0) == 1 and dec(s, max_q=17) == 1     # chunks of 1..16 tokens
+    assert dec(shape(head_dim=128, num_q_heads=32, num_kv_heads=2), max_q=16) == 2   # 256 rows per pair
+    assert dec(s, total=-1) == 1
+    assert dec(s, q_start=NULL) == 1
+    assert dec(s, q=NULL) == 1                                  # rows to compute but no q
+    assert dec(s, scale=float("inf")) == 1
+    assert dec(shape(head_dim=128, num_q_heads=8, num_kv_heads=2, num_seqs=0)) == 0
+    assert dec(shape(head_dim=96)) == 2
+    assert lib.pa_decode_multi_workspace_bytes(ctypes.byref(s), 0) == 0
+
+
+def test_shared_prefix_and_noalloc_checks(lib):
+    s = shape(head_dim=128, num_q_heads=8, num_kv_heads=2)
+
+    def dec(sh, groups=1, starts=FAKE, prefix=FAKE):
+        return lib.pa_decode_shared_prefix(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, groups, starts, prefix,
+                                           ctypes.c_float(0.1), FAKE, FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+    assert dec(s, groups=-1) == 1
+    assert dec(s, groups=2, starts=NULL) == 1 and dec(s, groups=2, prefix=NULL) == 1
+    assert dec(shape(head_dim=128, num_q_heads=8, num_kv_heads=2, num_seqs=0)) == 0
+    assert dec(shape(num_q_heads=12, num_kv_heads=8)) == 1
+    assert lib.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(shape(block_size=8))) == 0
+    # a shape no decode kernel serves is refused before any scratch is touched
+    assert lib.pa_decode_noalloc(ctypes.byref(shape(head_dim=96)), FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 ctypes.c_float(0.1), FAKE, NULL, NULL) == 1
