@@ -61,6 +61,8 @@ typedef enum pa_dtype { PA_FP16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2, PA_FP8_E5M2 =
 #define PA_DEVERR_COPY_PAIR 8u   /* copy pair id outside [0, num_blocks) */
 #define PA_DEVERR_TIMEOUT   16u  /* a bounded wait expired */
 #define PA_DEVERR_GROUP     32u  /* prefix group malformed, or a member does not share the prefix */
+#define PA_DEVERR_Q_RANGE   64u  /* a bf16 query element beyond fp16's finite range (8-bit and 4-bit
+                                    caches, which compute in fp16); its rows are not finite */
 
 typedef struct pa_shape {
     int32_t num_seqs;            /* N: sequences in the batch (>= 0) */
@@ -143,8 +145,10 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
  * pa_append_kv_int4: quantize k_new / v_new ([T][Hkv][d]) into the pool at
  * slot_mapping (negative skips; past the pool: PA_DEVERR_SLOT).
  * pa_decode_int4: pa_decode over the 4-bit pool (attention over the decoded
- * values); fp16 tensor-core arithmetic on the codes, the K scale applied to
- * each score and the V scale to each softmax weight, fp32 accumulation.
+ * values); fp16 tensor-core arithmetic on the codes (q rounded to fp16; a bf16
+ * query beyond fp16's finite range sets PA_DEVERR_Q_RANGE), the K scale
+ * applied to each score and the V scale to each softmax weight, fp32
+ * accumulation.
  * pa_copy_blocks_int4: copy-on-write copies of whole blocks of the pool.
  */
 size_t pa_decode_int4_workspace_bytes(const pa_shape* shape);
@@ -215,8 +219,9 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
  * pa_decode_fp8: pa_decode over the 8-bit pool, i.e. attention over
  * K = k_scale * decode(code), V = v_scale * decode(code).  It computes in fp16
  * on the tensor cores: q is rounded to fp16 (exact inside fp16's normal
- * range), codes convert to fp16 exactly, accumulation is fp32.  Its workspace
- * is sized by pa_decode_fp8_workspace_bytes.
+ * range; a bf16 query beyond fp16's finite range sets PA_DEVERR_Q_RANGE),
+ * codes convert to fp16 exactly, accumulation is fp32.  Its workspace is sized
+ * by pa_decode_fp8_workspace_bytes.
  * pa_copy_blocks_fp8: copy-on-write copies of whole blocks (all pieces) of
  * the 8-bit pool, as pa_copy_blocks; shape->dtype is the pool's kv_format.
  */
@@ -311,8 +316,10 @@ pa_status pa_copy_blocks(const pa_shape* shape, const int32_t* src_dst_pairs, in
  *  - Shapes whose minimum scratch exceeds PA_NOALLOC_SCRATCH_BYTES are
  *    rejected with PA_ERR_WORKSPACE before anything is enqueued; shapes whose
  *    preferred scratch exceeds it run with fewer run-time balanced chunks.
- *  - The first call on a device looks up the buffer's address on that device
- *    (with it current); make that first call before any stream capture.
+ *  - Every call looks up the buffer's address on the current device (a failed
+ *    lookup returns PA_ERR_CUDA).  The first lookup on a device may load the
+ *    library's device code; make the first call on each device before any
+ *    stream capture.
  *  - Every call on a device shares the one buffer and it keeps the last call's
  *    contents (the call clears the part that must start at zero).  Calls that
  *    overlap on the GPU -- on different streams, or unordered from different
@@ -324,6 +331,22 @@ pa_status pa_decode_noalloc(const pa_shape* shape, const void* q, const void* k_
                             const void* v_pool, const int32_t* block_tables,
                             const int32_t* context_lens, float scale, void* out,
                             uint32_t* err_word, void* stream);
+
+/*
+ * Fault injection for tests of the wait limit (no counterpart on the pages).
+ * With wait_ns > 0, every later launch of the decode attention kernel (by
+ * pa_decode, pa_decode_noalloc, pa_decode_fp8, pa_decode_int4 and the second
+ * pass of pa_decode_shared_prefix), in any thread of the process, makes each
+ * worker warp's first stage wait on a shared-memory barrier that nothing
+ * completes, for at most wait_ns.  When it gives up, the kernel takes its
+ * timeout path: it sets PA_DEVERR_TIMEOUT, issues no further copies, writes
+ * NaN to every output row and partial state of that worker, waits (at the
+ * normal 2 s limit) for its copies still in flight and returns.  The call's
+ * outputs are then NaN (rows of zero-length contexts stay zero) and
+ * pa_read_error returns PA_ERR_TIMEOUT.  wait_ns = 0 turns it off (the
+ * default).  wait_ns above 1e9 (1 s): PA_ERR_INVALID_ARG.
+ */
+pa_status pa_set_decode_stall_ns(uint64_t wait_ns);
 
 /*
  * Synchronise `stream`, read the device error word and map it to a status:

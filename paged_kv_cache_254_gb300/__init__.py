@@ -27,6 +27,7 @@ from .ops import (  # noqa: F401
     int4_pool,
     pa_decode_workspace_bytes,
     pa_read_error,
+    pa_set_decode_stall_ns,
     workspace_for,
 )
 

@@ -21,13 +21,15 @@ STATUS_NAMES = {
 }
 PA_FP16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3
 DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, DEVERR_GROUP = 1, 2, 4, 8, 16, 32
+DEVERR_Q_RANGE = 64
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_decode_workspace_bytes", "pa_decode", "pa_append_kv", "pa_copy_blocks", "pa_read_error",
            "pa_status_string", "pa_version", "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_bytes",
            "pa_decode_shared_prefix", "pa_decode_fp8_workspace_bytes", "pa_decode_fp8", "pa_append_kv_fp8",
            "pa_copy_blocks_fp8", "pa_decode_multi_workspace_bytes", "pa_decode_multi",
-           "pa_decode_int4_workspace_bytes", "pa_decode_int4", "pa_append_kv_int4", "pa_copy_blocks_int4")
+           "pa_decode_int4_workspace_bytes", "pa_decode_int4", "pa_append_kv_int4", "pa_copy_blocks_int4",
+           "pa_set_decode_stall_ns")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -114,6 +116,8 @@ def load() -> ctypes.CDLL:
         lib.pa_append_kv_int4.restype = I32
         lib.pa_copy_blocks_int4.argtypes = [SP, P, I32, P, P, P]
         lib.pa_copy_blocks_int4.restype = I32
+        lib.pa_set_decode_stall_ns.argtypes = [ctypes.c_uint64]
+        lib.pa_set_decode_stall_ns.restype = I32
         _lib = lib
         return lib
 

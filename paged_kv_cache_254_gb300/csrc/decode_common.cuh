@@ -272,14 +272,22 @@ __device__ __forceinline__ void load_q_frags8(uint32_t (&qa)[D / 16][4], const u
     }
 }
 
+// Returns true on this lane if an element left fp16's finite range (a bf16
+// query beyond 65504, or a non-finite one).
 template <int D, bool QBF16>
-__device__ __forceinline__ void q_frags8_to_f16(uint32_t (&qa)[D / 16][4]) {
+__device__ __forceinline__ bool q_frags8_to_f16(uint32_t (&qa)[D / 16][4]) {
+    bool bad = false;
     if constexpr (QBF16) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) qa[kk][i] = bf16x2_to_f16x2(qa[kk][i]);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t h = bf16x2_to_f16x2(qa[kk][i]);
+                bad |= (h & 0x7c00u) == 0x7c00u || (h & 0x7c000000u) == 0x7c000000u;
+                qa[kk][i] = h;
+            }
     }
+    return bad;
 }
 
 // consume_block for the 8-bit cache, over one 32-token stage at kb (Geom8

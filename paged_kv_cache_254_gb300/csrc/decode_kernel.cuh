@@ -69,7 +69,11 @@ struct DecodeParams {
     int32_t nd;                   // dynamic chunks wanted (0: the static split alone)
     int32_t N, Hq, Hkv, NB, MB;
     float scale_log2;             // scale * log2(e)
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;          // limit of every wait on copies
+    // Fault injection for tests (0: off): each worker's first stage wait is
+    // made on a barrier that nothing completes, bounded by stall_ns, so the
+    // timeout path runs; the drain of copies in flight keeps timeout_ns.
+    uint64_t stall_ns;
 };
 
 // KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2;
@@ -108,7 +112,8 @@ struct DecodeTraits {
     static constexpr int FST_OFF = CTX_OFF + CUM_SMEM * 4;  // int [CUM_SMEM] first blocks
     static constexpr int CQ_OFF = FST_OFF + CUM_SMEM * 4;
     static constexpr int PS_OFF = CQ_OFF + NW * QN * 32;    // poison flag per stage
-    static constexpr int SMEM_BYTES = PS_OFF + NW * R * 4 + 1024;  // + alignment slack
+    static constexpr int STALL_OFF = (PS_OFF + NW * R * 4 + 7) & ~7;   // barrier nothing completes (tests)
+    static constexpr int SMEM_BYTES = STALL_OFF + 8 + 1024;  // + alignment slack
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
     static_assert(R >= 2, "two stages per warp at least");
     static_assert(32 % UB == 0, "a batch of 32 table entries holds whole stages");
@@ -241,8 +246,10 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     int* sfst = reinterpret_cast<int*>(smem + Tr::FST_OFF);
     ChunkEnt* cq = reinterpret_cast<ChunkEnt*>(smem + Tr::CQ_OFF) + warp * Tr::QN;
 
+    const uint32_t stall_bar = smem_u32(smem + Tr::STALL_OFF);
     if (lane == 0) {
         for (int st = 0; st < R; ++st) mbar_init(full0 + 8 * st, 1);
+        if (warp == 0) mbar_init(stall_bar, 1);
         fence_mbar_init();
         if constexpr (!Tr::KV8) {
             if (warp == 0) {
@@ -372,17 +379,20 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     };
     open_chunk(next_id);
     long long nis = 0;        // stages issued
+    long long nreal = 0;      // of which with copies (all of them until an abort)
     int ist = 0;              // ring stage of the next fill (nis % R, kept without a division)
-    bool aborted = false;
+    bool aborted = false;     // warp-uniform
+    // After an abort the walk goes on without copies, so every chunk is still
+    // opened, and every row and partial state of this worker is written (NaN).
     auto issue = [&]() {
-        if (idone || aborted) return;
+        if (idone) return;
         const int st = ist;
         if (++ist == R) ist = 0;
         const int nblk = min(UB, ilen - ib);
         int ids[UB];
 #pragma unroll
         for (int u = 0; u < UB; ++u) ids[u] = __shfl_sync(0xffffffffu, tcur, (ib - tbase + u) & 31);
-        if (lane == 0) {
+        if (lane == 0 && !aborted) {
             bool bad = false;
 #pragma unroll
             for (int u = 0; u < UB; ++u) {
@@ -414,6 +424,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         }
         ++nis;
+        if (!aborted) nreal = nis;
         ib += nblk;
         if (ib == ilen) {
             seg_advance(is, ilen, p, tab);
@@ -470,7 +481,13 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     WarpAcc<D, Tr::NR> acc;
     uint32_t qa[Gm::KD][4];
     load_q(qa, it);
-    if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
+    auto q_to_f16 = [&]() {
+        if constexpr (Tr::KV8) {
+            if (__any_sync(0xffffffffu, q_frags8_to_f16<D, Tr::BF16>(qa)) && lane == 0)
+                set_err(p.err, PA_DEVERR_Q_RANGE);
+        }
+    };
+    q_to_f16();
     int ctx = tab.ctx[it.s];
     // The running state starts empty, or -- for the first suffix segment of
     // a sequence whose shared prefix was reduced by the prefix pass -- as the
@@ -528,7 +545,11 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             ++ncons;
             if (!aborted) {
-                if (mbar_wait_bounded(full0 + 8 * st, par, p.timeout_ns)) {
+                // every lane waits; the outcome is made warp-uniform
+                const bool stall = p.stall_ns != 0 && ncons == 1;
+                const bool ok = __all_sync(0xffffffffu, stall ? mbar_wait_bounded(stall_bar, 0, p.stall_ns)
+                                                              : mbar_wait_bounded(full0 + 8 * st, par, p.timeout_ns));
+                if (ok) {
                     nwait = ncons;
                 } else {
                     if (lane == 0) set_err(p.err, PA_DEVERR_TIMEOUT);
@@ -537,6 +558,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             if (aborted) {
                 poisoned = 1;
+                issue();
                 continue;
             }
             poisoned |= stage_poison[st];
@@ -641,14 +663,16 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             ctx = tab.ctx[it.s];
             load_q(qa, it);
         }
-        if constexpr (Tr::KV8) q_frags8_to_f16<D, Tr::BF16>(qa);
+        q_to_f16();
     }
 
-    // After a timeout, wait (bounded) for the copies still in flight before
-    // the CTA's shared memory is released.
+    // After a timeout, wait (bounded, at the full limit) for the copies still
+    // in flight before the CTA's shared memory is released.  Fill k of a ring
+    // stage is issued only after fill k - R was waited for, so the fills not
+    // known to have landed are the last R at most.
     if (aborted && lane == 0) {
-        for (long long k = nwait; k < nis; ++k) {
-            if (k < nis - R) continue;   // an older fill of the same stage
+        for (long long k = nwait; k < nreal; ++k) {
+            if (k < nreal - R) continue;   // an older fill of the same stage
             mbar_wait_bounded(full0 + 8 * (uint32_t)(k % R), (uint32_t)((k / R) & 1), p.timeout_ns);
         }
     }

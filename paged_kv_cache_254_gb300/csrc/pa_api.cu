@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -20,6 +21,10 @@ namespace {
 using namespace pa;
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // bound on any device-side wait
+constexpr uint64_t kMaxStallNs = 1000000000ull;  // longest injected stall (pa_set_decode_stall_ns)
+
+// Injected stall of the decode kernel's first stage wait (0: off).
+std::atomic<uint64_t> g_stall_ns{0};
 
 struct DecodeTables {
     DecodeKernelInfo t[2][2][2][5];   // [bf16][d == 128][bs == 32][log2 g]
@@ -187,6 +192,7 @@ pa_status run_decode(const DecodeKernelInfo* k, int ctas, DecodeLaunch& L, const
     L.p.cum = reinterpret_cast<const long long*>(base + counters_bytes(s));
     L.p.partials = reinterpret_cast<float*>(base + fixed);
     L.p.nd = (int32_t)nd;
+    L.p.stall_ns = g_stall_ns.load(std::memory_order_relaxed);
     L.grid = ctas;
     L.bf16 = s->dtype == PA_BF16;
     pa_decode_prepass<<<1, 1024, 0, L.stream>>>(L.p.context_lens, first_blocks, s->num_seqs,
@@ -374,7 +380,37 @@ size_t shared_prefix_layout(const pa_shape* s, long long dec_workers, int pre_ct
 
 }  // namespace
 
+namespace pa {
+
+// Smallest scratch pa_decode accepts for `shape` on the current device (one
+// chunk per worker warp), or 0 with *why set when the shape is invalid or
+// unsupported (its status) or a CUDA query fails (PA_ERR_CUDA).
+size_t decode_min_workspace_bytes(const pa_shape* shape, pa_status* why) {
+    const DecodeKernelInfo* k = nullptr;
+    const pa_status st = pick_decode(shape, &k);
+    if (st != PA_OK) {
+        *why = st;
+        return 0;
+    }
+    int dev = 0;
+    const int ctas = cudaGetDevice(&dev) == cudaSuccess ? k->max_ctas(dev) : -1;
+    if (ctas <= 0) {
+        *why = PA_ERR_CUDA;
+        return 0;
+    }
+    *why = PA_OK;
+    return decode_region_bytes(shape, (long long)ctas * k->workers, 0);
+}
+
+}  // namespace pa
+
 extern "C" {
+
+pa_status pa_set_decode_stall_ns(uint64_t wait_ns) {
+    if (wait_ns > kMaxStallNs) return PA_ERR_INVALID_ARG;
+    g_stall_ns.store(wait_ns, std::memory_order_relaxed);
+    return PA_OK;
+}
 
 size_t pa_decode_workspace_bytes(const pa_shape* shape) {
     const DecodeKernelInfo* k = nullptr;

@@ -153,6 +153,14 @@ def pa_copy_blocks(src_dst_pairs, k_pool, v_pool, err=None, stream=None):
     _lib.check(st, "pa_copy_blocks")
 
 
+def pa_set_decode_stall_ns(wait_ns: int) -> None:
+    """Fault injection for tests (see include/pa.h): with wait_ns > 0 every
+    later decode launch makes each worker's first stage wait on a barrier
+    that nothing completes, for at most wait_ns, so the kernel's timeout path
+    runs; 0 turns it off."""
+    _lib.check(_lib.load().pa_set_decode_stall_ns(ctypes.c_uint64(int(wait_ns))), "pa_set_decode_stall_ns")
+
+
 def pa_read_error(err, stream=None) -> int:
     """Synchronise the stream and return the status the error word maps to."""
     _need_cuda("err", err, torch.int32)

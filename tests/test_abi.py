@@ -45,11 +45,35 @@ def shape(**kw):
     return _lib.PaShape(*[base[f] for f, _ in _lib.PaShape._fields_])
 
 
-FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: checks fail before any launch
 NULL = ctypes.c_void_p(0)
+BUF_BYTES = 1 << 20
+_bufs = []
 
 
-def decode_status(lib, s, q=FAKE, scale=0.125, ws=FAKE, ws_bytes=1 << 30):
+def _real_buffer(nbytes=BUF_BYTES):
+    """Real, zeroed, 256-byte aligned memory for the pointer arguments whose
+    checks these tests exercise.  With a GPU present it is device memory, so a
+    host check that regressed would send a kernel to valid memory of the size
+    the call is told, never to an unmapped address; without one it is host
+    memory (no kernel can launch)."""
+    try:
+        import torch
+        cuda = torch.cuda.is_available()
+    except Exception:   # pragma: no cover
+        cuda = False
+    if cuda:
+        t = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        _bufs.append(t)
+        return ctypes.c_void_p(t.data_ptr())
+    b = (ctypes.c_uint8 * (nbytes + 256))()
+    _bufs.append(b)
+    return ctypes.c_void_p((ctypes.addressof(b) + 255) & ~255)
+
+
+FAKE = _real_buffer()   # every pointer argument that must pass the null check
+
+
+def decode_status(lib, s, q=FAKE, scale=0.125, ws=FAKE, ws_bytes=BUF_BYTES):
     return lib.pa_decode(ctypes.byref(s), q, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(scale), FAKE, ws,
                          ctypes.c_size_t(ws_bytes), NULL, NULL)
 
@@ -72,7 +96,7 @@ def test_decode_rejects_bad_shapes(lib, kw, status):
 def test_decode_rejects_null_and_misaligned(lib):
     s = shape()
     assert decode_status(lib, s, q=NULL) == 1
-    assert decode_status(lib, s, q=ctypes.c_void_p((1 << 20) + 2)) == 1
+    assert decode_status(lib, s, q=ctypes.c_void_p(FAKE.value + 2)) == 1
     assert decode_status(lib, s, scale=float("nan")) == 1
     assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), FAKE, FAKE, 0, NULL, NULL) == 1
 
@@ -112,7 +136,7 @@ def test_fp8_entry_point_checks(lib):
 
     def dec(sh, fmt=2, ks=1.0, vs=1.0, q=FAKE):
         return lib.pa_decode_fp8(ctypes.byref(sh), fmt, q, FAKE, FAKE, FAKE, f(0.1), f(ks), f(vs), FAKE,
-                                 FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+                                 FAKE, ctypes.c_size_t(BUF_BYTES), NULL, NULL)
     assert dec(s, fmt=0) == 1                      # a 16-bit code is not an 8-bit format
     assert dec(s, ks=0.0) == 1 and dec(s, vs=float("inf")) == 1
     assert dec(shape(head_dim=64)) == 2            # 8-bit cache rows must be 128 bytes
@@ -141,7 +165,7 @@ def test_int4_entry_point_checks(lib):
 
     def dec(sh, q=FAKE, scale=0.1):
         return lib.pa_decode_int4(ctypes.byref(sh), q, FAKE, FAKE, FAKE, f(scale), FAKE, FAKE,
-                                  ctypes.c_size_t(1 << 30), NULL, NULL)
+                                  ctypes.c_size_t(BUF_BYTES), NULL, NULL)
     assert dec(shape(head_dim=64)) == 2                     # the 4-bit layout is for head_dim 128
     assert dec(shape(head_dim=128, block_size=8)) == 2
     assert dec(s, q=NULL) == 1 and dec(s, scale=float("nan")) == 1
@@ -161,7 +185,7 @@ def test_multi_token_entry_point_checks(lib):
 
     def dec(sh, max_q=4, total=8, q=FAKE, q_start=FAKE, scale=0.1):
         return lib.pa_decode_multi(ctypes.byref(sh), max_q, total, q, q_start, FAKE, FAKE, FAKE, FAKE,
-                                   ctypes.c_float(scale), FAKE, FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+                                   ctypes.c_float(scale), FAKE, FAKE, ctypes.c_size_t(BUF_BYTES), NULL, NULL)
     assert dec(s, max_q=0) == 1 and dec(s, max_q=17) == 1     # chunks of 1..16 tokens
     assert dec(shape(head_dim=128, num_q_heads=32, num_kv_heads=2), max_q=16) == 2   # 256 rows per pair
     assert dec(s, total=-1) == 1
@@ -178,12 +202,19 @@ def test_shared_prefix_and_noalloc_checks(lib):
 
     def dec(sh, groups=1, starts=FAKE, prefix=FAKE):
         return lib.pa_decode_shared_prefix(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, groups, starts, prefix,
-                                           ctypes.c_float(0.1), FAKE, FAKE, ctypes.c_size_t(1 << 30), NULL, NULL)
+                                           ctypes.c_float(0.1), FAKE, FAKE, ctypes.c_size_t(BUF_BYTES), NULL, NULL)
     assert dec(s, groups=-1) == 1
     assert dec(s, groups=2, starts=NULL) == 1 and dec(s, groups=2, prefix=NULL) == 1
     assert dec(shape(head_dim=128, num_q_heads=8, num_kv_heads=2, num_seqs=0)) == 0
     assert dec(shape(num_q_heads=12, num_kv_heads=8)) == 1
     assert lib.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(shape(block_size=8))) == 0
     # a shape no decode kernel serves is refused before any scratch is touched
-    assert lib.pa_decode_noalloc(ctypes.byref(shape(head_dim=96)), FAKE, FAKE, FAKE, FAKE, FAKE,
-                                 ctypes.c_float(0.1), FAKE, NULL, NULL) == 1
+    assert lib.pa_decode_noalloc(ctypes.byref(shape(head_dim=96)), NULL, NULL, NULL, NULL, NULL,
+                                 ctypes.c_float(0.1), NULL, NULL, NULL) == 2
+    assert lib.pa_decode_noalloc(ctypes.byref(shape(num_q_heads=12, num_kv_heads=8)), NULL, NULL, NULL, NULL,
+                                 NULL, ctypes.c_float(0.1), NULL, NULL, NULL) == 1
+
+
+def test_stall_setter_checks_its_limit(lib):
+    assert lib.pa_set_decode_stall_ns(2_000_000_000) == 1   # above one second
+    assert lib.pa_set_decode_stall_ns(0) == 0

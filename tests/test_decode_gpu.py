@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from oracle.attention import decode_ref
-from tests.gpu_util import assert_close, dev_case, need_gpu
+from tests.gpu_util import assert_close, dev_case, need_gpu, plant_key, sharpen
 from workloads import CONFIGS, DecodeConfig, make_decode_case
 
 pytestmark = pytest.mark.gpu
@@ -181,3 +181,48 @@ def test_long_context_mha_full_size_sampled():
     assert_close(out, oracle(case, rows=rows), rows=rows, what="long_mha_32k")
     del case
     torch.cuda.empty_cache()
+
+
+# ---- peaked softmaxes: the running maximum moves, one weight dominates ----
+PEAK = [(8.0, 0.0), (32.0, 0.0), (2.0, 6.0)]      # (q multiplier, K growth along the context)
+MIX = (3000, 17, 5000, 4096, 1, 777, 33, 1500)    # pairs cut by chunk boundaries, and short ones
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d,B,g,Hkv", [(128, 16, 8, 8), (128, 32, 16, 4), (64, 16, 1, 8), (128, 16, 4, 4)])
+@pytest.mark.parametrize("q_mult,k_growth", PEAK)
+def test_peaked_softmax(dtype, d, B, g, Hkv, q_mult, k_growth):
+    cfg = small_cfg(MIX, Hq=Hkv * g, Hkv=Hkv, d=d, B=B, dtype=dtype, seed=200 + d + B + g)
+    case = make_decode_case(cfg, device="cuda")
+    sharpen(case, q_mult, k_growth)
+    assert_close(run(case), oracle(case), what=f"peaked {dtype} d{d} B{B} g{g} x{q_mult} +{k_growth}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_dominant_key_late_in_a_split_context(dtype):
+    # one key per sequence far above the rest, planted in the last blocks of
+    # long contexts (after many stages and chunk boundaries) or at the start
+    cfg = small_cfg(MIX, Hq=64, Hkv=8, dtype=dtype, seed=241)
+    case = make_decode_case(cfg, device="cuda")
+    for s, n in enumerate(case.context_lens):
+        plant_key(case, s, int(n) - 1 - (s % 3) * 7 if n > 21 else 0)
+    assert_close(run(case), oracle(case), what=f"dominant late key {dtype}")
+
+
+def test_32k_contexts_with_the_maximum_in_a_middle_piece():
+    # multi-head 32K contexts are cut into many pieces; the dominant key sits
+    # in a middle piece, so the merge's exp(m_p - M) factors decide the result
+    cfg = small_cfg([32768, 32768], Hq=8, Hkv=8, dtype="bf16", seed=251)
+    case = make_decode_case(cfg, device="cuda")
+    sharpen(case, 2.0)
+    plant_key(case, 0, 16000, target=12.0)
+    plant_key(case, 1, 20001, target=25.0)
+    assert_close(run(case), oracle(case), what="32K, maximum in a middle piece")
+
+
+def test_llama3_70b_batch256_peaked_sampled():
+    case = make_decode_case(CONFIGS["llama3_70b_b256"], device="cuda", seed=1013)
+    sharpen(case, 8.0)
+    out = run(case)
+    rows = sample_rows(case, 10, 15)
+    assert_close(out, oracle(case, rows=rows), rows=rows, what="llama3_70b_b256 peaked")

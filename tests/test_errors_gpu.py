@@ -87,3 +87,52 @@ def test_unsupported_shapes_raise():
     with pytest.raises(pa().PagedAttentionError, match="WORKSPACE"):
         pa().pa_decode(case.q, case.k_pool, case.v_pool, torch.from_numpy(case.block_tables).cuda(),
                        torch.from_numpy(case.context_lens).cuda(), case.scale, workspace=small_ws)
+
+
+def test_a_wait_that_runs_out_sets_timeout_and_the_call_returns():
+    """Fault injection on the host side: every worker's first stage wait is
+    made on a barrier that nothing completes, with a 200 us limit.  The kernel
+    must report PA_ERR_TIMEOUT, write NaN to every row (also the rows of pairs
+    split across chunks, which go through the merge), drain its copies and
+    return; the next call at the normal limit is clean and correct."""
+    from oracle.attention import decode_ref
+    case = case_with([3000, 17, 5000, 4096, 1, 777] * 4, Hq=64, Hkv=8)
+    want = decode_ref(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, case.scale)
+    pa().pa_set_decode_stall_ns(200_000)
+    try:
+        out, err = decode(case, case.block_tables, case.context_lens.copy())
+        assert pa().pa_read_error(err) == 5                  # PA_ERR_TIMEOUT
+        assert int(err.item()) & 16
+        assert torch.isnan(out.float()).all()
+    finally:
+        pa().pa_set_decode_stall_ns(0)
+    out, err = decode(case, case.block_tables, case.context_lens.copy())
+    assert pa().pa_read_error(err) == 0
+    assert_close(out, want, what="after the timeout")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "int4"])
+def test_timeout_path_of_the_quantized_decodes(kind):
+    from workloads import make_codes, make_int4_pool
+    case = case_with([700, 2000, 33], Hq=16, Hkv=2)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    bt = torch.from_numpy(case.block_tables).cuda()
+    cl = torch.from_numpy(case.context_lens).cuda()
+    if kind == "fp8":
+        pool = make_codes((case.num_blocks, 2, 2, 16, 128), g, "cuda")
+        run = lambda err: pa().pa_decode_fp8(case.q, pool, bt, cl, case.scale, 0.25, 0.25, err=err)  # noqa: E731
+    else:
+        pool = make_int4_pool(case.num_blocks, 2, 16, 128, g, "cuda")
+        run = lambda err: pa().pa_decode_int4(case.q, pool, bt, cl, case.scale, err=err)  # noqa: E731
+    pa().pa_set_decode_stall_ns(100_000)
+    try:
+        err = pa().new_error_word("cuda")
+        out = run(err)
+        assert pa().pa_read_error(err) == 5
+        assert torch.isnan(out.float()).all()
+    finally:
+        pa().pa_set_decode_stall_ns(0)
+    err = pa().new_error_word("cuda")
+    out = run(err)
+    assert pa().pa_read_error(err) == 0
+    assert torch.isfinite(out.float()).all()

@@ -9,7 +9,7 @@ import torch
 from oracle.attention import decode_ref
 from oracle.fp8 import append_fp8_ref, dequantized_pools
 from oracle.kv_ops import copy_ref
-from tests.gpu_util import assert_close, need_gpu
+from tests.gpu_util import assert_close, need_gpu, plant_key
 from workloads import CONFIGS, DecodeConfig, make_codes, make_decode_case, make_values
 
 pytestmark = pytest.mark.gpu
@@ -135,3 +135,69 @@ def oracle_rows(case, q, kv, rows):
     kf, vf = dequantized_pools(u8(kv.index_select(0, idx)), 16, 0.25, 0.25, "e4m3")
     tables = np.vectorize(lambda b: remap.get(int(b), -1))(case.block_tables)
     return decode_ref(q, kf, vf, tables, case.context_lens, case.scale, rows=rows)
+
+
+# ---- every finite code, peaked softmaxes, the quantising append at full batch ----
+# All finite codes of a format: magnitudes below 0x7F (E4M3: 0x7F is NaN) or
+# 0x7C (E5M2: 0x7C is infinity, above it NaN).  The scales map the largest
+# code to |k| = 8 and |v| = 4, the range the tolerance is stated for.
+FULL = {"e4m3": (0x7F, 448.0), "e5m2": (0x7C, 57344.0)}
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,g", [(16, 8), (32, 16), (16, 1)])
+def test_decode_over_every_finite_code(fmt, dtype, B, g):
+    below, top = FULL[fmt]
+    ctx = [1, 17, 100, 1000, 3001, 5000, 33, 777]
+    case, q, _ = fp8_case(ctx, 2 * g, 2, B, dtype, fmt, seed=300 + g + B)
+    gen = torch.Generator(device="cuda").manual_seed(301 + g)
+    kv = make_codes((case.num_blocks, 2, 2, B, 128), gen, "cuda", below)
+    ks, vs = 8.0 / top, 4.0 / top
+    err = pa().new_error_word("cuda")
+    out = run(case, q, kv, ks, vs, fmt, err=err)
+    assert pa().pa_read_error(err) == 0
+    assert_close(out, oracle(case, q, kv, ks, vs, fmt), what=f"fp8 full range {fmt} {dtype} B{B} g{g}")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("q_mult", [8.0, 32.0])
+def test_peaked_softmax(fmt, q_mult):
+    ctx = [3000, 17, 5000, 4096, 1, 777, 33, 1500]
+    case, q, kv = fp8_case(ctx, 64, 8, 16, "bf16", fmt, seed=310)
+    q.mul_(q_mult)
+    assert_close(run(case, q, kv, 0.3, 0.5, fmt), oracle(case, q, kv, 0.3, 0.5, fmt), what=f"fp8 peaked {fmt} x{q_mult}")
+
+
+def test_append_then_decode_full_batch():
+    """Every sequence of a 256-sequence batch appends its newest token --
+    N(0,1) * 3 values, quantised with scales that use the upper codes -- and
+    the decode reads it back, with one planted key that dominates."""
+    from oracle.kv_ops import slot_of
+    r = np.random.Generator(np.random.PCG64(320))
+    ctx = [int(c) for c in r.integers(16, 300, size=256, endpoint=True)]
+    case, q, kv = fp8_case(ctx, 16, 2, 16, "bf16", "e4m3", seed=321)
+    g = torch.Generator(device="cuda").manual_seed(322)
+    kn = make_values((256, 2, 128), "bf16", g, "cuda") * 3
+    vn = make_values((256, 2, 128), "bf16", g, "cuda") * 3
+    slots = np.array([slot_of(case.block_tables[s], ctx[s] - 1, 16) for s in range(256)], dtype=np.int64)
+    ks, vs = 0.05, 0.05
+    want = append_fp8_ref(u8(kv), kn.float().cpu().numpy(), vn.float().cpu().numpy(), slots, 16, ks, vs, "e4m3")
+    assert (want.reshape(-1) & 0x7F).max() > 0x70        # codes far above the random fill's range
+    pa().pa_append_kv_fp8(kn, vn, torch.from_numpy(slots).cuda(), kv, ks, vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(u8(kv).reshape(want.shape), want)
+    out = run(case, q, kv, ks, vs, "e4m3")
+    kf, vf = dequantized_pools(want, 16, ks, vs, "e4m3")
+    assert_close(out, decode_ref(q, kf, vf, case.block_tables, case.context_lens, case.scale),
+                 what="append+decode, full batch")
+
+
+def test_query_beyond_fp16_range_is_flagged():
+    case, q, kv = fp8_case([40, 70], 16, 2, 16, "bf16", "e4m3", seed=330)
+    q[1, 3, 5] = 1e6                                     # finite in bf16, not in fp16
+    err = pa().new_error_word("cuda")
+    out = run(case, q, kv, 0.3, 0.5, "e4m3", err=err)
+    assert pa().pa_read_error(err) == 4
+    assert int(err.item()) == 64                         # PA_DEVERR_Q_RANGE
+    assert torch.isfinite(out[0].float()).all()

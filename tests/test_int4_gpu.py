@@ -153,3 +153,36 @@ def test_masked_slots_with_non_finite_scales(B):
     got = decode(case, pool)
     assert torch.isfinite(got.float()).all()
     assert_close(got, want, what=f"non-finite masked scales B{B}")
+
+
+# ---- peaked softmaxes over the 4-bit cache ----
+def grow_k_scales(case, pool, growth):
+    """Multiply the K scale of every sequence's cached token t by
+    1 + growth * (t + 1) / ctx, so later keys score higher (the running
+    maximum keeps rising)."""
+    B = pool.shape[2]
+    raw = pool.view(pool.shape[0], pool.shape[1], -1)
+    ks = B * 128                                          # K scales follow the K and V codes
+    for s, n in enumerate(case.context_lens):
+        n = int(n)
+        nb = -(-n // B)
+        ids = torch.from_numpy(case.block_tables[s, :nb].astype(np.int64)).cuda()
+        sc = raw[ids, :, ks:ks + 4 * B].contiguous().view(torch.float32)          # [nb, Hkv, B]
+        t = torch.arange(nb * B, device="cuda", dtype=torch.float32).reshape(nb, 1, B)
+        sc = sc * (1.0 + growth * (t + 1.0) / n)
+        raw[ids, :, ks:ks + 4 * B] = sc.contiguous().view(torch.uint8).view(nb, raw.shape[1], 4 * B)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,g", [(16, 8), (32, 16), (16, 1)])
+@pytest.mark.parametrize("q_mult,growth", [(8.0, 0.0), (32.0, 0.0), (2.0, 6.0)])
+def test_peaked_softmax(dtype, B, g, q_mult, growth):
+    ctx = [3000, 17, 2000, 1, 777, 33, 1500]
+    Hkv = 2
+    case, pool = int4_case(ctx, Hkv * g, Hkv, B, dtype, seed=400 + B + g)
+    case.q.mul_(q_mult)
+    if growth:
+        grow_k_scales(case, pool, growth)
+    kf, vf = dequantized_pools(flat(pool), B, 128)
+    want = decode_ref(case.q, kf, vf, case.block_tables, case.context_lens, case.scale)
+    assert_close(decode(case, pool), want, what=f"int4 peaked {dtype} B{B} g{g} x{q_mult} +{growth}")

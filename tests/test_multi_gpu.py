@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from oracle.attention import decode_multi_ref, decode_ref
-from tests.gpu_util import assert_close, dev_case, need_gpu
+from tests.gpu_util import assert_close, dev_case, need_gpu, plant_key, sharpen
 from workloads import CONFIGS, DecodeConfig, make_decode_case, make_values
 
 pytestmark = pytest.mark.gpu
@@ -162,3 +162,30 @@ def test_host_rejects_unsupported_chunks():
         run(case, q, qs, max_q=9)                # 9 x 16 rows > 128
     with pytest.raises(pa().PagedAttentionError, match="INVALID"):
         run(case, q, qs, max_q=17)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("q_mult,k_growth", [(8.0, 0.0), (32.0, 0.0), (2.0, 6.0)])
+@pytest.mark.parametrize("g,max_q", [(8, 4), (4, 2), (1, 16)])
+def test_peaked_chunks(dtype, q_mult, k_growth, g, max_q):
+    # mma.sync kernel (up to 32 query rows per pair) on peaked softmaxes
+    ctx = [3000, 17, 2000, 4, 777, 33, 1500]
+    rng = np.random.Generator(np.random.PCG64(500 + g + max_q))
+    qlens = chunk_lens(ctx, max_q, rng)
+    qlens[0] = max_q
+    case, q, qs = multi_case(ctx, qlens, Hq=2 * g, Hkv=2, dtype=dtype, seed=501 + g)
+    q.mul_(q_mult)
+    sharpen(case, 1.0, k_growth)
+    assert_close(run(case, q, qs, max_q=max_q), oracle(case, q, qs), what=f"peaked chunks {dtype} g{g} q{max_q}")
+
+
+def test_dominant_keys_inside_and_before_the_chunk():
+    ctx = [2500, 700, 40]
+    qlens = [4, 3, 4]
+    case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=511)
+    # for the first chunk token of sequence 0: a key far before the chunk, and
+    # one inside the chunk that only its later tokens see
+    plant_key(case, 0, 1000, target=20.0, q=q[qs[0]])
+    plant_key(case, 0, 2498, target=35.0, q=q[qs[0] + 3])
+    plant_key(case, 1, 698, target=28.0, q=q[qs[1] + 2])
+    assert_close(run(case, q, qs, max_q=4), oracle(case, q, qs), what="planted keys, multi-token")

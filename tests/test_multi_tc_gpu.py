@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from oracle.attention import decode_multi_ref
-from tests.gpu_util import assert_close, dev_case, need_gpu
+from tests.gpu_util import assert_close, dev_case, need_gpu, plant_key, sharpen
 from workloads import CONFIGS, DecodeConfig, make_decode_case, make_values
 
 pytestmark = pytest.mark.gpu
@@ -187,3 +187,17 @@ def test_bad_context_length_poisons_its_rows(max_q):
     ref = decode_multi_ref(q[keep], case.k_pool, case.v_pool, case.block_tables[sub], case.context_lens[sub],
                            sub_qs, case.scale)
     assert_close(got[keep], ref, what=f"well-formed sequences, max_q {max_q}")
+
+
+@pytest.mark.parametrize("q_mult", [8.0, 32.0])
+def test_peaked_and_planted_keys_tcgen05(q_mult):
+    # 64 query rows per pair (tcgen05 kernel): peaked scores plus keys that
+    # dominate late in long split contexts and inside the chunk
+    ctx = [3000, 2000, 777, 64]
+    qlens = [8, 5, 8, 8]
+    case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=521)
+    q.mul_(q_mult)
+    plant_key(case, 0, 2950, target=60.0, q=q[qs[0]])
+    plant_key(case, 1, 1998, target=45.0, q=q[qs[1] + 4])
+    plant_key(case, 2, 100, target=50.0, q=q[qs[2] + 1])
+    assert_close(run(case, q, qs, max_q=8), oracle(case, q, qs), what=f"tcgen05 peaked x{q_mult}")

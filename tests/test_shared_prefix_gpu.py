@@ -8,7 +8,7 @@ import torch
 
 from oracle.attention import decode_ref, decode_shared_prefix_ref
 from oracle.kv_ops import append_ref, bits, copy_ref, slot_of
-from tests.gpu_util import ATOL, RTOL, assert_close, from_bits, need_gpu
+from tests.gpu_util import ATOL, RTOL, assert_close, from_bits, need_gpu, plant_key
 from workloads import SAMPLING, make_sampling_case, make_values, sampling_tables
 
 pytestmark = pytest.mark.gpu
@@ -176,3 +176,27 @@ def test_prefix_items_split_across_many_ctas(groups, what):
     plain = pa().pa_decode(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(), scale)
     a, b = out.double(), plain.double()
     assert ((a - b).abs() <= ATOL + RTOL * b.abs()).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("q_mult", [1.0, 8.0])
+def test_dominant_keys_in_prefix_and_suffix(dtype, q_mult):
+    """One key planted in the shared prefix and others in members' own
+    blocks, of different heights, so the prefix state (the carry) and the
+    suffix disagree on the running maximum in both directions."""
+    from types import SimpleNamespace
+    d, B, g = 128, 16, 4
+    groups = [(8, 40, [5, 70, 16, 0, 33, 100, 1, 64]), (4, 12, [300, 2, 47, 9])]
+    q, kp, vp, tables, ctx, starts, prefix = grouped_case(91, groups, 4 * g, 4, d, B, dtype, solo=(900, 5))
+    q.mul_(q_mult)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    c = SimpleNamespace(q=q, k_pool=kp, block_tables=tables, scale=scale)
+    plant_key(c, 0, 37, target=18.0)              # in group 0's shared prefix (40 blocks)
+    plant_key(c, 8, 12 * B + 200, target=30.0)    # in member 8's own blocks (group 1)
+    plant_key(c, 2, 40 * B + 10, target=9.0)      # below group 0's prefix key for its first head
+    plant_key(c, 3, 3, target=40.0)               # far above, inside the prefix again
+    plant_key(c, 12, 850, target=25.0)            # a sequence outside every group
+    err = pa().new_error_word("cuda")
+    got = run_sp(q, kp, vp, tables, ctx, starts, prefix, scale, err=err)
+    assert pa().pa_read_error(err) == 0
+    assert_close(got, decode_ref(q, kp, vp, tables, ctx, scale), what=f"planted keys {dtype} x{q_mult}")
