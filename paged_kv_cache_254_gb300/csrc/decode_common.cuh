@@ -42,9 +42,12 @@ struct Geom8 {
     static constexpr int BS = BS_;
     static constexpr int PIECE_BYTES = 2 * BS * 128;
     static constexpr int UB = 32 / BS;
-    static constexpr int STAGE_BYTES = UB * PIECE_BYTES;
-    static constexpr int NT = 4;         // 8-token n-tiles of S^T per stage
-    static constexpr int KT = 2;         // 16-token k-steps of PV per stage
+    // piece u of a stage sits at u * PIECE_PAD: with two pieces per stage the
+    // second is moved by 64 bytes, so the V rows of both pieces that one load
+    // instruction reads fall in different shared-memory banks
+    static constexpr int PIECE_PAD = UB == 2 ? PIECE_BYTES + 64 : PIECE_BYTES;
+    static constexpr int STAGE_BYTES = UB * PIECE_PAD;
+    static constexpr int COPY_BYTES = UB * PIECE_BYTES;   // bytes copied into a full stage
     static constexpr int KD = D / 16;
     static_assert(BS == 16 || BS == 32, "block_size");
 };
@@ -245,15 +248,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-// Token order of the 8-bit path.  In n-tile nt of S^T, column n holds stage
-// token perm_token(nt, n) (n-tiles 0, 1: tokens 0..15; 2, 3: tokens 16..31);
-// it makes the tokens that the PV fragments pair up (2 t4 + e and
-// 2 t4 + 8 + e of a 16-token k-step) sit next to each other in the
-// dims-first V, so a lane reads them with one 4-byte load.
-__device__ __forceinline__ int perm_token(int nt, int n) {
-    return 16 * (nt >> 1) + 4 * (n >> 1) + 2 * (nt & 1) + (n & 1);
-}
-
 // Q fragments for the 8-bit path with the head dims in the order the K bytes
 // are read: k-step kk, fragment column 2 t4 + e -> dim 32 t4 + 4 kk + e,
 // column 2 t4 + 8 + e -> dim 32 t4 + 4 kk + 2 + e.  Loaded as stored (q's
@@ -290,132 +284,6 @@ __device__ __forceinline__ bool q_frags8_to_f16(uint32_t (&qa)[D / 16][4]) {
     return bad;
 }
 
-// consume_block for the 8-bit cache, over one 32-token stage at kb (Geom8
-// layout).  K rows and dims-first V are turned into fp16 fragments in
-// registers; scores and PV run on the fp16 MMA.  Tokens >= valid are masked
-// out; 16-token groups wholly past valid are skipped (their bytes may belong
-// to no copy at all), and the caller has zeroed the V bytes of the masked
-// tokens inside the last group that is used.  The scales are applied outside
-// (K's inside scale_log2, V's at the final write).
-template <class Gm, int NR, bool E5M2>
-__device__ __forceinline__ void consume_stage8(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
-                                               WarpAcc<Gm::D, NR>& acc, float scale_log2, int lane) {
-    constexpr int BS = Gm::BS, PIECE = Gm::PIECE_BYTES;
-    const int g = lane >> 2;
-    const int t4 = lane & 3;
-    float sacc[Gm::NT][4];
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-        if (16 * (nt >> 1) < valid) {
-            const int tok = perm_token(nt, g);
-            const uint32_t rb = kb + (tok / BS) * PIECE + (tok % BS) * 128;
-            uint32_t w[8];
-            uint32_t w0[4], w1[4];
-            lds128(rb + (((2 * t4) ^ (tok & 7)) << 4), w0);
-            lds128(rb + (((2 * t4 + 1) ^ (tok & 7)) << 4), w1);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w[i] = w0[i];
-                w[i + 4] = w1[i];
-            }
-#pragma unroll
-            for (int kk = 0; kk < Gm::KD; ++kk) {
-                const uint32_t b0 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] & 0xffffu));
-                const uint32_t b1 = fp8x2_to_f16x2<E5M2>((uint16_t)(w[kk] >> 16));
-                mma16816<false>(sacc[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-            }
-        }
-    }
-
-    float mx[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) mx[r] = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] *= scale_log2;
-    // only a partial stage (the last of a segment) has slots to mask
-    if (valid < 32) {
-#pragma unroll
-        for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (perm_token(nt, 2 * t4 + (e & 1)) >= valid) sacc[nt][e] = -INFINITY;
-    }
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
-    float alpha[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float m_new = fmaxf(acc.m[r], mx[r]);
-        alpha[r] = ex2(acc.m[r] - m_new);
-        acc.m[r] = m_new;
-        acc.l[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = e >> 1;
-            if (r < NR) {
-                const float pe = ex2(sacc[nt][e] - acc.m[r]);
-                sacc[nt][e] = pe;
-                acc.l[r] += pe;
-            }
-        }
-    uint32_t pb[Gm::KT][NR][2], pl[Gm::KT][NR][2];
-#pragma unroll
-    for (int kt = 0; kt < Gm::KT; ++kt)
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float x0 = sacc[2 * kt + h][2 * r], x1 = sacc[2 * kt + h][2 * r + 1];
-                const uint32_t hi = pack2<false>(x0, x1);
-                pb[kt][r][h] = hi;
-                pl[kt][r][h] = pack2<false>(x0 - lo_of<false>(hi), x1 - hi_of<false>(hi));
-            }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
-        const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
-#pragma unroll
-        for (int mt = 0; mt < Gm::KD; ++mt) {
-            acc.o[mt][r][0] *= aa;
-            acc.o[mt][r][1] *= ab;
-            acc.o[mt][r][2] *= aa;
-            acc.o[mt][r][3] *= ab;
-        }
-    }
-#pragma unroll
-    for (int kt = 0; kt < Gm::KT; ++kt) {
-        if (16 * kt >= valid) break;
-        // V bytes of tokens 16 kt + 4 t4 .. + 3 for dim rows g and g + 8
-        const uint32_t vb = kb + ((16 * kt) / BS) * PIECE + BS * 128 + (16 * kt) % BS + 4 * t4;
-#pragma unroll
-        for (int mt = 0; mt < Gm::KD; ++mt) {
-            const uint32_t x = lds32(vb + (16 * mt + g) * BS);
-            const uint32_t y = lds32(vb + (16 * mt + g + 8) * BS);
-            const uint32_t a0 = fp8x2_to_f16x2<E5M2>((uint16_t)(x & 0xffffu));
-            const uint32_t a2 = fp8x2_to_f16x2<E5M2>((uint16_t)(x >> 16));
-            const uint32_t a1 = fp8x2_to_f16x2<E5M2>((uint16_t)(y & 0xffffu));
-            const uint32_t a3 = fp8x2_to_f16x2<E5M2>((uint16_t)(y >> 16));
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
-                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
-            }
-        }
-    }
-}
-
 // The 4-bit cache (head_dim 128): a (block, KV head) piece is the K codes
 // token-major (BS rows of 64 bytes), the V codes dims-first (128 rows of
 // BS / 2 bytes), then BS fp32 K scales and BS fp32 V scales -- one
@@ -431,180 +299,13 @@ struct Geom4 {
     static constexpr int VS = KS + 4 * BS;             // V scales offset
     static constexpr int PIECE_BYTES = VS + 4 * BS;
     static constexpr int UB = 32 / BS;
-    static constexpr int STAGE_BYTES = UB * PIECE_BYTES;
-    static constexpr int NT = 4;
-    static constexpr int KT = 2;
+    static constexpr int PIECE_PAD = UB == 2 ? PIECE_BYTES + 64 : PIECE_BYTES;   // as Geom8
+    static constexpr int STAGE_BYTES = UB * PIECE_PAD;
+    static constexpr int COPY_BYTES = UB * PIECE_BYTES;
     static constexpr int KD = D / 16;
     static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(PIECE_BYTES % 16 == 0, "pieces are copied in 16-byte units");
 };
-
-// consume_stage8 for the 4-bit cache.  Scores are sums over all dims of
-// q * code, scaled per token by its K scale; P is multiplied by each token's V
-// scale before the PV product (l keeps the plain weights).  Integer codes are
-// always finite, so masked slots need no zeroing; their scales (which may be
-// garbage) are replaced by 0 / skipped.
-template <class Gm, int NR>
-__device__ __forceinline__ void consume_stage4(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
-                                               WarpAcc<Gm::D, NR>& acc, float scale_log2, int lane) {
-    constexpr int BS = Gm::BS, PIECE = Gm::PIECE_BYTES;
-    const int g = lane >> 2;
-    const int t4 = lane & 3;
-    // per-token scales of this lane's columns: tokens 4 t4 .. + 3 and 16 + 4 t4 .. + 3
-    // (K's folded with scale_log2)
-    float ksc[2][4], vsc[2][4];
-#pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
-        const int tok = 16 * hlf + 4 * t4;
-        if (16 * hlf < valid) {
-            const uint32_t pb = kb + (tok / BS) * PIECE + 4 * (tok % BS);
-            uint32_t w[4];
-            lds128(pb + Gm::KS, w);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ksc[hlf][i] = __uint_as_float(w[i]) * scale_log2;
-            lds128(pb + Gm::VS, w);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vsc[hlf][i] = __uint_as_float(w[i]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ksc[hlf][i] = vsc[hlf][i] = 0.f;
-        }
-    }
-    // a partial stage (the last of a segment): masked slots get no V weight
-    if (valid < 32) {
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (16 * hlf + 4 * t4 + i >= valid) vsc[hlf][i] = 0.f;
-    }
-    float sacc[Gm::NT][4];
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-        if (16 * (nt >> 1) < valid) {
-            const int tok = perm_token(nt, g);
-            uint32_t w[4];   // dims 32 t4 .. 32 t4 + 31 of token tok
-            lds128(kb + (tok / BS) * PIECE + (tok % BS) * 64 + 16 * t4, w);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                // k-step 2 i takes pairs 0, 1 of word i; k-step 2 i + 1 pairs 2, 3
-                uint32_t b[4];
-                i4x8_to_f16x2(w[i], b);
-                mma16816<false>(sacc[nt], qa[2 * i][0], qa[2 * i][1], qa[2 * i][2], qa[2 * i][3], b[0], b[1]);
-                mma16816<false>(sacc[nt], qa[2 * i + 1][0], qa[2 * i + 1][1], qa[2 * i + 1][2], qa[2 * i + 1][3],
-                                b[2], b[3]);
-            }
-        }
-    }
-
-    float mx[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) mx[r] = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] *= ksc[nt >> 1][2 * (nt & 1) + (e & 1)];
-    if (valid < 32) {
-#pragma unroll
-        for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (perm_token(nt, 2 * t4 + (e & 1)) >= valid) sacc[nt][e] = -INFINITY;
-    }
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if ((e >> 1) < NR) mx[e >> 1] = fmaxf(mx[e >> 1], sacc[nt][e]);
-    float alpha[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float m_new = fmaxf(acc.m[r], mx[r]);
-        alpha[r] = ex2(acc.m[r] - m_new);
-        acc.m[r] = m_new;
-        acc.l[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = e >> 1;
-            if (r < NR) {
-                const float pe = ex2(sacc[nt][e] - acc.m[r]);
-                sacc[nt][e] = pe;
-                acc.l[r] += pe;
-            }
-        }
-    uint32_t pb[Gm::KT][NR][2], pl[Gm::KT][NR][2];
-#pragma unroll
-    for (int kt = 0; kt < Gm::KT; ++kt)
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int nt = 2 * kt + h;
-                const float x0 = sacc[nt][2 * r] * vsc[kt][2 * h];
-                const float x1 = sacc[nt][2 * r + 1] * vsc[kt][2 * h + 1];
-                const uint32_t hi = pack2<false>(x0, x1);
-                pb[kt][r][h] = hi;
-                pl[kt][r][h] = pack2<false>(x0 - lo_of<false>(hi), x1 - hi_of<false>(hi));
-            }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        const float aa = __shfl_sync(0xffffffffu, alpha[r], (2 * t4) * 4);
-        const float ab = __shfl_sync(0xffffffffu, alpha[r], (2 * t4 + 1) * 4);
-#pragma unroll
-        for (int mt = 0; mt < Gm::KD; ++mt) {
-            acc.o[mt][r][0] *= aa;
-            acc.o[mt][r][1] *= ab;
-            acc.o[mt][r][2] *= aa;
-            acc.o[mt][r][3] *= ab;
-        }
-    }
-#pragma unroll
-    for (int kt = 0; kt < Gm::KT; ++kt) {
-        if (16 * kt >= valid) break;
-        // V nibbles of tokens 16 kt + 4 t4 .. + 3 for dim rows g and g + 8
-        const int loc = (16 * kt) % BS + 4 * t4;
-        const uint32_t vb = kb + ((16 * kt) / BS) * PIECE + Gm::VC + 4 * (loc / 8);
-        const int sh = 8 * ((loc % 8) / 4);
-#pragma unroll
-        for (int mt = 0; mt < Gm::KD; ++mt) {
-            const uint32_t x = lds32(vb + (16 * mt + g) * (BS / 2)) >> sh;
-            const uint32_t y = lds32(vb + (16 * mt + g + 8) * (BS / 2)) >> sh;
-            const uint32_t a0 = i4_pair_lo(x);
-            const uint32_t a2 = i4_pair_hi(x);
-            const uint32_t a1 = i4_pair_lo(y);
-            const uint32_t a3 = i4_pair_hi(y);
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pb[kt][r][0], pb[kt][r][1]);
-                mma16816<false>(acc.o[mt][r], a0, a1, a2, a3, pl[kt][r][0], pl[kt][r][1]);
-            }
-        }
-    }
-}
-
-// Zero, in a 32-token 8-bit stage, the V bytes of tokens valid .. the end of
-// valid's 16-token group (0 < valid < 32; nothing when valid is a multiple
-// of 16, since consume_stage8 skips wholly masked groups).
-template <class Gm>
-__device__ __forceinline__ void zero_v8_tail(uint32_t kb, int valid, int lane) {
-    constexpr int BS = Gm::BS;
-    const int end = (valid + 15) & ~15;
-    const int w = end - valid;
-    if (w == 0) return;
-    const uint32_t vb = kb + (valid / BS) * Gm::PIECE_BYTES + BS * 128 + valid % BS;
-    for (int i = lane; i < Gm::D * w; i += 32) {
-        const int dim = i / w;
-        const uint32_t a = vb + dim * BS + (i - dim * w);
-        asm volatile("st.shared.u8 [%0], %1;" :: "r"(a), "h"((uint16_t)0) : "memory");
-    }
-}
 
 // Zero the V rows at offsets >= valid of a partly filled block (they may hold
 // anything, NaN included, and 0 * NaN would poison the PV product).

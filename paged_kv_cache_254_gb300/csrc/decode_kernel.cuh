@@ -49,6 +49,7 @@
 #include <type_traits>
 
 #include "decode_common.cuh"
+#include "decode_tok.cuh"
 
 namespace pa {
 
@@ -76,6 +77,16 @@ struct DecodeParams {
     uint64_t stall_ns;
 };
 
+// Bytes of pool data a full stage holds (without bank padding).
+template <class Gm, bool KV8>
+constexpr int stage_data_bytes() {
+    if constexpr (KV8) {
+        return Gm::COPY_BYTES;
+    } else {
+        return Gm::STAGE_BYTES;
+    }
+}
+
 // KVF: 0 = the cache holds q's 16-bit type; 1 = FP8 E4M3 codes; 2 = FP8 E5M2;
 // 3 = 4-bit integer codes with per-row scales.  KV8: any quantized cache (one
 // contiguous piece per (block, head), fetched by bulk copies).
@@ -90,17 +101,23 @@ struct DecodeTraits {
     static constexpr int G = G_;
     static constexpr bool BF16 = BF16_;
     static constexpr bool E5M2 = KVF_ == 2;
-    // About 192 KiB of stages per SM: stages of up to 8 KiB, two CTAs of four
-    // warps; 16 KiB stages, one CTA of six warps.  The 4-bit cache (4.3 KiB
-    // stages, more arithmetic per byte) runs three CTAs of four warps: more
-    // warps to hide each stage's latency, at 168 registers.
-    static constexpr int RING_PER_SM = 192 * 1024;
-    static constexpr int MIN_CTAS = I4 ? 3 : Gm::STAGE_BYTES <= 8192 ? 2 : 1;
+    // About 192 KiB of stages per SM (200 KiB for the quantized caches, whose
+    // two-piece stages carry 64 bytes of bank padding): stages of up to 8 KiB
+    // of data, two CTAs of four warps; 16 KiB stages, one CTA of six warps.
+    // The 4-bit cache (4.3 KiB stages, more arithmetic per byte) runs three
+    // CTAs of four warps: more warps to hide each stage's latency (two for
+    // groups of 16 query heads, which need more registers).
+    static constexpr int RING_PER_SM = (KV8 ? 200 : 192) * 1024;
+    static constexpr int DATA_BYTES = stage_data_bytes<Gm, KV8>();
+    static constexpr int MIN_CTAS = I4 ? (G_ > 8 ? 2 : 3) : DATA_BYTES <= 8192 ? 2 : 1;
     static constexpr int NW = MIN_CTAS == 1 ? 6 : 4;       // warps (workers) per CTA
     static constexpr int R_FIT = RING_PER_SM / (MIN_CTAS * NW * Gm::STAGE_BYTES);
     static constexpr int R = R_FIT > 8 ? 8 : R_FIT;        // stages per warp
     static constexpr int THREADS = NW * 32;
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
+    // quantized caches: the stage's tokens are the MMA rows (decode_tok.cuh)
+    static constexpr bool TR = KV8;
+    using Acc = std::conditional_t<TR, WarpAccT<D_, NR>, WarpAcc<D_, NR>>;
     static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad (16-byte rows)
     static constexpr int CSTRIDE = D_ + 2;                  // carry row (prefix pass): o[D], m, l
     static constexpr int CUM_SMEM = 512;                    // sequences whose tables fit in smem
@@ -411,7 +428,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
                     if (u < nblk)
-                        bulk_load(dst + u * Gm::PIECE_BYTES,
+                        bulk_load(dst + u * Gm::PIECE_PAD,
                                   p.kv8 + ((size_t)ids[u] * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES, fb);
             } else {
                 mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
@@ -478,7 +495,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ++qhead;
     };
     pop_chunk();
-    WarpAcc<D, Tr::NR> acc;
+    typename Tr::Acc acc;
     uint32_t qa[Gm::KD][4];
     load_q(qa, it);
     auto q_to_f16 = [&]() {
@@ -496,12 +513,26 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         acc.reset();
         if (it.first > 0 && it.b0 == 0) {
             const float* crow = p.carry + ((size_t)it.s * p.Hq + (size_t)it.kvh * G) * Tr::CSTRIDE;
+            if constexpr (Tr::TR) {
+                // heads 8 r + 2 t4 + c; the sum counted once (lanes g == 0)
 #pragma unroll
-            for (int r = 0; r < Tr::NR; ++r) {
-                const int head = g + 8 * r;
-                if (head < G) {
-                    acc.m[r] = __ldg(crow + head * Tr::CSTRIDE + D);
-                    if (t4 == 0) acc.l[r] = __ldg(crow + head * Tr::CSTRIDE + D + 1);
+                for (int r = 0; r < Tr::NR; ++r)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int head = 8 * r + 2 * t4 + c;
+                        if (head < G) {
+                            acc.m[r][c] = __ldg(crow + head * Tr::CSTRIDE + D);
+                            if (g == 0) acc.l[r][c] = __ldg(crow + head * Tr::CSTRIDE + D + 1);
+                        }
+                    }
+            } else {
+#pragma unroll
+                for (int r = 0; r < Tr::NR; ++r) {
+                    const int head = g + 8 * r;
+                    if (head < G) {
+                        acc.m[r] = __ldg(crow + head * Tr::CSTRIDE + D);
+                        if (t4 == 0) acc.l[r] = __ldg(crow + head * Tr::CSTRIDE + D + 1);
+                    }
                 }
             }
 #pragma unroll
@@ -567,14 +598,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const uint32_t kb = ring + st * Gm::STAGE_BYTES;
             bool zeroed = false;
             if constexpr (Tr::I4) {
-                consume_stage4<Gm, Tr::NR>(kb, valid, qa, acc, p.scale_log2, lane);
+                consume_stage4t<Gm, Tr::NR>(kb, valid, qa, acc, p.scale_log2, lane);
             } else if constexpr (Tr::KV8) {
-                if (valid < 32 && (valid & 15)) {
-                    zero_v8_tail<Gm>(kb, valid, lane);
-                    __syncwarp();
-                    zeroed = true;
-                }
-                consume_stage8<Gm, Tr::NR, Tr::E5M2>(kb, valid, qa, acc, p.scale_log2, lane);
+                consume_stage8t<Gm, Tr::NR, Tr::E5M2>(kb, valid, qa, acc, p.scale_log2, lane);
             } else {
                 const uint32_t vb = kb + Gm::CHUNK_BYTES;
                 if (valid < BS) {
@@ -592,10 +618,22 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
 
         // ---- finish the segment: output rows, or this chunk's piece ----
+        if constexpr (Tr::TR) {
+            // sums over the 8 lanes of a head column (rows g)
 #pragma unroll
-        for (int r = 0; r < Tr::NR; ++r) {
-            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
-            acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
+            for (int r = 0; r < Tr::NR; ++r)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    acc.l[r][c] += __shfl_xor_sync(0xffffffffu, acc.l[r][c], 4);
+                    acc.l[r][c] += __shfl_xor_sync(0xffffffffu, acc.l[r][c], 8);
+                    acc.l[r][c] += __shfl_xor_sync(0xffffffffu, acc.l[r][c], 16);
+                }
+        } else {
+#pragma unroll
+            for (int r = 0; r < Tr::NR; ++r) {
+                acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 1);
+                acc.l[r] += __shfl_xor_sync(0xffffffffu, acc.l[r], 2);
+            }
         }
         const long long P0 = it.gi - it.b0;           // flattened start of this pair
         const long long cfirst = sc.of(P0);
@@ -609,7 +647,12 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int head = 8 * r + 2 * t4 + c;
-                    const float L = __shfl_sync(0xffffffffu, acc.l[r], (2 * t4 + c) * 4);
+                    float L;
+                    if constexpr (Tr::TR) {
+                        L = acc.l[r][c];
+                    } else {
+                        L = __shfl_sync(0xffffffffu, acc.l[r], (2 * t4 + c) * 4);
+                    }
                     if (head < G) {
                         const float inv = p.v_scale / L;
 #pragma unroll
@@ -636,7 +679,20 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                         const int dim = 16 * mt + g + 8 * (e >> 1);
                         if (head < G) prow[head * Tr::PSTRIDE + dim] = poisoned ? qnan : acc.o[mt][r][e];
                     }
-            if (t4 == 0) {
+            if constexpr (Tr::TR) {
+                if (g == 0) {
+#pragma unroll
+                    for (int r = 0; r < Tr::NR; ++r)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int head = 8 * r + 2 * t4 + c;
+                            if (head < G) {
+                                prow[head * Tr::PSTRIDE + D] = acc.m[r][c];
+                                prow[head * Tr::PSTRIDE + D + 1] = acc.l[r][c];
+                            }
+                        }
+                }
+            } else if (t4 == 0) {
 #pragma unroll
                 for (int r = 0; r < Tr::NR; ++r) {
                     const int head = g + 8 * r;

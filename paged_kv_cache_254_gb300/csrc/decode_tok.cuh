@@ -1,0 +1,302 @@
+// The per-stage update of the quantized caches (8-bit floats, 4-bit integers
+// with per-row scales), with the stage's tokens as the MMA rows.
+//
+// A 32-token stage is two m-tiles of 16 tokens.  Scores are S = K Q^T
+// (m = tokens, n = the group's query heads, k = head dims), so a group of up
+// to 8 query heads fills the n = 8 of mma.sync.m16n8k16 and no MMA row is
+// spent on padding.  The output stays O^T += V^T P^T (m = dims, n = heads,
+// k = tokens); P reaches the B operand by one movmatrix transpose per 8x8
+// piece.  P enters as one fp16 value per weight: its rounding (at most 2^-12
+// of the weight) moves an output by at most 2^-12 * max |v|.
+//
+// Row j of m-tile mt holds stage token tok_row(mt, j).  The order is chosen so
+// that lane t4's PV operands (k indices 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 of
+// both k-steps) are the stage tokens 8 t4 .. 8 t4 + 7: one 32-bit word of a
+// 4-bit V row, or 8 bytes of an 8-bit one, feeds both k-steps.
+#pragma once
+
+#include "decode_common.cuh"
+
+namespace pa {
+
+__device__ __forceinline__ int tok_row(int mt, int j) {
+    return 8 * ((j & 7) >> 1) + 4 * mt + 2 * (j >> 3) + (j & 1);
+}
+
+// Running softmax state of one warp with heads as MMA columns: lane (g, t4)
+// keeps, for heads 8 nh + 2 t4 + c, the running maximum m (exp2 domain) and
+// the partial sum l over the tokens of its own rows; o is O^T (dims x heads)
+// in the accumulator layout of WarpAcc.
+template <int D, int NH>
+struct WarpAccT {
+    float m[NH][2], l[NH][2];
+    float o[D / 16][NH][4];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                m[nh][c] = -INFINITY;
+                l[nh][c] = 0.f;
+            }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][nh][e] = 0.f;
+    }
+};
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+}
+
+// Scores sc[mt][nh][e] (already in the exp2 domain, masked tokens -inf) ->
+// softmax update of acc, the weights times vw (per-token V weights of this
+// lane's rows, 0 for masked ones) as transposed fp16 B fragments pb, and the
+// rescale of acc.o.  Rows of this lane: tokens tb + 4 mt + 2 h, h = e >> 1.
+template <int D, int NH>
+__device__ __forceinline__ void softmax_rows(float (&sc)[2][NH][4], const float (&vw)[2][2],
+                                             WarpAccT<D, NH>& acc, uint32_t (&pb)[2][NH][2]) {
+    float alpha[NH][2];
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float mx = fmaxf(fmaxf(sc[0][nh][c], sc[0][nh][2 + c]), fmaxf(sc[1][nh][c], sc[1][nh][2 + c]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(acc.m[nh][c], mx);
+            alpha[nh][c] = ex2(acc.m[nh][c] - m_new);
+            acc.m[nh][c] = m_new;
+            acc.l[nh][c] *= alpha[nh][c];
+        }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) {
+            float w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float pe = ex2(sc[mt][nh][e] - acc.m[nh][e & 1]);
+                acc.l[nh][e & 1] += pe;
+                w[e] = pe * vw[mt][e >> 1];
+            }
+            // rows g (tokens of k index 2 t4, 2 t4 + 1 after the transpose)
+            // and g + 8 (k index 2 t4 + 8, 2 t4 + 9)
+            pb[mt][nh][0] = movm_trans(pack2<false>(w[0], w[1]));
+            pb[mt][nh][1] = movm_trans(pack2<false>(w[2], w[3]));
+        }
+    // this lane's O^T columns are its own heads: no exchange for the factors;
+    // skipped (a multiplication by exactly 1) when no maximum moved
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+        if (__any_sync(0xffffffffu, alpha[nh][0] != 1.f || alpha[nh][1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                acc.o[mt][nh][0] *= alpha[nh][0];
+                acc.o[mt][nh][1] *= alpha[nh][1];
+                acc.o[mt][nh][2] *= alpha[nh][0];
+                acc.o[mt][nh][3] *= alpha[nh][1];
+            }
+        }
+    }
+}
+
+// One 32-token stage of the 4-bit cache (Geom4 layout; piece u of the stage at
+// u * PIECE_PAD).  qa: Q fragments of load_q_frags8 converted to fp16 (for
+// head n-tile nh, k-step kk: b0 = qa[kk][nh], b1 = qa[kk][2 + nh]).  Tokens >=
+// valid are masked; their bytes may be stale (any nibble is a finite code) and
+// their scales anything: masked scores are set to -inf and masked V weights
+// to 0.
+template <class Gm, int NH>
+__device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
+                                                WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
+    constexpr int BS = Gm::BS, PP = Gm::PIECE_PAD;
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    const int tb = 8 * (g >> 1) + (g & 1);   // this lane's rows: tokens tb + 4 mt + 2 h
+    float ks[2][2], vw[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int tok = tb + 4 * mt + 2 * h;
+            const uint32_t a = kb + (tok / BS) * PP + 4 * (tok % BS);
+            ks[mt][h] = lds_f32(a + Gm::KS) * scale_log2;
+            vw[mt][h] = lds_f32(a + Gm::VS);
+        }
+    float sc[2][NH][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][nh][e] = 0.f;
+        const int r0 = tb + 4 * mt, r1 = r0 + 2;
+        uint32_t w0[4], w1[4];   // dims 32 t4 .. 32 t4 + 31 of rows g and g + 8
+        lds128(kb + (r0 / BS) * PP + (r0 % BS) * 64 + 16 * t4, w0);
+        lds128(kb + (r1 / BS) * PP + (r1 % BS) * 64 + 16 * t4, w1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // word i: k-step 2 i takes pairs 0, 1; k-step 2 i + 1 pairs 2, 3
+            uint32_t h0[4], h1[4];
+            i4x8_to_f16x2(w0[i], h0);
+            i4x8_to_f16x2(w1[i], h1);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+                mma16816<false>(sc[mt][nh], h0[0], h1[0], h0[1], h1[1], qa[2 * i][nh], qa[2 * i][2 + nh]);
+                mma16816<false>(sc[mt][nh], h0[2], h1[2], h0[3], h1[3], qa[2 * i + 1][nh], qa[2 * i + 1][2 + nh]);
+            }
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][nh][e] *= ks[mt][e >> 1];
+    // only a partial stage (the last of a segment) has slots to mask
+    if (valid < 32) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (tb + 4 * mt + 2 * h >= valid) {
+                    vw[mt][h] = 0.f;
+#pragma unroll
+                    for (int nh = 0; nh < NH; ++nh) {
+                        sc[mt][nh][2 * h] = -INFINITY;
+                        sc[mt][nh][2 * h + 1] = -INFINITY;
+                    }
+                }
+    }
+    uint32_t pb[2][NH][2];
+    softmax_rows<Gm::D, NH>(sc, vw, acc, pb);
+    // V: lane t4's tokens 8 t4 .. 8 t4 + 7 are one word of each dims-first row
+    const uint32_t vrow = kb + ((8 * t4) / BS) * PP + Gm::VC + 4 * (((8 * t4) % BS) / 8);
+#pragma unroll
+    for (int mt = 0; mt < Gm::KD; ++mt) {
+        const uint32_t x = lds32(vrow + (16 * mt + g) * (BS / 2));
+        const uint32_t y = lds32(vrow + (16 * mt + g + 8) * (BS / 2));
+        uint32_t hx[4], hy[4];
+        i4x8_to_f16x2(x, hx);
+        i4x8_to_f16x2(y, hy);
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh) {
+            mma16816<false>(acc.o[mt][nh], hx[0], hy[0], hx[1], hy[1], pb[0][nh][0], pb[0][nh][1]);
+            mma16816<false>(acc.o[mt][nh], hx[2], hy[2], hx[3], hy[3], pb[1][nh][0], pb[1][nh][1]);
+        }
+    }
+}
+
+// Keep the 16-bit halves of x whose token is below valid (pair tokens t, t + 1).
+__device__ __forceinline__ uint32_t keep_pair(uint32_t x, int t, int valid) {
+    return x & ((t < valid ? 0x0000ffffu : 0u) | (t + 1 < valid ? 0xffff0000u : 0u));
+}
+
+// One 32-token stage of the 8-bit cache (Geom8 layout; piece u at
+// u * PIECE_PAD).  Codes convert to fp16 exactly.  Masked tokens may hold any
+// byte, NaN codes included: their scores are set to -inf and their V operands
+// to zero in registers (MASK: a partial stage).
+template <class Gm, int NH, bool E5M2, bool MASK>
+__device__ __forceinline__ void consume_stage8t_impl(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
+                                                     WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
+    constexpr int BS = Gm::BS, PP = Gm::PIECE_PAD;
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+    const int tb = 8 * (g >> 1) + (g & 1);
+    float sc[2][NH][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][nh][e] = 0.f;
+        const int r0 = tb + 4 * mt, r1 = r0 + 2;
+        const uint32_t b0 = kb + (r0 / BS) * PP + (r0 % BS) * 128;
+        const uint32_t b1 = kb + (r1 / BS) * PP + (r1 % BS) * 128;
+        uint32_t w0[8], w1[8];   // dims 32 t4 .. 32 t4 + 31 of rows g and g + 8 (permuted 16-byte parts)
+        lds128(b0 + (((2 * t4) ^ (r0 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w0[0]));
+        lds128(b0 + (((2 * t4 + 1) ^ (r0 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w0[4]));
+        lds128(b1 + (((2 * t4) ^ (r1 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w1[0]));
+        lds128(b1 + (((2 * t4 + 1) ^ (r1 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w1[4]));
+#pragma unroll
+        for (int kk = 0; kk < Gm::KD; ++kk) {
+            const uint32_t a0 = fp8x2_to_f16x2<E5M2>((uint16_t)(w0[kk] & 0xffffu));
+            const uint32_t a2 = fp8x2_to_f16x2<E5M2>((uint16_t)(w0[kk] >> 16));
+            const uint32_t a1 = fp8x2_to_f16x2<E5M2>((uint16_t)(w1[kk] & 0xffffu));
+            const uint32_t a3 = fp8x2_to_f16x2<E5M2>((uint16_t)(w1[kk] >> 16));
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) mma16816<false>(sc[mt][nh], a0, a1, a2, a3, qa[kk][nh], qa[kk][2 + nh]);
+        }
+    }
+    float vw[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            vw[mt][h] = 1.f;
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+                sc[mt][nh][2 * h] *= scale_log2;
+                sc[mt][nh][2 * h + 1] *= scale_log2;
+                if (MASK && tb + 4 * mt + 2 * h >= valid) sc[mt][nh][2 * h] = sc[mt][nh][2 * h + 1] = -INFINITY;
+            }
+        }
+    uint32_t pb[2][NH][2];
+    softmax_rows<Gm::D, NH>(sc, vw, acc, pb);
+    // V: lane t4's tokens 8 t4 .. 8 t4 + 7 are 8 bytes of each dims-first row
+    const uint32_t vrow = kb + ((8 * t4) / BS) * PP + BS * 128 + (8 * t4) % BS;
+#pragma unroll
+    for (int mt = 0; mt < Gm::KD; ++mt) {
+        uint32_t x0, x1, y0, y1;
+        lds64(vrow + (16 * mt + g) * BS, x0, x1);
+        lds64(vrow + (16 * mt + g + 8) * BS, y0, y1);
+        uint32_t a[2][4];   // [k-step][a0..a3]
+        a[0][0] = fp8x2_to_f16x2<E5M2>((uint16_t)(x0 & 0xffffu));
+        a[0][2] = fp8x2_to_f16x2<E5M2>((uint16_t)(x0 >> 16));
+        a[0][1] = fp8x2_to_f16x2<E5M2>((uint16_t)(y0 & 0xffffu));
+        a[0][3] = fp8x2_to_f16x2<E5M2>((uint16_t)(y0 >> 16));
+        a[1][0] = fp8x2_to_f16x2<E5M2>((uint16_t)(x1 & 0xffffu));
+        a[1][2] = fp8x2_to_f16x2<E5M2>((uint16_t)(x1 >> 16));
+        a[1][1] = fp8x2_to_f16x2<E5M2>((uint16_t)(y1 & 0xffffu));
+        a[1][3] = fp8x2_to_f16x2<E5M2>((uint16_t)(y1 >> 16));
+        if (MASK) {
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                const int t = 8 * t4 + 4 * kt;
+                a[kt][0] = keep_pair(a[kt][0], t, valid);
+                a[kt][1] = keep_pair(a[kt][1], t, valid);
+                a[kt][2] = keep_pair(a[kt][2], t + 2, valid);
+                a[kt][3] = keep_pair(a[kt][3], t + 2, valid);
+            }
+        }
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+                mma16816<false>(acc.o[mt][nh], a[kt][0], a[kt][1], a[kt][2], a[kt][3], pb[kt][nh][0], pb[kt][nh][1]);
+    }
+}
+
+template <class Gm, int NH, bool E5M2>
+__device__ __forceinline__ void consume_stage8t(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
+                                                WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
+    if (valid < 32) {
+        consume_stage8t_impl<Gm, NH, E5M2, true>(kb, valid, qa, acc, scale_log2, lane);
+    } else {
+        consume_stage8t_impl<Gm, NH, E5M2, false>(kb, valid, qa, acc, scale_log2, lane);
+    }
+}
+
+}  // namespace pa

@@ -129,6 +129,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one row pair per lane
+// (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1); the result has
+// the same layout.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+    uint32_t r;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // Pure register arithmetic (not volatile): the compiler may schedule it
 // around the (volatile, ordered) shared-memory loads that feed it.
 template <bool BF16>
