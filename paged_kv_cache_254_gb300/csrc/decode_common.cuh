@@ -49,6 +49,8 @@ struct Geom8 {
     static constexpr int STAGE_BYTES = UB * PIECE_PAD;
     static constexpr int COPY_BYTES = UB * PIECE_BYTES;   // bytes copied into a full stage
     static constexpr int KD = D / 16;
+    static constexpr int TOK = 32;                         // tokens per stage
+    __host__ __device__ static constexpr int poff(int u) { return u * PIECE_PAD; }
     static_assert(BS == 16 || BS == 32, "block_size");
 };
 
@@ -289,7 +291,7 @@ __device__ __forceinline__ bool q_frags8_to_f16(uint32_t (&qa)[D / 16][4]) {
 // BS / 2 bytes), then BS fp32 K scales and BS fp32 V scales -- one
 // contiguous run of PIECE_BYTES in the pool.  Codes are nibbles code + 8; in
 // each 32-bit word of 8 elements, element 2k sits in nibble k and element
-// 2k + 1 in nibble k + 4.  A ring stage holds UB blocks of one pair: 32 tokens.
+// 2k + 1 in nibble k + 4.  A ring stage holds UB blocks of one pair: 64 tokens.
 template <int BS_>
 struct Geom4 {
     static constexpr int D = 128;
@@ -298,9 +300,19 @@ struct Geom4 {
     static constexpr int KS = BS * 128;                // K scales offset
     static constexpr int VS = KS + 4 * BS;             // V scales offset
     static constexpr int PIECE_BYTES = VS + 4 * BS;
-    static constexpr int UB = 32 / BS;
-    static constexpr int PIECE_PAD = UB == 2 ? PIECE_BYTES + 64 : PIECE_BYTES;   // as Geom8
-    static constexpr int STAGE_BYTES = UB * PIECE_PAD;
+    // a stage is 64 tokens: two halves of 32, each read like an 8-bit stage
+    static constexpr int TOK = 64;
+    static constexpr int UB = TOK / BS;
+    // piece u at poff(u): with 16-token blocks 64 bytes of padding follow
+    // every even piece, so the two pieces of a half start 64 bytes apart
+    // modulo 128 and sit in different shared-memory banks
+    __host__ __device__ static constexpr int poff(int u) {
+        return u * PIECE_BYTES + (BS == 16 ? 64 * ((u + 1) >> 1) : 0);
+    }
+    static_assert(BS == 32 || (PIECE_BYTES % 128 == 0 && (poff(1) - poff(0)) % 128 == 64 &&
+                               (poff(3) - poff(2)) % 128 == 64 && poff(2) >= poff(1) + PIECE_BYTES),
+                  "pieces of a stage must not overlap, and the two of a half must differ by 64 modulo 128");
+    static constexpr int STAGE_BYTES = poff(UB - 1) + PIECE_BYTES;
     static constexpr int COPY_BYTES = UB * PIECE_BYTES;
     static constexpr int KD = D / 16;
     static_assert(BS == 16 || BS == 32, "block_size");

@@ -104,15 +104,15 @@ struct DecodeTraits {
     // About 192 KiB of stages per SM (200 KiB for the quantized caches, whose
     // two-piece stages carry 64 bytes of bank padding): stages of up to 8 KiB
     // of data, two CTAs of four warps; 16 KiB stages, one CTA of six warps.
-    // The 4-bit cache (4.3 KiB stages, more arithmetic per byte) runs three
-    // CTAs of four warps: more warps to hide each stage's latency (two for
-    // groups of 16 query heads, which need more registers).
+    // The 4-bit cache: 64-token stages (8.5 KiB), two CTAs of four warps.
     static constexpr int RING_PER_SM = (KV8 ? 200 : 192) * 1024;
     static constexpr int DATA_BYTES = stage_data_bytes<Gm, KV8>();
-    static constexpr int MIN_CTAS = I4 ? (G_ > 8 ? 2 : 3) : DATA_BYTES <= 8192 ? 2 : 1;
+    static constexpr int MIN_CTAS = I4 ? 2 : DATA_BYTES <= 8192 ? 2 : 1;
     static constexpr int NW = MIN_CTAS == 1 ? 6 : 4;       // warps (workers) per CTA
     static constexpr int R_FIT = RING_PER_SM / (MIN_CTAS * NW * Gm::STAGE_BYTES);
-    static constexpr int R = R_FIT > 8 ? 8 : R_FIT;        // stages per warp
+    // stages per warp; the 4-bit cache's 64-token stages: three per warp (two
+    // CTAs of four warps, 210 KB of copies in flight per SM)
+    static constexpr int R = I4 ? 3 : R_FIT > 8 ? 8 : R_FIT;
     static constexpr int THREADS = NW * 32;
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
     // quantized caches: the stage's tokens are the MMA rows (decode_tok.cuh)
@@ -120,7 +120,7 @@ struct DecodeTraits {
     using Acc = std::conditional_t<TR, WarpAccT<D_, NR>, WarpAcc<D_, NR>>;
     static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad (16-byte rows)
     static constexpr int CSTRIDE = D_ + 2;                  // carry row (prefix pass): o[D], m, l
-    static constexpr int CUM_SMEM = 512;                    // sequences whose tables fit in smem
+    static constexpr int CUM_SMEM = I4 ? 256 : 512;         // sequences whose tables fit in smem
     static constexpr int QN = 16;                           // open chunks per warp (> R + 1)
     // shared memory, offsets from a 1024-byte aligned base
     static constexpr int BAR_OFF = NW * R * Gm::STAGE_BYTES;
@@ -428,7 +428,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int u = 0; u < UB; ++u)
                     if (u < nblk)
-                        bulk_load(dst + u * Gm::PIECE_PAD,
+                        bulk_load(dst + Gm::poff(u),
                                   p.kv8 + ((size_t)ids[u] * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES, fb);
             } else {
                 mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);

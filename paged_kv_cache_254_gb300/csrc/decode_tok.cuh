@@ -1,7 +1,8 @@
 // The per-stage update of the quantized caches (8-bit floats, 4-bit integers
 // with per-row scales), with the stage's tokens as the MMA rows.
 //
-// A 32-token stage is two m-tiles of 16 tokens.  Scores are S = K Q^T
+// A 32-token stage (8-bit cache) is two m-tiles of 16 tokens; a 64-token
+// stage (4-bit cache) is two such halves.  Scores are S = K Q^T
 // (m = tokens, n = the group's query heads, k = head dims), so a group of up
 // to 8 query heads fills the n = 8 of mma.sync.m16n8k16 and no MMA row is
 // spent on padding.  The output stays O^T += V^T P^T (m = dims, n = heads,
@@ -59,19 +60,22 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
 
-// Scores sc[mt][nh][e] (already in the exp2 domain, masked tokens -inf) ->
-// softmax update of acc, the weights times vw (per-token V weights of this
-// lane's rows, 0 for masked ones) as transposed fp16 B fragments pb, and the
-// rescale of acc.o.  Rows of this lane: tokens tb + 4 mt + 2 h, h = e >> 1.
-template <int D, int NH>
-__device__ __forceinline__ void softmax_rows(float (&sc)[2][NH][4], const float (&vw)[2][2],
-                                             WarpAccT<D, NH>& acc, uint32_t (&pb)[2][NH][2]) {
+// Scores sc[mt][nh][e] of MT m-tiles (already in the exp2 domain, masked
+// tokens -inf) -> softmax update of acc, the weights times vw (per-token V
+// weights of this lane's rows, 0 for masked ones) as transposed fp16 B
+// fragments pb (k-step mt), and the rescale of acc.o.  Row h of this lane in
+// m-tile mt: fragment row g + 8 h (elements e with e >> 1 == h).
+template <int D, int NH, int MT>
+__device__ __forceinline__ void softmax_rows(float (&sc)[MT][NH][4], const float (&vw)[MT][2],
+                                             WarpAccT<D, NH>& acc, uint32_t (&pb)[MT][NH][2]) {
     float alpha[NH][2];
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            float mx = fmaxf(fmaxf(sc[0][nh][c], sc[0][nh][2 + c]), fmaxf(sc[1][nh][c], sc[1][nh][2 + c]));
+            float mx = fmaxf(sc[0][nh][c], sc[0][nh][2 + c]);
+#pragma unroll
+            for (int mt = 1; mt < MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][nh][c], sc[mt][nh][2 + c]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -81,7 +85,7 @@ __device__ __forceinline__ void softmax_rows(float (&sc)[2][NH][4], const float 
             acc.l[nh][c] *= alpha[nh][c];
         }
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh) {
             float w[4];
@@ -112,40 +116,43 @@ __device__ __forceinline__ void softmax_rows(float (&sc)[2][NH][4], const float 
     }
 }
 
-// One 32-token stage of the 4-bit cache (Geom4 layout; piece u of the stage at
-// u * PIECE_PAD).  qa: Q fragments of load_q_frags8 converted to fp16 (for
-// head n-tile nh, k-step kk: b0 = qa[kk][nh], b1 = qa[kk][2 + nh]).  Tokens >=
-// valid are masked; their bytes may be stale (any nibble is a finite code) and
-// their scales anything: masked scores are set to -inf and masked V weights
-// to 0.
+// One 64-token stage of the 4-bit cache (Geom4 layout; piece u of the stage
+// at Gm::poff(u)): two halves of 32 tokens, m-tiles 2 hf and 2 hf + 1 for
+// half hf, each half ordered as tok_row.  qa: Q fragments of load_q_frags8
+// converted to fp16 (for head n-tile nh, k-step kk: b0 = qa[kk][nh],
+// b1 = qa[kk][2 + nh]).  Tokens >= valid are masked; their bytes may be
+// stale (any nibble is a finite code) and their scales anything: masked
+// scores are set to -inf and masked V weights to 0.
 template <class Gm, int NH>
 __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
                                                 WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
-    constexpr int BS = Gm::BS, PP = Gm::PIECE_PAD;
+    constexpr int BS = Gm::BS, MT = 4;
     const int g = lane >> 2;
     const int t4 = lane & 3;
-    const int tb = 8 * (g >> 1) + (g & 1);   // this lane's rows: tokens tb + 4 mt + 2 h
-    float ks[2][2], vw[2][2];
+    const int tb = 8 * (g >> 1) + (g & 1);   // rows of this lane: tokens 32 hf + tb + 4 (mt & 1) + 2 h
+    auto row_tok = [&](int mt, int h) { return 32 * (mt >> 1) + tb + 4 * (mt & 1) + 2 * h; };
+    auto tok_addr = [&](int tok) -> uint32_t { return kb + Gm::poff(tok / BS); };
+    float ks[MT][2], vw[MT][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int tok = tb + 4 * mt + 2 * h;
-            const uint32_t a = kb + (tok / BS) * PP + 4 * (tok % BS);
+            const int tok = row_tok(mt, h);
+            const uint32_t a = tok_addr(tok) + 4 * (tok % BS);
             ks[mt][h] = lds_f32(a + Gm::KS) * scale_log2;
             vw[mt][h] = lds_f32(a + Gm::VS);
         }
-    float sc[2][NH][4];
+    float sc[MT][NH][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[mt][nh][e] = 0.f;
-        const int r0 = tb + 4 * mt, r1 = r0 + 2;
+        const int r0 = row_tok(mt, 0), r1 = r0 + 2;
         uint32_t w0[4], w1[4];   // dims 32 t4 .. 32 t4 + 31 of rows g and g + 8
-        lds128(kb + (r0 / BS) * PP + (r0 % BS) * 64 + 16 * t4, w0);
-        lds128(kb + (r1 / BS) * PP + (r1 % BS) * 64 + 16 * t4, w1);
+        lds128(tok_addr(r0) + (r0 % BS) * 64 + 16 * t4, w0);
+        lds128(tok_addr(r1) + (r1 % BS) * 64 + 16 * t4, w1);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             // word i: k-step 2 i takes pairs 0, 1; k-step 2 i + 1 pairs 2, 3
@@ -160,18 +167,18 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
         }
     }
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[mt][nh][e] *= ks[mt][e >> 1];
     // only a partial stage (the last of a segment) has slots to mask
-    if (valid < 32) {
+    if (valid < Gm::TOK) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                if (tb + 4 * mt + 2 * h >= valid) {
+                if (row_tok(mt, h) >= valid) {
                     vw[mt][h] = 0.f;
 #pragma unroll
                     for (int nh = 0; nh < NH; ++nh) {
@@ -180,21 +187,31 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
                     }
                 }
     }
-    uint32_t pb[2][NH][2];
-    softmax_rows<Gm::D, NH>(sc, vw, acc, pb);
-    // V: lane t4's tokens 8 t4 .. 8 t4 + 7 are one word of each dims-first row
-    const uint32_t vrow = kb + ((8 * t4) / BS) * PP + Gm::VC + 4 * (((8 * t4) % BS) / 8);
+    uint32_t pb[MT][NH][2];
+    softmax_rows<Gm::D, NH, MT>(sc, vw, acc, pb);
+    // V: in half hf, lane t4's tokens 32 hf + 8 t4 .. + 7 are one word of each
+    // dims-first row
+    uint32_t vrow[2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int t0 = 32 * hf + 8 * t4;
+        vrow[hf] = tok_addr(t0) + Gm::VC + 4 * ((t0 % BS) / 8);
+    }
 #pragma unroll
     for (int mt = 0; mt < Gm::KD; ++mt) {
-        const uint32_t x = lds32(vrow + (16 * mt + g) * (BS / 2));
-        const uint32_t y = lds32(vrow + (16 * mt + g + 8) * (BS / 2));
-        uint32_t hx[4], hy[4];
-        i4x8_to_f16x2(x, hx);
-        i4x8_to_f16x2(y, hy);
 #pragma unroll
-        for (int nh = 0; nh < NH; ++nh) {
-            mma16816<false>(acc.o[mt][nh], hx[0], hy[0], hx[1], hy[1], pb[0][nh][0], pb[0][nh][1]);
-            mma16816<false>(acc.o[mt][nh], hx[2], hy[2], hx[3], hy[3], pb[1][nh][0], pb[1][nh][1]);
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t x = lds32(vrow[hf] + (16 * mt + g) * (BS / 2));
+            const uint32_t y = lds32(vrow[hf] + (16 * mt + g + 8) * (BS / 2));
+            uint32_t hx[4], hy[4];
+            i4x8_to_f16x2(x, hx);
+            i4x8_to_f16x2(y, hy);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+                mma16816<false>(acc.o[mt][nh], hx[0], hy[0], hx[1], hy[1], pb[2 * hf][nh][0], pb[2 * hf][nh][1]);
+                mma16816<false>(acc.o[mt][nh], hx[2], hy[2], hx[3], hy[3], pb[2 * hf + 1][nh][0],
+                                pb[2 * hf + 1][nh][1]);
+            }
         }
     }
 }
@@ -211,7 +228,7 @@ __device__ __forceinline__ uint32_t keep_pair(uint32_t x, int t, int valid) {
 template <class Gm, int NH, bool E5M2, bool MASK>
 __device__ __forceinline__ void consume_stage8t_impl(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
                                                      WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
-    constexpr int BS = Gm::BS, PP = Gm::PIECE_PAD;
+    constexpr int BS = Gm::BS;
     const int g = lane >> 2;
     const int t4 = lane & 3;
     const int tb = 8 * (g >> 1) + (g & 1);
@@ -223,8 +240,8 @@ __device__ __forceinline__ void consume_stage8t_impl(uint32_t kb, int valid, con
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[mt][nh][e] = 0.f;
         const int r0 = tb + 4 * mt, r1 = r0 + 2;
-        const uint32_t b0 = kb + (r0 / BS) * PP + (r0 % BS) * 128;
-        const uint32_t b1 = kb + (r1 / BS) * PP + (r1 % BS) * 128;
+        const uint32_t b0 = kb + Gm::poff(r0 / BS) + (r0 % BS) * 128;
+        const uint32_t b1 = kb + Gm::poff(r1 / BS) + (r1 % BS) * 128;
         uint32_t w0[8], w1[8];   // dims 32 t4 .. 32 t4 + 31 of rows g and g + 8 (permuted 16-byte parts)
         lds128(b0 + (((2 * t4) ^ (r0 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w0[0]));
         lds128(b0 + (((2 * t4 + 1) ^ (r0 & 7)) << 4), *reinterpret_cast<uint32_t(*)[4]>(&w0[4]));
@@ -254,9 +271,9 @@ __device__ __forceinline__ void consume_stage8t_impl(uint32_t kb, int valid, con
             }
         }
     uint32_t pb[2][NH][2];
-    softmax_rows<Gm::D, NH>(sc, vw, acc, pb);
+    softmax_rows<Gm::D, NH, 2>(sc, vw, acc, pb);
     // V: lane t4's tokens 8 t4 .. 8 t4 + 7 are 8 bytes of each dims-first row
-    const uint32_t vrow = kb + ((8 * t4) / BS) * PP + BS * 128 + (8 * t4) % BS;
+    const uint32_t vrow = kb + Gm::poff((8 * t4) / BS) + BS * 128 + (8 * t4) % BS;
 #pragma unroll
     for (int mt = 0; mt < Gm::KD; ++mt) {
         uint32_t x0, x1, y0, y1;
