@@ -104,14 +104,14 @@ struct DecodeTraits {
     // About 192 KiB of stages per SM (200 KiB for the quantized caches, whose
     // two-piece stages carry 64 bytes of bank padding): stages of up to 8 KiB
     // of data, two CTAs of four warps; 16 KiB stages, one CTA of six warps.
-    // The 4-bit cache: 64-token stages (8.5 KiB), two CTAs of four warps.
+    // The 4-bit cache: 64-token stages (8.6 KiB), two CTAs of four warps with
+    // three stages each (212 KB of copies in flight per SM).
     static constexpr int RING_PER_SM = (KV8 ? 200 : 192) * 1024;
     static constexpr int DATA_BYTES = stage_data_bytes<Gm, KV8>();
     static constexpr int MIN_CTAS = I4 ? 2 : DATA_BYTES <= 8192 ? 2 : 1;
     static constexpr int NW = MIN_CTAS == 1 ? 6 : 4;       // warps (workers) per CTA
     static constexpr int R_FIT = RING_PER_SM / (MIN_CTAS * NW * Gm::STAGE_BYTES);
-    // stages per warp; the 4-bit cache's 64-token stages: three per warp (two
-    // CTAs of four warps, 210 KB of copies in flight per SM)
+    // stages per warp (the 4-bit cache: see above)
     static constexpr int R = I4 ? 3 : R_FIT > 8 ? 8 : R_FIT;
     static constexpr int THREADS = NW * 32;
     static constexpr int NR = G > 8 ? 2 : 1;                // 8-row groups of query heads in use
@@ -121,7 +121,10 @@ struct DecodeTraits {
     static constexpr int PSTRIDE = D_ + 4;                  // partial row: o[D], m, l, 2 pad (16-byte rows)
     static constexpr int CSTRIDE = D_ + 2;                  // carry row (prefix pass): o[D], m, l
     static constexpr int CUM_SMEM = I4 ? 256 : 512;         // sequences whose tables fit in smem
-    static constexpr int QN = 16;                           // open chunks per warp (> R + 1)
+    static constexpr int QN = R + 2 <= 8 ? 8 : 16;          // open chunks per warp (> R + 1)
+    // smem base alignment: 1024 for the 128-byte swizzled tensor copies of the
+    // 16-bit cache, 128 for the plain bulk copies of the quantized ones
+    static constexpr int ALIGN = KV8 ? 128 : 1024;
     // shared memory, offsets from a 1024-byte aligned base
     static constexpr int BAR_OFF = NW * R * Gm::STAGE_BYTES;
     static constexpr int CUM_OFF = BAR_OFF + NW * R * 8;    // long long [CUM_SMEM + 1]
@@ -130,7 +133,7 @@ struct DecodeTraits {
     static constexpr int CQ_OFF = FST_OFF + CUM_SMEM * 4;
     static constexpr int PS_OFF = CQ_OFF + NW * QN * 32;    // poison flag per stage
     static constexpr int STALL_OFF = (PS_OFF + NW * R * 4 + 7) & ~7;   // barrier nothing completes (tests)
-    static constexpr int SMEM_BYTES = STALL_OFF + 8 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = STALL_OFF + 8 + ALIGN;  // + alignment slack
     static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group size");
     static_assert(R >= 2, "two stages per warp at least");
     static_assert(32 % UB == 0, "a batch of 32 table entries holds whole stages");
@@ -249,7 +252,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     using Gm = typename Tr::Gm;
     constexpr int D = Tr::D, BS = Tr::BS, G = Tr::G, NW = Tr::NW, R = Tr::R, UB = Tr::UB;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + (Tr::ALIGN - 1)) &
+                                               ~uintptr_t(Tr::ALIGN - 1));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;       // fragment row group
@@ -563,7 +567,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         int ctx_next = 0;
         if (nx_here) {
             ctx_next = tab.ctx[nx.s];
-            load_q(qn, nx);
+            if constexpr (!Tr::KV8) load_q(qn, nx);   // the quantized paths keep the registers
         }
         init_acc();
         int poisoned = 0;
@@ -707,10 +711,14 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (nx_here) {
             it = nx;
             ctx = ctx_next;
+            if constexpr (Tr::KV8) {
+                load_q(qa, it);
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < Gm::KD; ++kk)
+                for (int kk = 0; kk < Gm::KD; ++kk)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) qa[kk][i] = qn[kk][i];
+                    for (int i = 0; i < 4; ++i) qa[kk][i] = qn[kk][i];
+            }
         } else {
             // the chunk is done; the next one (if any) was queued by the
             // issue side, which is always ahead

@@ -127,20 +127,24 @@ template <class Gm, int NH>
 __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
                                                 WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
     constexpr int BS = Gm::BS, MT = 4;
+    constexpr int HALF = Gm::poff(32 / BS);  // offset of the second half's pieces
     const int g = lane >> 2;
     const int t4 = lane & 3;
-    const int tb = 8 * (g >> 1) + (g & 1);   // rows of this lane: tokens 32 hf + tb + 4 (mt & 1) + 2 h
-    auto row_tok = [&](int mt, int h) { return 32 * (mt >> 1) + tb + 4 * (mt & 1) + 2 * h; };
-    auto tok_addr = [&](int tok) -> uint32_t { return kb + Gm::poff(tok / BS); };
+    // This lane's rows are tokens 32 hf + tb + 4 (mt & 1) + 2 h; all of one half
+    // lie in one piece, so every address below is a per-lane base plus a
+    // compile-time offset.
+    const int tb = 8 * (g >> 1) + (g & 1);
+    const uint32_t kbase = kb + Gm::poff(tb / BS) + (tb % BS) * 64 + 16 * t4;   // K row tb
+    const uint32_t sbase = kb + Gm::poff(tb / BS) + 4 * (tb % BS) + Gm::KS;     // K scale of tb
+    const uint32_t vbase = kb + Gm::poff((8 * t4) / BS) + Gm::VC + 4 * (((8 * t4) % BS) / 8) + g * (BS / 2);
     float ks[MT][2], vw[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int tok = row_tok(mt, h);
-            const uint32_t a = tok_addr(tok) + 4 * (tok % BS);
-            ks[mt][h] = lds_f32(a + Gm::KS) * scale_log2;
-            vw[mt][h] = lds_f32(a + Gm::VS);
+            const uint32_t a = sbase + HALF * (mt >> 1) + 4 * (4 * (mt & 1) + 2 * h);
+            ks[mt][h] = lds_f32(a) * scale_log2;
+            vw[mt][h] = lds_f32(a + 4 * BS);
         }
     float sc[MT][NH][4];
 #pragma unroll
@@ -149,10 +153,9 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[mt][nh][e] = 0.f;
-        const int r0 = row_tok(mt, 0), r1 = r0 + 2;
         uint32_t w0[4], w1[4];   // dims 32 t4 .. 32 t4 + 31 of rows g and g + 8
-        lds128(tok_addr(r0) + (r0 % BS) * 64 + 16 * t4, w0);
-        lds128(tok_addr(r1) + (r1 % BS) * 64 + 16 * t4, w1);
+        lds128(kbase + HALF * (mt >> 1) + 64 * (4 * (mt & 1)), w0);
+        lds128(kbase + HALF * (mt >> 1) + 64 * (4 * (mt & 1) + 2), w1);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             // word i: k-step 2 i takes pairs 0, 1; k-step 2 i + 1 pairs 2, 3
@@ -178,7 +181,7 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                if (row_tok(mt, h) >= valid) {
+                if (32 * (mt >> 1) + tb + 4 * (mt & 1) + 2 * h >= valid) {
                     vw[mt][h] = 0.f;
 #pragma unroll
                     for (int nh = 0; nh < NH; ++nh) {
@@ -190,19 +193,13 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
     uint32_t pb[MT][NH][2];
     softmax_rows<Gm::D, NH, MT>(sc, vw, acc, pb);
     // V: in half hf, lane t4's tokens 32 hf + 8 t4 .. + 7 are one word of each
-    // dims-first row
-    uint32_t vrow[2];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        const int t0 = 32 * hf + 8 * t4;
-        vrow[hf] = tok_addr(t0) + Gm::VC + 4 * ((t0 % BS) / 8);
-    }
+    // dims-first row (rows 16 mt + g and 16 mt + g + 8)
 #pragma unroll
     for (int mt = 0; mt < Gm::KD; ++mt) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            const uint32_t x = lds32(vrow[hf] + (16 * mt + g) * (BS / 2));
-            const uint32_t y = lds32(vrow[hf] + (16 * mt + g + 8) * (BS / 2));
+            const uint32_t x = lds32(vbase + HALF * hf + 16 * mt * (BS / 2));
+            const uint32_t y = lds32(vbase + HALF * hf + (16 * mt + 8) * (BS / 2));
             uint32_t hx[4], hy[4];
             i4x8_to_f16x2(x, hx);
             i4x8_to_f16x2(y, hy);
