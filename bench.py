@@ -39,20 +39,33 @@ METRIC = "paged decode attention: effective HBM GB/s (% of GB300 peak), tokens/s
 WORKLOAD = "llama3_70b_b256"
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu DRAM traffic per decode launch (bytes read + written), keyed by a hash
-# of the decode kernel's source; a stale entry reports null.
-TRAFFIC = {
-    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one pa_decode_kernel launch
-    ("b9279b1ffad2199e", "llama3_70b_b256"): 4_861_498_112,   # 4,829,106,432 read + 32,391,680 written
-}
+# DRAM traffic of the dominant kernel per launch, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of a SMALL case: the first 64
+# sequences of the workload (inputs above L2, a few GB on the device).  The
+# line scales it to the full launch by algorithmic bytes (traffic grows in
+# proportion to the KV stream).  Keyed by a hash of the kernel sources and
+# the cache type; a stale key reports null.
+#   (hash, kv dtype): (captured dram bytes, algorithmic bytes of the captured launch)
+TRAFFIC = {}
+
+KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "decode_common.cuh", "ptx.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_254_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def scaled_traffic(khash: str, kv: str, alg_bytes: int):
+    """Captured DRAM bytes of the small case scaled to `alg_bytes`, or None."""
+    rec = TRAFFIC.get((khash, kv))
+    if rec is None:
+        return None
+    dram, alg = rec
+    return int(round(dram * alg_bytes / alg))
 
 
 def parse_args(argv=None):
@@ -568,7 +581,7 @@ def gpu_arm(args):
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = TRAFFIC.get((khash, args.config)) if args.num_seqs is None and not quant and not multi else None
+    traffic = None if (multi or use_prefix) else scaled_traffic(khash, args.kv_dtype, ubytes)
 
     if rank != 0:
         return
@@ -599,11 +612,19 @@ def gpu_arm(args):
         "pct_of_hbm_peak": round(100 * value / (world * peak), 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
+                     # achieved = the whole call (all its launches) timed with CUDA events
+                     "timed": ("pa_decode_shared_prefix call (prefix pass, pre-pass, decode, merge)" if use_prefix
+                               else "pa_decode_multi call (pre-pass, attention, merge)" if multi
+                               else "pa_decode_int4 call (pre-pass, attention, merge)" if int4
+                               else "pa_decode_fp8 call (pre-pass, attention, merge)" if fp8
+                               else "pa_decode call (pre-pass, attention, merge)"),
                      "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
                                 "pa_decode_kernel (4-bit cache)" if int4 else
                                 "pa_decode_kernel (8-bit cache)" if fp8 else
                                 ("pa_multi_tc_kernel (tcgen05)" if args.q_len * Hq // Hkv >= 33 else
                                  "pa_multi_kernel (mma.sync)") if multi else "pa_decode_kernel"),
+                     "traffic_source": ("ncu dram bytes of the attention kernel on the first 64 sequences, "
+                                        "scaled by algorithmic bytes" if traffic is not None else None),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": ubytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "kernel_hash": khash},
