@@ -502,11 +502,13 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     typename Tr::Acc acc;
     uint32_t qa[Gm::KD][4];
     load_q(qa, it);
+    float qc[Tr::NR][2];   // 4-bit cache: the code offset per head (prepare_q4)
     auto q_to_f16 = [&]() {
         if constexpr (Tr::KV8) {
             if (__any_sync(0xffffffffu, q_frags8_to_f16<D, Tr::BF16>(qa)) && lane == 0)
                 set_err(p.err, PA_DEVERR_Q_RANGE);
         }
+        if constexpr (Tr::I4) prepare_q4<Gm::KD, Tr::NR>(qa, qc, lane);
     };
     q_to_f16();
     int ctx = tab.ctx[it.s];
@@ -602,7 +604,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const uint32_t kb = ring + st * Gm::STAGE_BYTES;
             bool zeroed = false;
             if constexpr (Tr::I4) {
-                consume_stage4t<Gm, Tr::NR>(kb, valid, qa, acc, p.scale_log2, lane);
+                consume_stage4t<Gm, Tr::NR>(kb, valid, qa, qc, acc, p.scale_log2, lane);
             } else if constexpr (Tr::KV8) {
                 consume_stage8t<Gm, Tr::NR, Tr::E5M2>(kb, valid, qa, acc, p.scale_log2, lane);
             } else {
@@ -622,6 +624,7 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
 
         // ---- finish the segment: output rows, or this chunk's piece ----
+        if constexpr (Tr::I4) fix_o4<D, Tr::NR>(acc);
         if constexpr (Tr::TR) {
             // sums over the 8 lanes of a head column (rows g)
 #pragma unroll

@@ -28,10 +28,13 @@ __device__ __forceinline__ int tok_row(int mt, int j) {
 // keeps, for heads 8 nh + 2 t4 + c, the running maximum m (exp2 domain) and
 // the partial sum l over the tokens of its own rows; o is O^T (dims x heads)
 // in the accumulator layout of WarpAcc.
+// z: for the 4-bit cache, the sums over tokens of the fp16 PV weights as
+// the tensor core used them (one extra MMA tile; see consume_stage4t).
 template <int D, int NH>
 struct WarpAccT {
     float m[NH][2], l[NH][2];
     float o[D / 16][NH][4];
+    float z[NH][4];
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -41,6 +44,10 @@ struct WarpAccT {
                 m[nh][c] = -INFINITY;
                 l[nh][c] = 0.f;
             }
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) z[nh][e] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -112,20 +119,35 @@ __device__ __forceinline__ void softmax_rows(float (&sc)[MT][NH][4], const float
                 acc.o[mt][nh][2] *= alpha[nh][0];
                 acc.o[mt][nh][3] *= alpha[nh][1];
             }
+            acc.z[nh][0] *= alpha[nh][0];
+            acc.z[nh][1] *= alpha[nh][1];
         }
     }
 }
 
 // One 64-token stage of the 4-bit cache (Geom4 layout; piece u of the stage
 // at Gm::poff(u)): two halves of 32 tokens, m-tiles 2 hf and 2 hf + 1 for
-// half hf, each half ordered as tok_row.  qa: Q fragments of load_q_frags8
-// converted to fp16 (for head n-tile nh, k-step kk: b0 = qa[kk][nh],
-// b1 = qa[kk][2 + nh]).  Tokens >= valid are masked; their bytes may be
-// stale (any nibble is a finite code) and their scales anything: masked
-// scores are set to -inf and masked V weights to 0.
+// half hf, each half ordered as tok_row.
+//
+// The codes enter the tensor core as the stored nibbles n = code + 8 read as
+// fp16 subnormals (i4x8_to_sub16: one AND per pair, exact), n * 2^-24 for
+// the even pairs of a word and n * 2^-20 for the odd ones:
+//  - scores: the odd pairs' Q operand is q / 16 (prepare_q4), so the MMA gives
+//    2^-24 * sum_d q_d n_d, and s = (2^24 S - qc) * k_scale with
+//    qc = 8 * sum_d q_d (the code offset, per head; prepare_q4);
+//  - PV: the weights of the rows paired with the even V pairs enter times 16,
+//    so O' = 2^-20 * sum_t w_t n_t; one more MMA against a constant operand
+//    accumulates z = 2^-20 * sum_t w_t from the same fp16 weights, and the
+//    output is 2^20 (O' - 8 z) (fix_o4).
+// qa: Q fragments of load_q_frags8 converted to fp16 and prepared by
+// prepare_q4 (head n-tile nh, k-step kk: b0 = qa[kk][nh], b1 = qa[kk][2 + nh]).
+// Tokens >= valid are masked; their bytes may be stale (any nibble is a finite
+// code) and their scales anything: masked scores are set to -inf and masked V
+// weights to 0.
 template <class Gm, int NH>
 __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const uint32_t (&qa)[Gm::KD][4],
-                                                WarpAccT<Gm::D, NH>& acc, float scale_log2, int lane) {
+                                                const float (&qc)[NH][2], WarpAccT<Gm::D, NH>& acc,
+                                                float scale_log2, int lane) {
     constexpr int BS = Gm::BS, MT = 4;
     constexpr int HALF = Gm::poff(32 / BS);  // offset of the second half's pieces
     const int g = lane >> 2;
@@ -160,8 +182,8 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
         for (int i = 0; i < 4; ++i) {
             // word i: k-step 2 i takes pairs 0, 1; k-step 2 i + 1 pairs 2, 3
             uint32_t h0[4], h1[4];
-            i4x8_to_f16x2(w0[i], h0);
-            i4x8_to_f16x2(w1[i], h1);
+            i4x8_to_sub16(w0[i], h0);
+            i4x8_to_sub16(w1[i], h1);
 #pragma unroll
             for (int nh = 0; nh < NH; ++nh) {
                 mma16816<false>(sc[mt][nh], h0[0], h1[0], h0[1], h1[1], qa[2 * i][nh], qa[2 * i][2 + nh]);
@@ -174,7 +196,7 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[mt][nh][e] *= ks[mt][e >> 1];
+            for (int e = 0; e < 4; ++e) sc[mt][nh][e] = fmaf(sc[mt][nh][e], 16777216.f, -qc[nh][e & 1]) * ks[mt][e >> 1];
     // only a partial stage (the last of a segment) has slots to mask
     if (valid < Gm::TOK) {
 #pragma unroll
@@ -190,6 +212,10 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
                     }
                 }
     }
+    // rows g of each m-tile pair with the even V pairs (2^-24): their
+    // weights enter times 16
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) vw[mt][0] *= 16.f;
     uint32_t pb[MT][NH][2];
     softmax_rows<Gm::D, NH, MT>(sc, vw, acc, pb);
     // V: in half hf, lane t4's tokens 32 hf + 8 t4 .. + 7 are one word of each
@@ -201,8 +227,8 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
             const uint32_t x = lds32(vbase + HALF * hf + 16 * mt * (BS / 2));
             const uint32_t y = lds32(vbase + HALF * hf + (16 * mt + 8) * (BS / 2));
             uint32_t hx[4], hy[4];
-            i4x8_to_f16x2(x, hx);
-            i4x8_to_f16x2(y, hy);
+            i4x8_to_sub16(x, hx);
+            i4x8_to_sub16(y, hy);
 #pragma unroll
             for (int nh = 0; nh < NH; ++nh) {
                 mma16816<false>(acc.o[mt][nh], hx[0], hy[0], hx[1], hy[1], pb[2 * hf][nh][0], pb[2 * hf][nh][1]);
@@ -211,6 +237,49 @@ __device__ __forceinline__ void consume_stage4t(uint32_t kb, int valid, const ui
             }
         }
     }
+    // z += the weights against a constant A operand: 2^-24 (even pairs) and
+    // 2^-20 (odd pairs), as fp16 subnormals
+    constexpr uint32_t ONE_EVEN = 0x00010001u, ONE_ODD = 0x00100010u;
+#pragma unroll
+    for (int k = 0; k < MT; ++k)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+            mma16816<false>(acc.z[nh], ONE_EVEN, ONE_EVEN, ONE_ODD, ONE_ODD, pb[k][nh][0], pb[k][nh][1]);
+}
+
+// Q operand of consume_stage4t for a new segment: the odd pairs' q / 16
+// (exact unless the result is subnormal), and qc[nh][c] = 8 * sum_d q_d over
+// the head 8 nh + 2 t4 + c, from the same fp16 values.
+template <int KD, int NH>
+__device__ __forceinline__ void prepare_q4(uint32_t (&qa)[KD][4], float (&qc)[NH][2], int lane) {
+    const int t4 = lane & 3;
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+        float s = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KD; ++kk) {
+            uint32_t h;
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(qa[kk][2 + nh]), "r"(0x2c002c00u));
+            qa[kk][2 + nh] = h;
+            s += lo_of<false>(qa[kk][nh]) + hi_of<false>(qa[kk][nh]) + 16.f * (lo_of<false>(h) + hi_of<false>(h));
+        }
+        // this lane holds 32 dims of head 8 nh + g; the 4 lanes of a row group all of them
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) qc[nh][c] = 8.f * __shfl_sync(0xffffffffu, s, (2 * t4 + c) * 4);
+    }
+}
+
+// The output accumulator of consume_stage4t in true scale: 2^20 (O' - 8 z).
+template <int D, int NH>
+__device__ __forceinline__ void fix_o4(WarpAccT<D, NH>& acc) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc.o[mt][nh][e] = 1048576.f * fmaf(-8.f, acc.z[nh][e & 1], acc.o[mt][nh][e]);
 }
 
 // Keep the 16-bit halves of x whose token is below valid (pair tokens t, t + 1).

@@ -243,6 +243,19 @@ __device__ __forceinline__ void i4x8_to_f16x2(uint32_t x, uint32_t (&h)[4]) {
     h[3] = i4_pair_hi(y);
 }
 
+// The eight nibbles n of one word as fp16 subnormals, exactly: a nibble at
+// bits 0..3 of a 16-bit half reads as n * 2^-24, one at bits 4..7 as
+// n * 2^-20 (one AND each, no arithmetic).  Pair 0: nibbles 0, 4 (2^-24);
+// pair 1: nibbles 1, 5 (2^-20); pair 2: nibbles 2, 6 (2^-24); pair 3:
+// nibbles 3, 7 (2^-20).
+__device__ __forceinline__ void i4x8_to_sub16(uint32_t x, uint32_t (&h)[4]) {
+    const uint32_t y = x >> 8;
+    h[0] = x & 0x000f000fu;
+    h[1] = x & 0x00f000f0u;
+    h[2] = y & 0x000f000fu;
+    h[3] = y & 0x00f000f0u;
+}
+
 // Two floats -> two 8-bit float codes (low byte = first), round to nearest
 // even, finite values beyond the format's range saturate.
 template <bool E5M2>
