@@ -436,12 +436,17 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                                   p.kv8 + ((size_t)ids[u] * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES, fb);
             } else {
                 mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-                const int y = (ids[0] * p.Hkv + is.kvh) * BS;
-#pragma unroll
-                for (int h = 0; h < Gm::HALVES; ++h) {
-                    tma_load_2d(dst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                    tma_load_2d(dst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-                }
+            }
+        }
+        if constexpr (!Tr::KV8) {
+            // the K and V boxes, one per lane (each TMA instruction holds its
+            // issuing thread for a while; lanes issue them side by side)
+            __syncwarp();
+            if (!aborted && lane < 2 * Gm::HALVES) {
+                const int id = (unsigned)ids[0] < (unsigned)p.NB ? ids[0] : 0;   // a bad id is flagged above
+                const int h = lane >> 1, v = lane & 1;
+                tma_load_2d(ring + st * Gm::STAGE_BYTES + (v ? Gm::CHUNK_BYTES : 0) + h * Gm::BOX_BYTES,
+                            v ? &tmap_v : &tmap_k, h * 64, (id * p.Hkv + is.kvh) * BS, full0 + 8 * st);
             }
         }
         ++nis;

@@ -284,22 +284,25 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                            (k == nst - 2 ? TC_PENULT : 0);
                                 rc.poison = poison;
                                 rc.seg = nseg;
-                                const uint32_t dst = ring + st * Tr::STAGE_BYTES;
                                 mbar_arrive_expect_tx(full(st), (uint32_t)(nbs * BS * 128 * HALVES * 2));
-#pragma unroll
-                                for (int i = 0; i < SB; ++i) {
-                                    if (i >= nbs) break;
-                                    const int y = (idv[i] * p.Hkv + it.kvh) * BS;
-#pragma unroll
-                                    for (int h = 0; h < HALVES; ++h) {
-                                        const uint32_t off = h * Tr::HALF_BYTES + i * BS * 128;
-                                        tma_load_2d(dst + off, &tmap_k, h * 64, y, full(st));
-                                        tma_load_2d(dst + Tr::KV_BYTES + off, &tmap_v, h * 64, y, full(st));
-                                    }
-                                }
                             }
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
+                        __syncwarp();   // lane 0's claim of the slot orders the other lanes' copies
+                        // the stage's copies, one per lane (each TMA instruction holds its
+                        // issuing thread for a while; lanes issue them side by side):
+                        // lane = (block i, column half h, K or V)
+                        {
+                            constexpr int NCOPY = SB * HALVES * 2;
+                            const int ci = lane / (HALVES * 2), ch = (lane >> 1) % HALVES, cv = lane & 1;
+                            int cid = __shfl_sync(0xffffffffu, ids, (bb + ci) & 31);
+                            if ((unsigned)cid >= (unsigned)p.NB) cid = 0;   // flagged and poisoned above
+                            if (ok && lane < NCOPY && ci < nbs) {
+                                const uint32_t dst = ring + st * Tr::STAGE_BYTES + (cv ? Tr::KV_BYTES : 0) +
+                                                     ch * Tr::HALF_BYTES + ci * BS * 128;
+                                tma_load_2d(dst, cv ? &tmap_v : &tmap_k, ch * 64, (cid * p.Hkv + it.kvh) * BS, full(st));
+                            }
+                        }
                         ++j;
                         if (++st == R) {
                             st = 0;
@@ -337,29 +340,25 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         __syncwarp();
     } else if (warp == Tr::MMA_WARP) {
         // ================================================================ MMA
-        // Issue order S_0, S_1, then (S_{j+2}, PV_j) for j = 0, 1, ...: the
-        // scores run two stages ahead of the PV products, so the softmax of one
-        // stage never waits for its scores; PVs go in stage order (O accumulates
-        // in order).  Every wait blocks in the barrier (bounded).  Deadlock-free:
-        // S_{j+2} needs only the copy of stage j + 2 (its slot was freed by
-        // PV_{j+2-R}, R >= 3), the scores of stage j read (s_free) and at a
-        // segment start the Q tile; PV_j needs P_j and, at a segment start, the
-        // previous segment's output read, all issued or produced before it.
+        // One thread issues the scores S_j and the products PV_j, each as soon
+        // as its inputs are ready (non-blocking tests of the barriers): S_j
+        // needs the copy of stage j, the scores of stage j - 2 read out of its
+        // TMEM buffer (s_free) and, at a segment start, the Q tile; PV_j needs
+        // P_j written and, at a segment start, the previous segment's output
+        // read.  PVs go in stage order (O accumulates in order) and S runs at
+        // most 4 stages ahead (the slot records kept per stage in flight).  A
+        // PV is never held behind the copy of a later stage, so ring slots are
+        // released as early as the products allow.  Deadlock-free: every
+        // condition is produced by work issued earlier or by other warps that
+        // only wait on earlier stages.  No progress for the wait limit: abort.
         if (lane == 0) {
             int js = 0, jp = 0, nseg = 0, pv_seg = 0;    // next S, next PV, Q tiles consumed, segments begun
             int s_st = 0;                                // ring slot and phase of stage js
             uint32_t s_ph = 0;
             uint32_t meta = 0;                           // per stage in flight (js % 4): slot | first << 7
             bool end_seen = false, ok = true;
-            // 0: the end record, 1: issued, -1: a wait timed out
-            auto issue_s = [&]() -> int {
-                if (!mbar_wait_bounded(full(s_st), s_ph, p.timeout_ns)) return -1;
-                const int flags = recs[s_st].flags;
-                if (flags & TC_END) return 0;
-                if ((flags & TC_FIRST) && !mbar_wait_bounded(q_full, (uint32_t)(nseg & 1), p.timeout_ns)) return -1;
+            auto issue_s = [&](int flags) {
                 const int b = js & 1;
-                if (js >= 2 && !mbar_wait_bounded(s_free + 8 * b, (uint32_t)(((js - 2) >> 1) & 1), p.timeout_ns))
-                    return -1;
                 if (flags & TC_FIRST) ++nseg;
                 tc_fence_after();
                 const uint64_t qd = sdesc_sw128(q_tile, 16, 1024);
@@ -378,17 +377,8 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     s_st = 0;
                     s_ph ^= 1u;
                 }
-                return 1;
             };
-            auto issue_pv = [&]() -> bool {
-                const uint32_t m8 = (meta >> (8u * (uint32_t)(jp & 3))) & 0xffu;
-                const int st = (int)(m8 & 0x7fu);
-                const bool first = (m8 & 0x80u) != 0;
-                const int b = jp & 1;
-                if (!mbar_wait_bounded(p_full + 8 * b, (uint32_t)((jp >> 1) & 1), p.timeout_ns)) return false;
-                // a segment's first PV overwrites O: the previous segment's output must have been read
-                if (first && pv_seg > 0 && !mbar_wait_bounded(o_free, (uint32_t)((pv_seg - 1) & 1), p.timeout_ns))
-                    return false;
+            auto issue_pv = [&](int st, bool first, int b) {
                 if (first) ++pv_seg;
                 tc_fence_after();
                 const uint32_t pt = tmem + Tr::P_COL + 64 * b;
@@ -402,27 +392,40 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 mma_commit(pv_done + 8 * b);
                 mma_commit(empty(st));
                 ++jp;
-                return true;
             };
-            for (int i = 0; i < 2 && ok && !end_seen; ++i) {
-                const int r = issue_s();
-                if (r < 0) ok = false;
-                if (r == 0) end_seen = true;
-            }
-            while (ok && jp < js) {
-                if (*abort_flag) {
-                    ok = false;
-                    break;
+            uint64_t t_last = global_timer_ns();
+            for (uint32_t spin = 0;; ++spin) {
+                bool progress = false;
+                if (jp < js) {
+                    const uint32_t m8 = (meta >> (8u * (uint32_t)(jp & 3))) & 0xffu;
+                    const int b = jp & 1;
+                    const bool first = (m8 & 0x80u) != 0;
+                    if (mbar_test_wait(p_full + 8 * b, (uint32_t)((jp >> 1) & 1)) &&
+                        (!first || pv_seg == 0 || mbar_test_wait(o_free, (uint32_t)((pv_seg - 1) & 1)))) {
+                        issue_pv((int)(m8 & 0x7fu), first, b);
+                        progress = true;
+                    }
                 }
-                if (!end_seen) {
-                    const int r = issue_s();
-                    if (r < 0) {
+                if (!end_seen && js < jp + 4 && mbar_test_wait(full(s_st), s_ph)) {
+                    const int flags = recs[s_st].flags;
+                    if (flags & TC_END) {
+                        end_seen = true;
+                        progress = true;
+                    } else if ((!(flags & TC_FIRST) || mbar_test_wait(q_full, (uint32_t)(nseg & 1))) &&
+                               (js < 2 || mbar_test_wait(s_free + 8 * (js & 1), (uint32_t)(((js - 2) >> 1) & 1)))) {
+                        issue_s(flags);
+                        progress = true;
+                    }
+                }
+                if (end_seen && jp == js) break;
+                if (progress) {
+                    t_last = global_timer_ns();
+                } else if ((spin & 63u) == 0) {
+                    if (*abort_flag || global_timer_ns() - t_last > p.timeout_ns) {
                         ok = false;
                         break;
                     }
-                    if (r == 0) end_seen = true;
                 }
-                if (!issue_pv()) ok = false;
             }
             if (!ok) {
                 set_err(p.err, PA_DEVERR_TIMEOUT);
