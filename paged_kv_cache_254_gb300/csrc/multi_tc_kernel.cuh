@@ -18,7 +18,7 @@
 // as a hi + lo pair of 16-bit values (two MMAs), keeping ~16 bits of each
 // weight as the mma.sync kernels do.
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (352 threads, one CTA per SM):
 //   warps 0-7  softmax: warp w handles rows 32 (w % 4) .. + 31 (its TMEM lane
 //              quarter; thread = query row) and keys 32 (w / 4) .. + 31 of
 //              each stage; the two warps of a row quarter exchange their
@@ -30,8 +30,9 @@
 //   warp 8     copies: per segment the Q tile (one 3-D TMA per 64-column
 //              half: box = g heads x max_q tokens, landing as rows i * g + hh),
 //              per stage the K and V boxes of its blocks (2-D TMA).
-//   warp 9     MMA: allocates TMEM; issues S of stage j + 1 before PV of
-//              stage j so the softmax of one stage overlaps the tensor core.
+//   warp 9     scores: allocates TMEM; issues S of each stage as soon as its
+//              copy has landed and its TMEM buffer is free.
+//   warp 10    PV: issues the PV product of each stage once its P is written.
 //
 // Lazy rescaling.  A row keeps the reference maximum m_ref used for its
 // weights; only when a stage raises the row maximum above m_ref + 8 (log2
@@ -79,8 +80,8 @@ struct TcTraits {
     static constexpr int MISC_OFF = XCH_OFF + XCH_BYTES;      // TMEM base, abort flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;   // + alignment slack
     static constexpr int SOFT_WARPS = 8;
-    static constexpr int THREADS = 32 * (SOFT_WARPS + 2);
-    static constexpr int COPY_WARP = SOFT_WARPS, MMA_WARP = SOFT_WARPS + 1;
+    static constexpr int THREADS = 32 * (SOFT_WARPS + 3);
+    static constexpr int COPY_WARP = SOFT_WARPS, MMA_WARP = SOFT_WARPS + 1, PV_WARP = SOFT_WARPS + 2;
     static constexpr int TMEM_COLS = 512;
     static constexpr int O_COL = 128;                        // S buffers at columns 0 and 64
     static constexpr int P_COL = 256;                        // P buffer b at P_COL + 64 b: hi, then lo
@@ -151,6 +152,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     volatile unsigned long long* xch = reinterpret_cast<volatile unsigned long long*>(smem + Tr::XCH_OFF);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Tr::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::MISC_OFF + 4);
+    volatile int* n_stages = reinterpret_cast<volatile int*>(smem + Tr::MISC_OFF + 8);   // set at the end record
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < R; ++st) {
@@ -165,9 +167,10 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        mbar_init(fin, 1);
+        mbar_init(fin, 2);                      // the score thread and the PV thread
         mbar_init(o_free, SW / 2);              // a segment's output read: the four warps of its last stage
         *abort_flag = 0;
+        *n_stages = 0x7fffffff;
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < Tr::XCH_BYTES / 8; i += Tr::THREADS) xch[i] = 0ull;   // tag 0: nothing yet
@@ -339,46 +342,96 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         }
         __syncwarp();
     } else if (warp == Tr::MMA_WARP) {
-        // ================================================================ MMA
-        // One thread issues the scores S_j and the products PV_j, each as soon
-        // as its inputs are ready (non-blocking tests of the barriers): S_j
-        // needs the copy of stage j, the scores of stage j - 2 read out of its
-        // TMEM buffer (s_free) and, at a segment start, the Q tile; PV_j needs
-        // P_j written and, at a segment start, the previous segment's output
-        // read.  PVs go in stage order (O accumulates in order) and S runs at
-        // most 4 stages ahead (the slot records kept per stage in flight).  A
-        // PV is never held behind the copy of a later stage, so ring slots are
-        // released as early as the products allow.  Deadlock-free: every
-        // condition is produced by work issued earlier or by other warps that
-        // only wait on earlier stages.  No progress for the wait limit: abort.
+        // ================================================================ scores
+        // One thread issues S_j as soon as its inputs are ready: the copy of
+        // stage j, the scores of stage j - 2 read out of its TMEM buffer
+        // (s_free) and, at a segment start, the Q tile.  The PV products are
+        // issued by another thread (PV_WARP), so neither kind of MMA waits
+        // behind the other's inputs.  At the end record it publishes the
+        // number of stages.  No progress for the wait limit: abort.
         if (lane == 0) {
-            int js = 0, jp = 0, nseg = 0, pv_seg = 0;    // next S, next PV, Q tiles consumed, segments begun
+            int js = 0, nseg = 0;                        // next S, Q tiles consumed
             int s_st = 0;                                // ring slot and phase of stage js
             uint32_t s_ph = 0;
-            uint32_t meta = 0;                           // per stage in flight (js % 4): slot | first << 7
-            bool end_seen = false, ok = true;
-            auto issue_s = [&](int flags) {
-                const int b = js & 1;
-                if (flags & TC_FIRST) ++nseg;
-                tc_fence_after();
-                const uint64_t qd = sdesc_sw128(q_tile, 16, 1024);
-                const uint64_t kd = sdesc_sw128(ring + s_st * Tr::STAGE_BYTES, 16, 1024);
+            bool ok = true;
+            uint64_t t_last = global_timer_ns();
+            for (uint32_t spin = 0;; ++spin) {
+                if (mbar_test_wait(full(s_st), s_ph)) {
+                    const int flags = recs[s_st].flags;
+                    if (flags & TC_END) {
+                        *n_stages = js;
+                        break;
+                    }
+                    if ((!(flags & TC_FIRST) || mbar_test_wait(q_full, (uint32_t)(nseg & 1))) &&
+                        (js < 2 || mbar_test_wait(s_free + 8 * (js & 1), (uint32_t)(((js - 2) >> 1) & 1)))) {
+                        const int b = js & 1;
+                        if (flags & TC_FIRST) ++nseg;
+                        tc_fence_after();
+                        const uint64_t qd = sdesc_sw128(q_tile, 16, 1024);
+                        const uint64_t kd = sdesc_sw128(ring + s_st * Tr::STAGE_BYTES, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step, +a half tile per 4 (address >> 4)
-                    mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (Tr::Q_HALF >> 4) + (k % 4) * 2),
-                            kd + (uint64_t)((k / 4) * (Tr::HALF_BYTES >> 4) + (k % 4) * 2), IDESC_S, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step, +a half tile per 4 (address >> 4)
+                            mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (Tr::Q_HALF >> 4) + (k % 4) * 2),
+                                    kd + (uint64_t)((k / 4) * (Tr::HALF_BYTES >> 4) + (k % 4) * 2), IDESC_S,
+                                    k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(s_full + 8 * b);
+                        if (flags & TC_LAST) mma_commit(q_empty);
+                        ++js;
+                        if (++s_st == R) {
+                            s_st = 0;
+                            s_ph ^= 1u;
+                        }
+                        t_last = global_timer_ns();
+                        continue;
+                    }
                 }
-                mma_commit(s_full + 8 * b);
-                if (flags & TC_LAST) mma_commit(q_empty);
-                const uint32_t sh = 8u * (uint32_t)(js & 3);
-                meta = (meta & ~(0xffu << sh)) | ((uint32_t)s_st | ((flags & TC_FIRST) ? 0x80u : 0u)) << sh;
-                ++js;
-                if (++s_st == R) {
-                    s_st = 0;
-                    s_ph ^= 1u;
+                if ((spin & 63u) == 0 && (*abort_flag || global_timer_ns() - t_last > p.timeout_ns)) {
+                    ok = false;
+                    break;
                 }
-            };
-            auto issue_pv = [&](int st, bool first, int b) {
+            }
+            if (!ok) {
+                set_err(p.err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA issued (by both threads) completes before tensor memory is released
+            mma_commit(fin);
+            mbar_wait_bounded(fin, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == Tr::PV_WARP) {
+        // ================================================================ PV
+        // One thread issues PV_j in stage order once P_j is written and, at a
+        // segment start, the previous segment's output has been read; the
+        // commit frees the stage's ring slot.  It stops at the number of
+        // stages the score thread publishes.
+        if (lane == 0) {
+            int jp = 0, pv_seg = 0;
+            bool ok = true;
+            while (true) {
+                const int b = jp & 1;
+                bool ready = false;
+                const uint64_t t0 = global_timer_ns();
+                for (uint32_t spin = 0;; ++spin) {
+                    if (jp >= *n_stages) break;
+                    if (mbar_test_wait(p_full + 8 * b, (uint32_t)((jp >> 1) & 1))) {
+                        ready = true;
+                        break;
+                    }
+                    if ((spin & 63u) == 0 && (*abort_flag || global_timer_ns() - t0 > p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ready) break;
+                const int st = jp % R;
+                const bool first = (recs[st].flags & TC_FIRST) != 0;
+                // a segment's first PV overwrites O: the previous segment's output must have been read
+                if (first && pv_seg > 0 && !mbar_wait_bounded(o_free, (uint32_t)((pv_seg - 1) & 1), p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
                 if (first) ++pv_seg;
                 tc_fence_after();
                 const uint32_t pt = tmem + Tr::P_COL + 64 * b;
@@ -392,48 +445,12 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 mma_commit(pv_done + 8 * b);
                 mma_commit(empty(st));
                 ++jp;
-            };
-            uint64_t t_last = global_timer_ns();
-            for (uint32_t spin = 0;; ++spin) {
-                bool progress = false;
-                if (jp < js) {
-                    const uint32_t m8 = (meta >> (8u * (uint32_t)(jp & 3))) & 0xffu;
-                    const int b = jp & 1;
-                    const bool first = (m8 & 0x80u) != 0;
-                    if (mbar_test_wait(p_full + 8 * b, (uint32_t)((jp >> 1) & 1)) &&
-                        (!first || pv_seg == 0 || mbar_test_wait(o_free, (uint32_t)((pv_seg - 1) & 1)))) {
-                        issue_pv((int)(m8 & 0x7fu), first, b);
-                        progress = true;
-                    }
-                }
-                if (!end_seen && js < jp + 4 && mbar_test_wait(full(s_st), s_ph)) {
-                    const int flags = recs[s_st].flags;
-                    if (flags & TC_END) {
-                        end_seen = true;
-                        progress = true;
-                    } else if ((!(flags & TC_FIRST) || mbar_test_wait(q_full, (uint32_t)(nseg & 1))) &&
-                               (js < 2 || mbar_test_wait(s_free + 8 * (js & 1), (uint32_t)(((js - 2) >> 1) & 1)))) {
-                        issue_s(flags);
-                        progress = true;
-                    }
-                }
-                if (end_seen && jp == js) break;
-                if (progress) {
-                    t_last = global_timer_ns();
-                } else if ((spin & 63u) == 0) {
-                    if (*abort_flag || global_timer_ns() - t_last > p.timeout_ns) {
-                        ok = false;
-                        break;
-                    }
-                }
             }
             if (!ok) {
                 set_err(p.err, PA_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            // every MMA issued completes before tensor memory is released
             mma_commit(fin);
-            mbar_wait_bounded(fin, 0, p.timeout_ns);
         }
         __syncwarp();
     } else {
