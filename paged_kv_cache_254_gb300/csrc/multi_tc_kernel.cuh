@@ -11,7 +11,8 @@
 // in stages of 64 (64 / B blocks of one pair).
 //
 //   S  = Q K^T   M 128, N 64, K = head_dim   (Q, K: K-major swizzled tiles)
-//   O += P V     M 128, N = head_dim, K 64   (P: K-major; V: MN-major tile)
+//   O += P V     M 128, N = head_dim, K 64   (P: K-major; V: MN-major tiles,
+//                                             one per block)
 //
 // with S (two 64-column fp32 buffers), P (two buffers of 16-bit weights, the
 // A operand of the PV product) and O (fp32) all in tensor memory.  P enters
@@ -64,6 +65,12 @@ struct TcTraits {
     static constexpr int Q_BYTES = HALVES * Q_HALF;
     static constexpr int HALF_BYTES = KEYS * 128;            // one column half of a stage's K or V
     static constexpr int KV_BYTES = HALVES * HALF_BYTES;
+    // V of a stage as one tile per block, [column half][BS rows][128 B] (what
+    // one 3-D TMA box of the whole (block, KV head) chunk writes); K keeps
+    // [column half][64 keys][128 B] (two boxes per block), so the score MMA
+    // spans the stage's 64 keys with one row-group stride
+    static constexpr int HALF_STRIDE = BS * 128;             // between the column halves of a V block tile
+    static constexpr int BLK_BYTES = HALVES * HALF_STRIDE;   // one block's V tile
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;         // K, then V
     static constexpr int RING_OFF = Q_BYTES;
     static constexpr int SMEM_CAP = 227 * 1024;
@@ -292,18 +299,24 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         __syncwarp();   // lane 0's claim of the slot orders the other lanes' copies
-                        // the stage's copies, one per lane (each TMA instruction holds its
-                        // issuing thread for a while; lanes issue them side by side):
-                        // lane = (block i, column half h, K or V)
+                        // the stage's copies, one box per lane (the TMA unit takes boxes
+                        // one at a time: V goes as one box per block)
                         {
-                            constexpr int NCOPY = SB * HALVES * 2;
-                            const int ci = lane / (HALVES * 2), ch = (lane >> 1) % HALVES, cv = lane & 1;
-                            int cid = __shfl_sync(0xffffffffu, ids, (bb + ci) & 31);
+                            // lanes 0 .. SB * HALVES - 1: K boxes (block i, column half h);
+                            // the next SB lanes: one V box per block (all halves)
+                            constexpr int NK = SB * HALVES;
+                            const bool kl = lane < NK;
+                            const int ci = kl ? lane / HALVES : lane - NK, ch = lane % HALVES;
+                            int cid = __shfl_sync(0xffffffffu, ids, (bb + (ci & (SB - 1))) & 31);
                             if ((unsigned)cid >= (unsigned)p.NB) cid = 0;   // flagged and poisoned above
-                            if (ok && lane < NCOPY && ci < nbs) {
-                                const uint32_t dst = ring + st * Tr::STAGE_BYTES + (cv ? Tr::KV_BYTES : 0) +
-                                                     ch * Tr::HALF_BYTES + ci * BS * 128;
-                                tma_load_2d(dst, cv ? &tmap_v : &tmap_k, ch * 64, (cid * p.Hkv + it.kvh) * BS, full(st));
+                            const int y = (cid * p.Hkv + it.kvh) * BS;
+                            if (ok && lane < NK + SB && ci < nbs) {
+                                if (kl)
+                                    tma_load_2d(ring + st * Tr::STAGE_BYTES + ch * Tr::HALF_BYTES + ci * BS * 128, &tmap_k,
+                                                ch * 64, y, full(st));
+                                else
+                                    tma_load_3d(ring + st * Tr::STAGE_BYTES + Tr::KV_BYTES + ci * Tr::BLK_BYTES, &tmap_v, 0,
+                                                y, 0, full(st));
                             }
                         }
                         ++j;
@@ -435,10 +448,12 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (first) ++pv_seg;
                 tc_fence_after();
                 const uint32_t pt = tmem + Tr::P_COL + 64 * b;
-                const uint64_t vd = sdesc_sw128(ring + st * Tr::STAGE_BYTES + Tr::KV_BYTES, Tr::HALF_BYTES, 1024);
+                const uint32_t vbase = ring + st * Tr::STAGE_BYTES + Tr::KV_BYTES;
 #pragma unroll
                 for (int k = 0; k < KEYS / 16; ++k) {
-                    const uint64_t bv = vd + (uint64_t)(k * ((16 * 128) >> 4));
+                    // keys 16 k .. 16 k + 15: rows (16 k) % BS .. of block tile (16 k) / BS
+                    const uint64_t bv = sdesc_sw128(vbase + ((16 * k) / BS) * Tr::BLK_BYTES + ((16 * k) % BS) * 128,
+                                                    Tr::HALF_STRIDE, 1024);
                     mma_f16_ts(tmem + Tr::O_COL, pt + 8 * k, bv, IDESC_O, (first && k == 0) ? 0u : 1u);
                     mma_f16_ts(tmem + Tr::O_COL, pt + 32 + 8 * k, bv, IDESC_O, 1u);
                 }
@@ -624,9 +639,9 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 uint8_t* vt = smem + Tr::RING_OFF + st * Tr::STAGE_BYTES + Tr::KV_BYTES;
                 const int nz = (KEYS - vvalid) * HALVES * 8;
                 for (int i = stid; i < nz; i += 128) {
-                    const int row = vvalid + i / (HALVES * 8), part = i % (HALVES * 8);
-                    *reinterpret_cast<uint4*>(vt + (part / 8) * Tr::HALF_BYTES + row * 128 + (part % 8) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                    const int key = vvalid + i / (HALVES * 8), part = i % (HALVES * 8);
+                    *reinterpret_cast<uint4*>(vt + (key / BS) * Tr::BLK_BYTES + (part / 8) * Tr::HALF_STRIDE +
+                                              (key % BS) * 128 + (part % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }

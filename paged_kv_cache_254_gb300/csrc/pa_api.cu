@@ -240,6 +240,26 @@ bool pool_map(CUtensorMap* m, const void* pool, const pa_shape* s) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The pool as a 3-D tensor (column within a 64-column half, row = (block,
+// kv head, slot), half): one box of 64 columns x block_size rows x all halves
+// lands as the halves' 128-byte swizzled [rows][128 B] tiles one after the
+// other -- a whole (block, kv head) chunk in one copy.  The half stride
+// (128 bytes) is below the row stride; both views cover the same bytes.
+bool pool_map_chunk(CUtensorMap* m, const void* pool, const pa_shape* s) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int halves = s->head_dim / 64;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)s->num_blocks * s->num_kv_heads * s->block_size, (cuuint64_t)halves};
+    const cuuint64_t strides[2] = {(cuuint64_t)s->head_dim * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)s->block_size, (cuuint32_t)halves};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q [T][Hq][D] as a 3-D tensor (head_dim, heads, tokens): boxes of 64
 // columns x g heads x q_box tokens land as rows i * g + hh, 128-byte swizzled.
 bool q_map(CUtensorMap* m, const void* q, const pa_shape* s, int total_q, int q_box) {
@@ -784,7 +804,10 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < multi_region_bytes(shape, ctas, k->rows))
         return PA_ERR_WORKSPACE;
     CUtensorMap mk, mv, mq;
-    if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+    // the tcgen05 kernel copies V as whole (block, kv head) chunks
+    if (!pool_map(&mk, k_pool, shape) ||
+        !(tc ? pool_map_chunk(&mv, v_pool, shape) : pool_map(&mv, v_pool, shape)))
+        return PA_ERR_CUDA;
     const int q_box = std::min(max_q_len, total_q);
     if (tc && !q_map(&mq, q, shape, total_q, q_box)) return PA_ERR_CUDA;
 
