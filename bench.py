@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # the cache type; a stale key reports null.
 #   (hash, kv dtype): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("40d030185515212d", "bf16"): (1_218_299_136 + 20_797_184, 1_216_111_324),
-    ("40d030185515212d", "fp8_e4m3"): (610_190_336 + 14_897_152, 609_141_468),
-    ("40d030185515212d", "int4"): (324_754_688 + 7_011_584, 324_624_348),
+    ("c62c98d725465c97", "bf16"): (1_218_195_712 + 21_107_968, 1_216_111_324),
+    ("c62c98d725465c97", "fp8_e4m3"): (610_135_296 + 14_837_504, 609_141_468),
+    ("c62c98d725465c97", "int4"): (324_677_632 + 6_619_136, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")

@@ -63,14 +63,17 @@ struct TcTraits {
     static constexpr int HALVES = D / 64;                    // 128-byte column halves of a row
     static constexpr int Q_HALF = ROWS * 128;
     static constexpr int Q_BYTES = HALVES * Q_HALF;
-    static constexpr int HALF_BYTES = KEYS * 128;            // one column half of a stage's K or V
-    static constexpr int KV_BYTES = HALVES * HALF_BYTES;
-    // V of a stage as one tile per block, [column half][BS rows][128 B] (what
-    // one 3-D TMA box of the whole (block, KV head) chunk writes); K keeps
-    // [column half][64 keys][128 B] (two boxes per block), so the score MMA
-    // spans the stage's 64 keys with one row-group stride
+    static constexpr int KV_BYTES = KEYS * D * 2;            // a stage's K, or its V
+    // Each block of a stage arrives as one TMA box per operand.
+    //  * K: [8-row group][column half][8 rows][128 B] (a 4-D box), so the
+    //    8-row groups of one half follow each other HALVES x 1024 bytes apart
+    //    across the stage's blocks and the score MMA spans all 64 keys with
+    //    one descriptor (that fixed group stride);
+    //  * V: [column half][BS rows][128 B] (a 3-D box), an MN-major tile per
+    //    block for the PV product.
+    static constexpr int GROUP_STRIDE = HALVES * 1024;       // between 8-key groups of K
     static constexpr int HALF_STRIDE = BS * 128;             // between the column halves of a V block tile
-    static constexpr int BLK_BYTES = HALVES * HALF_STRIDE;   // one block's V tile
+    static constexpr int BLK_BYTES = HALVES * HALF_STRIDE;   // one block's K or V tile
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;         // K, then V
     static constexpr int RING_OFF = Q_BYTES;
     static constexpr int SMEM_CAP = 227 * 1024;
@@ -300,23 +303,20 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         __syncwarp();   // lane 0's claim of the slot orders the other lanes' copies
                         // the stage's copies, one box per lane (the TMA unit takes boxes
-                        // one at a time: V goes as one box per block)
+                        // one at a time, so each block's K and V go as one box each):
+                        // lanes 0 .. SB - 1 the K boxes, the next SB lanes the V boxes
                         {
-                            // lanes 0 .. SB * HALVES - 1: K boxes (block i, column half h);
-                            // the next SB lanes: one V box per block (all halves)
-                            constexpr int NK = SB * HALVES;
-                            const bool kl = lane < NK;
-                            const int ci = kl ? lane / HALVES : lane - NK, ch = lane % HALVES;
+                            const bool kl = lane < SB;
+                            const int ci = kl ? lane : lane - SB;
                             int cid = __shfl_sync(0xffffffffu, ids, (bb + (ci & (SB - 1))) & 31);
                             if ((unsigned)cid >= (unsigned)p.NB) cid = 0;   // flagged and poisoned above
                             const int y = (cid * p.Hkv + it.kvh) * BS;
-                            if (ok && lane < NK + SB && ci < nbs) {
+                            const uint32_t dst = ring + st * Tr::STAGE_BYTES + (kl ? 0 : Tr::KV_BYTES) + ci * Tr::BLK_BYTES;
+                            if (ok && lane < 2 * SB && ci < nbs) {
                                 if (kl)
-                                    tma_load_2d(ring + st * Tr::STAGE_BYTES + ch * Tr::HALF_BYTES + ci * BS * 128, &tmap_k,
-                                                ch * 64, y, full(st));
+                                    tma_load_4d(dst, &tmap_k, 0, 0, 0, y / 8, full(st));
                                 else
-                                    tma_load_3d(ring + st * Tr::STAGE_BYTES + Tr::KV_BYTES + ci * Tr::BLK_BYTES, &tmap_v, 0,
-                                                y, 0, full(st));
+                                    tma_load_3d(dst, &tmap_v, 0, y, 0, full(st));
                             }
                         }
                         ++j;
@@ -381,11 +381,12 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         if (flags & TC_FIRST) ++nseg;
                         tc_fence_after();
                         const uint64_t qd = sdesc_sw128(q_tile, 16, 1024);
-                        const uint64_t kd = sdesc_sw128(ring + s_st * Tr::STAGE_BYTES, 16, 1024);
+                        const uint64_t kd = sdesc_sw128(ring + s_st * Tr::STAGE_BYTES, 16, Tr::GROUP_STRIDE);
 #pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step, +a half tile per 4 (address >> 4)
+                        for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step; per 4: Q's next half tile,
+                                                                // K's next 1024-byte atom (address >> 4)
                             mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (Tr::Q_HALF >> 4) + (k % 4) * 2),
-                                    kd + (uint64_t)((k / 4) * (Tr::HALF_BYTES >> 4) + (k % 4) * 2), IDESC_S,
+                                    kd + (uint64_t)((k / 4) * (1024 >> 4) + (k % 4) * 2), IDESC_S,
                                     k > 0 ? 1u : 0u);
                         }
                         mma_commit(s_full + 8 * b);

@@ -260,6 +260,29 @@ bool pool_map_chunk(CUtensorMap* m, const void* pool, const pa_shape* s) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The pool as a 4-D tensor (column within a 64-column half, row within an
+// 8-row group, half, 8-row group): one box of 64 columns x 8 rows x all halves
+// x block_size / 8 groups lands a whole (block, kv head) chunk as
+// [group][half][8 rows][128 B], one 1024-byte swizzle atom per (group, half).
+// Consecutive 8-row groups of a half are then a fixed stride apart (halves x
+// 1024 bytes) across the blocks of a stage, so one K-major descriptor spans
+// all of a stage's keys.
+bool pool_map_groups(CUtensorMap* m, const void* pool, const pa_shape* s) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int halves = s->head_dim / 64;
+    const cuuint64_t rows = (cuuint64_t)s->num_blocks * s->num_kv_heads * s->block_size;
+    const cuuint64_t dims[4] = {64, 8, (cuuint64_t)halves, rows / 8};
+    const cuuint64_t strides[3] = {(cuuint64_t)s->head_dim * 2, 128, (cuuint64_t)s->head_dim * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, (cuuint32_t)halves, (cuuint32_t)s->block_size / 8};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt =
+        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 4, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q [T][Hq][D] as a 3-D tensor (head_dim, heads, tokens): boxes of 64
 // columns x g heads x q_box tokens land as rows i * g + hh, 128-byte swizzled.
 bool q_map(CUtensorMap* m, const void* q, const pa_shape* s, int total_q, int q_box) {
@@ -804,8 +827,9 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < multi_region_bytes(shape, ctas, k->rows))
         return PA_ERR_WORKSPACE;
     CUtensorMap mk, mv, mq;
-    // the tcgen05 kernel copies V as whole (block, kv head) chunks
-    if (!pool_map(&mk, k_pool, shape) ||
+    // the tcgen05 kernel copies K and V as whole (block, kv head) chunks: K in
+    // 8-row groups (one descriptor spans a stage's keys), V as column halves
+    if (!(tc ? pool_map_groups(&mk, k_pool, shape) : pool_map(&mk, k_pool, shape)) ||
         !(tc ? pool_map_chunk(&mv, v_pool, shape) : pool_map(&mv, v_pool, shape)))
         return PA_ERR_CUDA;
     const int q_box = std::min(max_q_len, total_q);

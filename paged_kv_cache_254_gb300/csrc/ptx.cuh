@@ -94,6 +94,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
 }
 
+// 4-D tiled tensor load into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar) : "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory (16-byte aligned, size a
 // multiple of 16); completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
