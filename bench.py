@@ -625,7 +625,7 @@ def gpu_arm(args):
                      "kernel": ("pa_prefix_kernel + pa_decode_kernel" if use_prefix else
                                 "pa_decode_kernel (4-bit cache)" if int4 else
                                 "pa_decode_kernel (8-bit cache)" if fp8 else
-                                ("pa_multi_tc_kernel (tcgen05)" if args.q_len * Hq // Hkv >= 33 else
+                                ("pa_multi_tc_kernel (tcgen05)" if args.q_len * Hq // Hkv > 16 else
                                  "pa_multi_kernel (mma.sync)") if multi else "pa_decode_kernel"),
                      "traffic_source": ("ncu dram bytes of the attention kernel on the first 64 sequences, "
                                         "scaled by algorithmic bytes" if traffic is not None else None),

@@ -3,15 +3,9 @@
 
 namespace pa {
 
-void multi_table_fp16_d128(MultiKernelInfo (&t)[2][4]) {
-    t[0][0] = multi_info<MultiTraits<128, 16, 1, false>>();
-    t[0][1] = multi_info<MultiTraits<128, 16, 2, false>>();
-    t[0][2] = multi_info<MultiTraits<128, 16, 4, false>>();
-    t[0][3] = multi_info<MultiTraits<128, 16, 8, false>>();
-    t[1][0] = multi_info<MultiTraits<128, 32, 1, false>>();
-    t[1][1] = multi_info<MultiTraits<128, 32, 2, false>>();
-    t[1][2] = multi_info<MultiTraits<128, 32, 4, false>>();
-    t[1][3] = multi_info<MultiTraits<128, 32, 8, false>>();
+void multi_table_fp16_d128(MultiKernelInfo (&t)[2]) {
+    t[0] = multi_info<MultiTraits<128, 16, 1, false>>();
+    t[1] = multi_info<MultiTraits<128, 32, 1, false>>();
 }
 
 }  // namespace pa

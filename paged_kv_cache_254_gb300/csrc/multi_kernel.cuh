@@ -571,10 +571,10 @@ MultiKernelInfo multi_info() {
                            Tr::ROWS};
 }
 
-// Index: [bs == 32][log2(NW)]; one table per (dtype, head_dim), defined in multi_*.cu.
-void multi_table_bf16_d128(MultiKernelInfo (&t)[2][4]);
-void multi_table_bf16_d64(MultiKernelInfo (&t)[2][4]);
-void multi_table_fp16_d128(MultiKernelInfo (&t)[2][4]);
-void multi_table_fp16_d64(MultiKernelInfo (&t)[2][4]);
+// Index: [bs == 32] (one 16-row tile, NW = 1); one table per (dtype, head_dim), defined in multi_*.cu.
+void multi_table_bf16_d128(MultiKernelInfo (&t)[2]);
+void multi_table_bf16_d64(MultiKernelInfo (&t)[2]);
+void multi_table_fp16_d128(MultiKernelInfo (&t)[2]);
+void multi_table_fp16_d64(MultiKernelInfo (&t)[2]);
 
 }  // namespace pa

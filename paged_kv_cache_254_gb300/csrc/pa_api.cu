@@ -364,31 +364,37 @@ const PrefixKernelInfo& pick_prefix(const pa_shape* s) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ---------------------------------------------------------------- multi-token query
-// Kernel for a launch whose chunks hold up to max_q tokens: 16-row tiles per
-// CTA = the rows of one (sequence, KV head) pair, max_q * g <= 128.
-pa_status pick_multi(const pa_shape* s, int max_q, const MultiKernelInfo** out) {
+// Launches whose (sequence, KV head) pairs carry more than 16 query rows
+// (max_q * g) run on the tensor-core (tcgen05) kernel: 128-row MMA tiles, one
+// CTA per SM.  Up to 16 rows, the mma.sync kernel's single 16-row tile per
+// pair reads each block once for all rows and stays close to the HBM bound;
+// above that its tiles double the MMA and softmax work per block while the
+// tcgen05 tile costs the same up to 128 rows (70B-shaped batch, 4-token
+// chunks: 1.09 ms on two mma.sync tiles, 0.86 ms on tcgen05).
+constexpr int kTcMinRows = 17;
+
+// Shape rules shared by both multi-token kernels; `rows` = max_q * g.
+pa_status check_multi(const pa_shape* s, int max_q, int* rows) {
     const DecodeKernelInfo* k16 = nullptr;
     pa_status st = pick_decode(s, &k16);                  // the same shape rules as decode
     if (st != PA_OK) return st;
     if (max_q < 1 || max_q > 16) return PA_ERR_INVALID_ARG;
-    const int rows = max_q * (s->num_q_heads / s->num_kv_heads);
-    if (rows > 128) return PA_ERR_UNSUPPORTED;
-    const int nw = rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 4 : 8;
+    *rows = max_q * (s->num_q_heads / s->num_kv_heads);
+    return *rows > 128 ? PA_ERR_UNSUPPORTED : PA_OK;
+}
+
+// The mma.sync kernel: one 16-row tile per (sequence, KV head) pair.
+const MultiKernelInfo* pick_multi(const pa_shape* s) {
     static const auto tab = [] {
-        struct T { MultiKernelInfo t[2][2][2][4]; } x;   // [bf16][d == 128][bs == 32][log2 nw]
+        struct T { MultiKernelInfo t[2][2][2]; } x;      // [bf16][d == 128][bs == 32]
         multi_table_fp16_d64(x.t[0][0]);
         multi_table_fp16_d128(x.t[0][1]);
         multi_table_bf16_d64(x.t[1][0]);
         multi_table_bf16_d128(x.t[1][1]);
         return x;
     }();
-    *out = &tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32][log2_exact(nw)];
-    return PA_OK;
+    return &tab.t[s->dtype == PA_BF16][s->head_dim == 128][s->block_size == 32];
 }
-
-// Launches whose pairs carry at least this many query rows run on the
-// tensor-core (tcgen05) kernel: 128-row MMA tiles, one CTA per SM.
-constexpr int kTcMinRows = 33;
 
 const MultiKernelInfo* pick_multi_tc(const pa_shape* s) {
     static const auto tab = [] {
@@ -786,14 +792,15 @@ int32_t pa_version(void) { return 100; }
 
 
 size_t pa_decode_multi_workspace_bytes(const pa_shape* shape, int32_t max_q_len) {
-    const MultiKernelInfo* k = nullptr;
-    if (pick_multi(shape, max_q_len, &k) != PA_OK) return 0;
+    int rows = 0;
+    if (check_multi(shape, max_q_len, &rows) != PA_OK) return 0;
+    const MultiKernelInfo* k = pick_multi(shape);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const int ctas = k->max_ctas(dev);
     if (ctas <= 0) return 0;
     size_t need = multi_region_bytes(shape, ctas, k->rows);
-    if (max_q_len * (shape->num_q_heads / shape->num_kv_heads) >= kTcMinRows) {
+    if (rows >= kTcMinRows) {
         const MultiKernelInfo* t = pick_multi_tc(shape);
         const int tctas = t->max_ctas(dev);
         if (tctas <= 0) return 0;
@@ -806,13 +813,14 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
                           const int32_t* q_start, const void* k_pool, const void* v_pool,
                           const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
                           void* workspace, size_t workspace_bytes, uint32_t* err_word, void* stream) {
-    const MultiKernelInfo* k = nullptr;
-    pa_status st = pick_multi(shape, max_q_len, &k);
+    int g_rows = 0;
+    pa_status st = check_multi(shape, max_q_len, &g_rows);
     if (st != PA_OK) return st;
     if (total_q < 0) return PA_ERR_INVALID_ARG;
-    const int g_rows = max_q_len * (shape->num_q_heads / shape->num_kv_heads);
+    // with no query rows at all (total_q 0) the mma.sync kernel only checks
+    // the chunk descriptions: every chunk is empty or malformed
     const bool tc = g_rows >= kTcMinRows && total_q > 0;
-    if (tc) k = pick_multi_tc(shape);
+    const MultiKernelInfo* k = tc ? pick_multi_tc(shape) : pick_multi(shape);
     if (!q_start || !k_pool || !v_pool || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
     if (total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||

@@ -1,6 +1,6 @@
 """Parity of the tensor-core (tcgen05) multi-token kernel with the fp64 oracle.
 
-Launches whose (sequence, KV head) pairs carry at least 33 query rows
+Launches whose (sequence, KV head) pairs carry more than 16 query rows
 (max_q_len x group size) run on the 128-row tcgen05 kernel; smaller ones on
 the mma.sync kernel.  These cases sit above the threshold unless noted."""
 
@@ -51,7 +51,7 @@ EDGE = [1, 2, 15, 16, 17, 31, 33, 63, 64, 65, 100, 129, 517]
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B", [16, 32])
-@pytest.mark.parametrize("g,max_q", [(4, 9), (8, 5), (8, 8), (16, 3), (16, 8), (4, 16)])
+@pytest.mark.parametrize("g,max_q", [(4, 5), (8, 3), (16, 2), (4, 9), (8, 5), (8, 8), (16, 3), (16, 8), (4, 16)])
 def test_ragged_chunks(dtype, d, B, g, max_q):
     rng = np.random.Generator(np.random.PCG64(1000 + 10 * g + max_q + d + B))
     qlens = [int(rng.integers(0, min(max_q, c) + 1)) for c in EDGE]
@@ -83,13 +83,13 @@ def test_prefill_chunks_from_empty_cache():
 
 
 def test_same_answer_as_the_mma_sync_kernel():
-    # max_q_len 4 (32 rows) runs the mma.sync kernel, max_q_len 5 the tcgen05
-    # one; chunks of at most 4 tokens are valid for both
+    # max_q_len 2 (16 rows) runs the mma.sync kernel, max_q_len 3 the tcgen05
+    # one; chunks of at most 2 tokens are valid for both
     ctx = [700, 3000, 45, 1200, 5, 64]
-    qlens = [4, 3, 4, 1, 4, 2]
+    qlens = [2, 1, 2, 1, 2, 2]
     case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=23, poison=True)
-    a = run(case, q, qs, max_q=4)
-    b = run(case, q, qs, max_q=5)
+    a = run(case, q, qs, max_q=2)
+    b = run(case, q, qs, max_q=3)
     ref = oracle(case, q, qs)
     assert_close(a, ref, what="mma.sync")
     assert_close(b, ref, what="tcgen05")
@@ -168,10 +168,10 @@ def test_verify_batch_16_token_chunks_sampled():
         assert_close(got[16 * s:16 * s + 16], ref, what=f"sequence {s}")
 
 
-@pytest.mark.parametrize("max_q", [4, 8])     # 32 rows per pair: mma.sync kernel; 64 rows: tcgen05
+@pytest.mark.parametrize("max_q", [2, 4, 8])  # 16 rows per pair: mma.sync kernel; 32, 64 rows: tcgen05
 def test_bad_context_length_poisons_its_rows(max_q):
     ctx = [300, 500, 77, 1000]
-    qlens = [max_q, 2, 3, max_q]
+    qlens = [max_q, 2, min(3, max_q), max_q]
     case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=53)
     cl = case.context_lens.copy()
     cl[1] = case.block_tables.shape[1] * case.cfg.block_size + 5      # longer than its table can hold
@@ -190,14 +190,32 @@ def test_bad_context_length_poisons_its_rows(max_q):
 
 
 @pytest.mark.parametrize("q_mult", [8.0, 32.0])
-def test_peaked_and_planted_keys_tcgen05(q_mult):
-    # 64 query rows per pair (tcgen05 kernel): peaked scores plus keys that
-    # dominate late in long split contexts and inside the chunk
+@pytest.mark.parametrize("max_q", [3, 8])         # 24 and 64 query rows per pair
+def test_peaked_and_planted_keys_tcgen05(q_mult, max_q):
+    # tcgen05 kernel: peaked scores plus keys that dominate late in long split
+    # contexts and inside the chunk
     ctx = [3000, 2000, 777, 64]
-    qlens = [8, 5, 8, 8]
-    case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=521)
+    qlens = [max_q, min(5, max_q), max_q, max_q]
+    case, q, qs = multi_case(ctx, qlens, Hq=16, Hkv=2, seed=521 + max_q)
     q.mul_(q_mult)
     plant_key(case, 0, 2950, target=60.0, q=q[qs[0]])
-    plant_key(case, 1, 1998, target=45.0, q=q[qs[1] + 4])
+    plant_key(case, 1, 1998, target=45.0, q=q[qs[1] + min(4, max_q - 1)])
     plant_key(case, 2, 100, target=50.0, q=q[qs[2] + 1])
-    assert_close(run(case, q, qs, max_q=8), oracle(case, q, qs), what=f"tcgen05 peaked x{q_mult}")
+    assert_close(run(case, q, qs, max_q=max_q), oracle(case, q, qs), what=f"tcgen05 peaked x{q_mult} q{max_q}")
+
+
+def test_verify_batch_4_token_chunks_sampled():
+    # the 70B-shaped batch with 4-token chunks (three drafted tokens + one; 32
+    # rows per pair), checked on its first 6 sequences
+    cfg = CONFIGS["llama3_70b_b256"]
+    case = make_decode_case(cfg, device="cuda", seed=41)
+    N = len(case.context_lens)
+    qs = (np.arange(N + 1) * 4).astype(np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(43)
+    q = make_values((4 * N, cfg.num_q_heads, cfg.head_dim), cfg.dtype, gen, "cuda")
+    got = run(case, q, qs, max_q=4)
+    n = 6
+    ref = decode_multi_ref(q[:4 * n], case.k_pool, case.v_pool, case.block_tables[:n], case.context_lens[:n],
+                           qs[:n + 1], case.scale)
+    assert_close(got[:4 * n], ref, what="70B batch, 4-token chunks")
+    assert torch.isfinite(got.float()).all()
