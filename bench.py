@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # the cache type; a stale key reports null.
 #   (hash, kv dtype): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("c62c98d725465c97", "bf16"): (1_218_195_712 + 21_107_968, 1_216_111_324),
-    ("c62c98d725465c97", "fp8_e4m3"): (610_135_296 + 14_837_504, 609_141_468),
-    ("c62c98d725465c97", "int4"): (324_677_632 + 6_619_136, 324_624_348),
+    ("5fd304c972fbaa3b", "bf16"): (1_218_195_712 + 21_180_416, 1_216_111_324),
+    ("5fd304c972fbaa3b", "fp8_e4m3"): (610_137_600 + 14_552_832, 609_141_468),
+    ("5fd304c972fbaa3b", "int4"): (324_624_896 + 6_251_264, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")

@@ -35,12 +35,14 @@
 // combination.
 //
 // Inside a warp.  Each warp owns R shared-memory stages with one mbarrier
-// each.  Lane 0 issues the copies of a stage (two-dimensional TMA loads with
-// 128-byte swizzle for the 16-bit cache, one bulk copy per block piece for the
-// 8-bit cache) R stages ahead of the one being computed, and refills a stage
-// as soon as it has been folded in (consume_block / consume_stage8: mma.sync
-// scores, online softmax, PV).  Block ids come from the table 32 at a time,
-// one per lane.  No warp ever waits for another.
+// each.  The copies of a stage (two-dimensional TMA loads with 128-byte
+// swizzle for the 16-bit cache, one bulk copy per block piece for the
+// quantized caches) are issued R stages ahead of the one being computed, and
+// a stage is refilled as soon as it has been folded in (mma.sync scores,
+// online softmax, PV: consume_block for the 16-bit cache with the query heads
+// as MMA rows; consume_stage8t / consume_stage4t for the quantized caches
+// with the stage's tokens as MMA rows).  Block ids come from the table 32 at
+// a time, one per lane.  No warp ever waits for another.
 //
 // Every wait is bounded (PA_DEVERR_TIMEOUT); bad block ids and context lengths
 // set error bits and poison the affected rows with NaN instead of trapping.

@@ -468,9 +468,16 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
 // by the log-sum-exp rule.  A pair is cut where a chunk boundary falls
 // strictly inside it; one CTA per boundary, and the first boundary inside a
 // pair merges it (the others return), so only cut pairs cost work.  Each warp
-// merges rows of the pair: D / 4 lanes per row, 4 dims each.
+// merges rows of the pair: D / 4 lanes per row, 4 dims each.  With up to
+// MERGE_PIECES pieces, a row's (m, l, o slice) of every piece are loaded in
+// one round before any is used (one memory latency per row, and the CTA's
+// MERGE_THREADS / 32 warps keep that many rows in flight); more pieces take
+// two passes.
+constexpr int MERGE_THREADS = 512;
+constexpr int MERGE_PIECES = 4;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(MERGE_THREADS)
 pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_start,
                const int32_t* __restrict__ context_lens, const float* __restrict__ partials,
                uint16_t* __restrict__ out, int N, int Hkv, int G, int rows_per_chunk, int nchunks_hint,
@@ -514,20 +521,50 @@ pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_
                              (sc.lo(cfirst) < P0 ? (size_t)rows_per_chunk * PSTRIDE : 0) + (size_t)row * PSTRIDE;
         const float* rest = partials + (size_t)cfirst * cstride + (size_t)row * PSTRIDE;
         auto piece = [&](int i) -> const float* { return i == 0 ? first : rest + (size_t)i * cstride; };
-        float M = -INFINITY;
-        for (int i = 0; i < np; ++i) M = fmaxf(M, piece(i)[D]);
-        const float Mref = M == -INFINITY ? 0.f : M;
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < np; ++i) {
-            const float* pr = piece(i);
-            const float f = ex2(pr[D] - Mref);
-            L += pr[D + 1] * f;
-            const float4 v = *reinterpret_cast<const float4*>(pr + d0);
-            acc.x += v.x * f;
-            acc.y += v.y * f;
-            acc.z += v.z * f;
-            acc.w += v.w * f;
+        if (np <= MERGE_PIECES) {
+            float mv[MERGE_PIECES], lv[MERGE_PIECES];
+            float4 ov[MERGE_PIECES];
+#pragma unroll
+            for (int i = 0; i < MERGE_PIECES; ++i) {
+                if (i < np) {
+                    const float* pr = piece(i);
+                    mv[i] = pr[D];
+                    lv[i] = pr[D + 1];
+                    ov[i] = *reinterpret_cast<const float4*>(pr + d0);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < MERGE_PIECES; ++i)
+                if (i < np) M = fmaxf(M, mv[i]);
+            const float Mref = M == -INFINITY ? 0.f : M;
+#pragma unroll
+            for (int i = 0; i < MERGE_PIECES; ++i) {
+                if (i < np) {
+                    const float f = ex2(mv[i] - Mref);
+                    L += lv[i] * f;
+                    acc.x += ov[i].x * f;
+                    acc.y += ov[i].y * f;
+                    acc.z += ov[i].z * f;
+                    acc.w += ov[i].w * f;
+                }
+            }
+        } else {
+            float M = -INFINITY;
+            for (int i = 0; i < np; ++i) M = fmaxf(M, piece(i)[D]);
+            const float Mref = M == -INFINITY ? 0.f : M;
+            for (int i = 0; i < np; ++i) {
+                const float* pr = piece(i);
+                const float f = ex2(pr[D] - Mref);
+                L += pr[D + 1] * f;
+                const float4 v = *reinterpret_cast<const float4*>(pr + d0);
+                acc.x += v.x * f;
+                acc.y += v.y * f;
+                acc.z += v.z * f;
+                acc.w += v.w * f;
+            }
         }
         if (!writer) continue;
         const float inv = 1.f / L;

@@ -879,11 +879,11 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     const int g = shape->num_q_heads / shape->num_kv_heads;
     if (ctas > 1) {   // one CTA per chunk boundary: the pairs cut there
         if (shape->head_dim == 128)
-            pa_multi_merge<128><<<ctas - 1, 256, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
+            pa_multi_merge<128><<<ctas - 1, MERGE_THREADS, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
                                                                 d.Hkv, g, k->rows, ctas, max_q_len, total_q,
                                                                 shape->dtype == PA_BF16);
         else
-            pa_multi_merge<64><<<ctas - 1, 256, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
+            pa_multi_merge<64><<<ctas - 1, MERGE_THREADS, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
                                                                d.Hkv, g, k->rows, ctas, max_q_len, total_q,
                                                                shape->dtype == PA_BF16);
     }

@@ -221,37 +221,6 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t v) {
     return r;
 }
 
-// Two 4-bit codes -> f16x2: nibbles at bits 0..3 and 16..19 of x hold
-// code + 8; OR-ing them under the fp16 pattern of 1024 gives 1024 + nibble
-// exactly, and subtracting 1032 leaves the code.
-__device__ __forceinline__ uint32_t i4_pair_lo(uint32_t x) {
-    const uint32_t h = (x & 0x000f000fu) | 0x64006400u;
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
-    return r;
-}
-
-// The same for the nibbles at bits 4..7 and 20..23, without a shift: under
-// the pattern of 1024 they read as 1024 + 16 nibble, and (1024 + 16 n) / 16
-// - 72 = n - 8 is exact in one fp16 fused multiply-add (1/16 is a power of
-// two and every intermediate is an integer or 64 + n below 2^11).
-__device__ __forceinline__ uint32_t i4_pair_hi(uint32_t x) {
-    const uint32_t h = (x & 0x00f000f0u) | 0x64006400u;
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(h), "r"(0x2c002c00u), "r"(0xd480d480u));
-    return r;
-}
-
-// The eight codes of one word -> four f16x2 pairs; pair k holds the nibbles
-// k and k + 4 (one shift for all four).
-__device__ __forceinline__ void i4x8_to_f16x2(uint32_t x, uint32_t (&h)[4]) {
-    const uint32_t y = x >> 8;
-    h[0] = i4_pair_lo(x);
-    h[1] = i4_pair_hi(x);
-    h[2] = i4_pair_lo(y);
-    h[3] = i4_pair_hi(y);
-}
-
 // The eight nibbles n of one word as fp16 subnormals, exactly: a nibble at
 // bits 0..3 of a 16-bit half reads as n * 2^-24, one at bits 4..7 as
 // n * 2^-20 (one AND each, no arithmetic).  Pair 0: nibbles 0, 4 (2^-24);
