@@ -11,7 +11,10 @@
 //
 // Rows.  For a (sequence, KV head) pair the query rows are r = i * g + hh
 // (token i of the chunk, head hh of the group): q_len * g <= 16 * NW rows,
-// 16 per warp (one m16 tile of the score MMA, as in the decode kernel).
+// 16 per warp (one m16 tile of the score MMA, as in the decode kernel).  The
+// library runs this kernel with NW = 1 (launches of up to 16 rows per pair);
+// larger ones go to the tcgen05 kernel (multi_tc_kernel.cuh), whose 128-row
+// tile costs the same at any row count.
 //
 // Work split.  The pairs' blocks are laid end to end and cut into one equal
 // contiguous chunk per CTA (the decode kernel's static split).  A CTA reads

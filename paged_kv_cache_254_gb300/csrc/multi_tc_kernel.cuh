@@ -3,7 +3,7 @@
 // merge post-pass as pa_multi_kernel (chunked prefill and speculative
 // verification: thewebvale "vLLM & High-Throughput Serving", section 4;
 // letsbuildsolutions "How LLM Inference Engines Work", speculative decoding),
-// for launches whose (sequence, KV head) pairs carry up to 128 query rows.
+// for launches whose (sequence, KV head) pairs carry 17 to 128 query rows.
 //
 // Tile.  The rows r = i * g + hh of a pair (token i of the chunk, head hh of
 // the group) are the M = 128 rows of every MMA; rows past q_len * g are
@@ -11,8 +11,8 @@
 // in stages of 64 (64 / B blocks of one pair).
 //
 //   S  = Q K^T   M 128, N 64, K = head_dim   (Q, K: K-major swizzled tiles)
-//   O += P V     M 128, N = head_dim, K 64   (P: K-major; V: MN-major tiles,
-//                                             one per block)
+//   O += P V     M 128, N = head_dim, K 64   (P: from tensor memory; V:
+//                                             MN-major tiles, one per block)
 //
 // with S (two 64-column fp32 buffers), P (two buffers of 16-bit weights, the
 // A operand of the PV product) and O (fp32) all in tensor memory.  P enters
@@ -20,20 +20,21 @@
 // weight as the mma.sync kernels do.
 //
 // Warp roles (352 threads, one CTA per SM):
-//   warps 0-7  softmax: warp w handles rows 32 (w % 4) .. + 31 (its TMEM lane
-//              quarter; thread = query row) and keys 32 (w / 4) .. + 31 of
-//              each stage; the two warps of a row quarter exchange their
-//              partial row maxima through shared memory.  Masks per row
-//              (causal limit), runs the online softmax and writes P to
-//              TMEM; zeroes the V rows of a stage past the context; at a
-//              segment end loads its half of O and writes the output rows or
-//              the partial state.
+//   warps 0-7  softmax, two streams on alternating stages: warp w takes rows
+//              32 (w % 4) .. + 31 (its TMEM lane quarter; thread = query row)
+//              of the stages of parity w / 4.  Masks per row (causal limit),
+//              runs the online softmax and writes P to tensor memory; zeroes
+//              the V rows of a stage past the context; at a segment end loads
+//              O and writes the output rows or the partial state.
 //   warp 8     copies: per segment the Q tile (one 3-D TMA per 64-column
-//              half: box = g heads x max_q tokens, landing as rows i * g + hh),
-//              per stage the K and V boxes of its blocks (2-D TMA).
-//   warp 9     scores: allocates TMEM; issues S of each stage as soon as its
-//              copy has landed and its TMEM buffer is free.
-//   warp 10    PV: issues the PV product of each stage once its P is written.
+//              half: box = g heads x max_q tokens, landing as rows i * g + hh);
+//              per stage one TMA box per block and operand, issued by
+//              different lanes (the TMA unit's cost is per box, so fewer,
+//              larger boxes keep more bytes in flight).
+//   warp 9     scores: allocates TMEM; one thread issues S of each stage as
+//              soon as its copy has landed and its TMEM buffer is free.
+//   warp 10    PV: one thread issues the PV product of each stage once its P
+//              is written; the commit frees the stage's ring slot.
 //
 // Lazy rescaling.  A row keeps the reference maximum m_ref used for its
 // weights; only when a stage raises the row maximum above m_ref + 8 (log2
