@@ -62,8 +62,6 @@ struct TcTraits {
     static constexpr int KEYS = 64;                          // keys per stage (N of the score MMA)
     static constexpr int SB = KEYS / BS;                     // blocks per stage
     static constexpr int HALVES = D / 64;                    // 128-byte column halves of a row
-    static constexpr int Q_HALF = ROWS * 128;
-    static constexpr int Q_BYTES = HALVES * Q_HALF;
     static constexpr int KV_BYTES = KEYS * D * 2;            // a stage's K, or its V
     // Each block of a stage arrives as one TMA box per operand.
     //  * K: [8-row group][column half][8 rows][128 B] (a 4-D box), so the
@@ -76,20 +74,33 @@ struct TcTraits {
     static constexpr int HALF_STRIDE = BS * 128;             // between the column halves of a V block tile
     static constexpr int BLK_BYTES = HALVES * HALF_STRIDE;   // one block's K or V tile
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;         // K, then V
-    static constexpr int RING_OFF = Q_BYTES;
+    // Shared memory: barriers, stage records, exchange cells and a few words
+    // first (sized for R_CAP stages); then the Q tile, as many rows as the
+    // launch's chunks fill (q_rows(): the rows past them are read by the score
+    // MMA and discarded, whatever they hold); then the ring, as many stages as
+    // fit (ring_stages()), so shorter chunks get a deeper ring.
     static constexpr int SMEM_CAP = 227 * 1024;
+    static constexpr int SMEM_BYTES = SMEM_CAP;              // all of it, 1024 of it alignment slack
+    static constexpr int R_CAP = 12;
     static constexpr int REC_BYTES = 48;
     static constexpr int NBAR_FIXED = 12;    // s_full[2] s_free[2] p_full[2] pv_done[2] q_full q_empty fin o_free
     // tagged cells per row: softmax references along a segment's stages [4],
     // and the partial row sums handed to a segment's last stage [4] (value, reference)
     static constexpr int XCH_BYTES = (4 + 2 * 4) * ROWS * 8;
-    static constexpr int R_FIT = (SMEM_CAP - 1024 - RING_OFF - 8192) / STAGE_BYTES;
-    static constexpr int R = R_FIT > 12 ? 12 : R_FIT;
-    static constexpr int BAR_OFF = RING_OFF + R * STAGE_BYTES;
-    static constexpr int REC_OFF = (BAR_OFF + 8 * (2 * R + NBAR_FIXED) + 15) / 16 * 16;
-    static constexpr int XCH_OFF = REC_OFF + R * REC_BYTES;
-    static constexpr int MISC_OFF = XCH_OFF + XCH_BYTES;      // TMEM base, abort flag
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;   // + alignment slack
+    static constexpr int BAR_OFF = 0;
+    static constexpr int REC_OFF = (BAR_OFF + 8 * (2 * R_CAP + NBAR_FIXED) + 15) / 16 * 16;
+    static constexpr int XCH_OFF = REC_OFF + R_CAP * REC_BYTES;
+    static constexpr int MISC_OFF = XCH_OFF + XCH_BYTES;      // TMEM base, abort flag, stage count
+    static constexpr int Q_OFF = (MISC_OFF + 16 + 1023) / 1024 * 1024;
+    // rows of the Q tile: the launch's q_box tokens x g heads, whole 8-row swizzle atoms
+    __host__ __device__ static constexpr int q_rows(int q_box, int g) {
+        return q_box * g >= ROWS ? ROWS : (q_box * g + 7) / 8 * 8;
+    }
+    __host__ __device__ static constexpr int ring_stages(int qrows) {
+        return (SMEM_CAP - 1024 - Q_OFF - HALVES * qrows * 128) / STAGE_BYTES > R_CAP
+                   ? R_CAP
+                   : (SMEM_CAP - 1024 - Q_OFF - HALVES * qrows * 128) / STAGE_BYTES;
+    }
     static constexpr int SOFT_WARPS = 8;
     static constexpr int THREADS = 32 * (SOFT_WARPS + 3);
     static constexpr int COPY_WARP = SOFT_WARPS, MMA_WARP = SOFT_WARPS + 1, PV_WARP = SOFT_WARPS + 2;
@@ -100,8 +111,7 @@ struct TcTraits {
     static constexpr float TAU = 8.f;                        // lazy-rescale threshold (log2 units)
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BS == 16 || BS == 32, "block_size");
-    static_assert(R >= 3, "three ring stages at least (the MMA issue order relies on it)");
-    static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
+    static_assert(ring_stages(ROWS) >= 3, "three ring stages at least (the MMA issue order relies on it)");
     static_assert(O_COL + D <= P_COL && P_COL + 128 <= TMEM_COLS, "tensor memory");
 };
 
@@ -141,7 +151,7 @@ template <class Tr>
 __global__ void __launch_bounds__(Tr::THREADS, 1)
 pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const MultiParams mp) {
-    constexpr int D = Tr::D, BS = Tr::BS, R = Tr::R, SB = Tr::SB, HALVES = Tr::HALVES, KEYS = Tr::KEYS;
+    constexpr int D = Tr::D, BS = Tr::BS, SB = Tr::SB, HALVES = Tr::HALVES, KEYS = Tr::KEYS;
     constexpr int SW = Tr::SOFT_WARPS;
     constexpr uint32_t IDESC_S = idesc_f16<Tr::BF16>(128, KEYS, false, false);
     constexpr uint32_t IDESC_O = idesc_f16<Tr::BF16>(128, D, false, true);
@@ -152,8 +162,12 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int lane = threadIdx.x & 31;
     const int G = p.Hq / p.Hkv;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t q_tile = sbase;
-    const uint32_t ring = sbase + Tr::RING_OFF;
+    const int qrows = Tr::q_rows(mp.q_box, G);
+    const uint32_t q_half = (uint32_t)qrows * 128;            // between the Q tile's column halves
+    const int R = Tr::ring_stages(qrows);                     // ring stages
+    const uint32_t q_tile = sbase + Tr::Q_OFF;
+    const uint32_t ring_off = Tr::Q_OFF + HALVES * q_half;
+    const uint32_t ring = sbase + ring_off;
     const uint32_t bars = sbase + Tr::BAR_OFF;
     auto full = [&](int st) -> uint32_t { return bars + 8 * st; };
     auto empty = [&](int st) -> uint32_t { return bars + 8 * (R + st); };
@@ -255,7 +269,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             mbar_arrive_expect_tx(q_full, (uint32_t)(HALVES * 128 * G * mp.q_box));
 #pragma unroll
                             for (int h = 0; h < HALVES; ++h)
-                                tma_load_3d(q_tile + h * Tr::Q_HALF, &tmap_q, h * 64, it.kvh * G, q0, q_full);
+                                tma_load_3d(q_tile + h * q_half, &tmap_q, h * 64, it.kvh * G, q0, q_full);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -386,7 +400,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k) {      // +32 bytes per K step; per 4: Q's next half tile,
                                                                 // K's next 1024-byte atom (address >> 4)
-                            mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (Tr::Q_HALF >> 4) + (k % 4) * 2),
+                            mma_f16(tmem + 64 * b, qd + (uint64_t)((k / 4) * (q_half >> 4) + (k % 4) * 2),
                                     kd + (uint64_t)((k / 4) * (1024 >> 4) + (k % 4) * 2), IDESC_S,
                                     k > 0 ? 1u : 0u);
                         }
@@ -638,7 +652,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             // V rows past the context or past the blocks copied are zero for the PV product
             const int vvalid = max(0, min(nkeys, ctx - t0));
             if (vvalid < KEYS) {
-                uint8_t* vt = smem + Tr::RING_OFF + st * Tr::STAGE_BYTES + Tr::KV_BYTES;
+                uint8_t* vt = smem + ring_off + st * Tr::STAGE_BYTES + Tr::KV_BYTES;
                 const int nz = (KEYS - vvalid) * HALVES * 8;
                 for (int i = stid; i < nz; i += 128) {
                     const int key = vvalid + i / (HALVES * 8), part = i % (HALVES * 8);
