@@ -441,14 +441,14 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
         }
         if constexpr (!Tr::KV8) {
-            // the K and V boxes, one per lane (each TMA instruction holds its
-            // issuing thread for a while; lanes issue them side by side)
+            // the block's K and V chunks, one 3-D box each ([column half][BS
+            // rows][128 B]), issued by two lanes side by side (the TMA unit's
+            // cost is per box, and each instruction holds its thread a while)
             __syncwarp();
-            if (!aborted && lane < 2 * Gm::HALVES) {
+            if (!aborted && lane < 2) {
                 const int id = (unsigned)ids[0] < (unsigned)p.NB ? ids[0] : 0;   // a bad id is flagged above
-                const int h = lane >> 1, v = lane & 1;
-                tma_load_2d(ring + st * Gm::STAGE_BYTES + (v ? Gm::CHUNK_BYTES : 0) + h * Gm::BOX_BYTES,
-                            v ? &tmap_v : &tmap_k, h * 64, (id * p.Hkv + is.kvh) * BS, full0 + 8 * st);
+                tma_load_3d(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0), lane ? &tmap_v : &tmap_k, 0,
+                            (id * p.Hkv + is.kvh) * BS, 0, full0 + 8 * st);
             }
         }
         ++nis;

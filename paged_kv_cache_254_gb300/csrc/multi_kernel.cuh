@@ -293,11 +293,8 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             const uint32_t dst = ring + st * Gm::STAGE_BYTES;
             mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
             const int y = (id * p.Hkv + is.kvh) * BS;
-#pragma unroll
-            for (int h = 0; h < Gm::HALVES; ++h) {
-                tma_load_2d(dst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                tma_load_2d(dst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-            }
+            tma_load_3d(dst, &tmap_k, 0, y, 0, fb);                    // one box per chunk: [half][BS rows][128 B]
+            tma_load_3d(dst + Gm::CHUNK_BYTES, &tmap_v, 0, y, 0, fb);
         }
         ++nis;
         ++ib;

@@ -223,28 +223,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// The pool viewed as a 2-D tensor: rows = (block, kv head, slot), columns =
-// head_dim; boxes of 64 columns x block_size rows land 128-byte swizzled.
-bool pool_map(CUtensorMap* m, const void* pool, const pa_shape* s) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)s->head_dim,
-                                (cuuint64_t)s->num_blocks * s->num_kv_heads * s->block_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)s->head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)s->block_size};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return enc(m, dt, 2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The pool as a 3-D tensor (column within a 64-column half, row = (block,
 // kv head, slot), half): one box of 64 columns x block_size rows x all halves
 // lands as the halves' 128-byte swizzled [rows][128 B] tiles one after the
 // other -- a whole (block, kv head) chunk in one copy.  The half stride
-// (128 bytes) is below the row stride; both views cover the same bytes.
+// (128 bytes) is below the row stride.
 bool pool_map_chunk(CUtensorMap* m, const void* pool, const pa_shape* s) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -491,7 +474,7 @@ pa_status pa_decode(const pa_shape* shape, const void* q, const void* k_pool, co
     if (!workspace || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
-    if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+    if (!pool_map_chunk(&mk, k_pool, shape) || !pool_map_chunk(&mv, v_pool, shape)) return PA_ERR_CUDA;
 
     DecodeLaunch L{};
     L.tmap_k = &mk;
@@ -555,7 +538,7 @@ pa_status pa_decode_shared_prefix(const pa_shape* shape, const void* q, const vo
         return PA_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
-    if (!pool_map(&mk, k_pool, shape) || !pool_map(&mv, v_pool, shape)) return PA_ERR_CUDA;
+    if (!pool_map_chunk(&mk, k_pool, shape) || !pool_map_chunk(&mv, v_pool, shape)) return PA_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     const float scale_log2 = (float)((double)scale * 1.4426950408889634);   // log2(e)
@@ -837,8 +820,8 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     CUtensorMap mk, mv, mq;
     // the tcgen05 kernel copies K and V as whole (block, kv head) chunks: K in
     // 8-row groups (one descriptor spans a stage's keys), V as column halves
-    if (!(tc ? pool_map_groups(&mk, k_pool, shape) : pool_map(&mk, k_pool, shape)) ||
-        !(tc ? pool_map_chunk(&mv, v_pool, shape) : pool_map(&mv, v_pool, shape)))
+    if (!(tc ? pool_map_groups(&mk, k_pool, shape) : pool_map_chunk(&mk, k_pool, shape)) ||
+        !pool_map_chunk(&mv, v_pool, shape))
         return PA_ERR_CUDA;
     const int q_box = std::min(max_q_len, total_q);
     if (tc && !q_map(&mq, q, shape, total_q, q_box)) return PA_ERR_CUDA;

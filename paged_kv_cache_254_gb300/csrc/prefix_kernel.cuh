@@ -312,11 +312,9 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                         mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
                         const int y = (id * p.Hkv + it.kvh) * BS;
                         const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
-#pragma unroll
-                        for (int h = 0; h < Gm::HALVES; ++h) {
-                            tma_load_2d(kdst + h * Gm::BOX_BYTES, &tmap_k, h * 64, y, fb);
-                            tma_load_2d(kdst + Gm::CHUNK_BYTES + h * Gm::BOX_BYTES, &tmap_v, h * 64, y, fb);
-                        }
+                        // one box per chunk: [column half][BS rows][128 B]
+                        tma_load_3d(kdst, &tmap_k, 0, y, 0, fb);
+                        tma_load_3d(kdst + Gm::CHUNK_BYTES, &tmap_v, 0, y, 0, fb);
                     }
                     issued += run;
                     done += run;
