@@ -426,21 +426,28 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             }
             if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
             stage_poison[st] = bad ? 1 : 0;
-            const uint32_t fb = full0 + 8 * st;
-            const uint32_t dst = ring + st * Gm::STAGE_BYTES;
             if constexpr (Tr::KV8) {
-                // each block's piece is one contiguous run in the pool
-                mbar_arrive_expect_tx(fb, nblk * Gm::PIECE_BYTES);
-#pragma unroll
-                for (int u = 0; u < UB; ++u)
-                    if (u < nblk)
-                        bulk_load(dst + Gm::poff(u),
-                                  p.kv8 + ((size_t)ids[u] * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES, fb);
+                mbar_arrive_expect_tx(full0 + 8 * st, nblk * Gm::PIECE_BYTES);
             } else {
-                mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
+                mbar_arrive_expect_tx(full0 + 8 * st, Gm::STAGE_BYTES);
             }
         }
-        if constexpr (!Tr::KV8) {
+        if constexpr (Tr::KV8) {
+            // each block's piece is one contiguous run in the pool: one bulk
+            // copy per piece, lane u issuing piece u (each copy instruction
+            // holds its issuing thread a while; lanes issue side by side)
+            __syncwarp();
+            if (!aborted && lane < nblk) {
+                int id = 0;
+#pragma unroll
+                for (int u = 0; u < UB; ++u)
+                    if (u == lane) id = ids[u];
+                if ((unsigned)id >= (unsigned)p.NB) id = 0;   // flagged by lane 0 above
+                bulk_load(ring + st * Gm::STAGE_BYTES + Gm::poff(lane),
+                          p.kv8 + ((size_t)id * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES,
+                          full0 + 8 * st);
+            }
+        } else {
             // the block's K and V chunks, one 3-D box each ([column half][BS
             // rows][128 B]), issued by two lanes side by side (the TMA unit's
             // cost is per box, and each instruction holds its thread a while)
