@@ -282,20 +282,20 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         const int st = ist;
         if (++ist == R) ist = 0;
         int id = __shfl_sync(0xffffffffu, tcur, (ib - tbase) & 31);
+        const bool bad = (unsigned)id >= (unsigned)p.NB;
+        if (bad) id = 0;
+        const uint32_t fb = full0 + 8 * st;
         if (lane == 0) {
-            const bool bad = (unsigned)id >= (unsigned)p.NB;
-            if (bad) {
-                set_err(p.err, PA_DEVERR_BLOCK_ID);
-                id = 0;
-            }
+            if (bad) set_err(p.err, PA_DEVERR_BLOCK_ID);
             stage_poison[st] = bad ? 1 : 0;
-            const uint32_t fb = full0 + 8 * st;
-            const uint32_t dst = ring + st * Gm::STAGE_BYTES;
             mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
-            const int y = (id * p.Hkv + is.kvh) * BS;
-            tma_load_3d(dst, &tmap_k, 0, y, 0, fb);                    // one box per chunk: [half][BS rows][128 B]
-            tma_load_3d(dst + Gm::CHUNK_BYTES, &tmap_v, 0, y, 0, fb);
         }
+        __syncwarp();
+        // one box per chunk ([column half][BS rows][128 B]): K from lane 0, V
+        // from lane 1, side by side
+        if (lane < 2)
+            tma_load_3d(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0), lane ? &tmap_v : &tmap_k, 0,
+                        (id * p.Hkv + is.kvh) * BS, 0, fb);
         ++nis;
         ++ib;
         if (ib == ilen) {
@@ -386,7 +386,7 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
             if (warp == 0 && !idone) {
                 // refill this slot once every warp has released it
-                const bool ok = mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns);
+                const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * st, par, p.timeout_ns));
                 if (!ok) {
                     if (lane == 0) {
                         set_err(p.err, PA_DEVERR_TIMEOUT);
