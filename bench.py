@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # the cache type; a stale key reports null.
 #   (hash, kv dtype): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("5fd304c972fbaa3b", "bf16"): (1_218_195_712 + 21_180_416, 1_216_111_324),
-    ("5fd304c972fbaa3b", "fp8_e4m3"): (610_137_600 + 14_552_832, 609_141_468),
-    ("5fd304c972fbaa3b", "int4"): (324_624_896 + 6_251_264, 324_624_348),
+    ("b38d995c81ab74bf", "bf16"): (1_218_225_152 + 20_959_488, 1_216_111_324),
+    ("b38d995c81ab74bf", "fp8_e4m3"): (610_174_720 + 14_523_136, 609_141_468),
+    ("b38d995c81ab74bf", "int4"): (324_636_160 + 5_971_968, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")
