@@ -43,13 +43,14 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum) of a SMALL case: the first 64
 # sequences of the workload (inputs above L2, a few GB on the device).  The
 # line scales it to the full launch by algorithmic bytes (traffic grows in
-# proportion to the KV stream).  Keyed by a hash of the kernel sources and
-# the cache type; a stale key reports null.
-#   (hash, kv dtype): (captured dram bytes, algorithmic bytes of the captured launch)
+# proportion to the KV stream).  Keyed by a hash of the kernel sources, the
+# cache type and the workload; any other key (a changed source, another
+# workload or kernel instantiation) reports null.
+#   (hash, kv dtype, workload): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("b38d995c81ab74bf", "bf16"): (1_218_225_152 + 20_959_488, 1_216_111_324),
-    ("b38d995c81ab74bf", "fp8_e4m3"): (610_174_720 + 14_523_136, 609_141_468),
-    ("b38d995c81ab74bf", "int4"): (324_636_160 + 5_971_968, 324_624_348),
+    ("b38d995c81ab74bf", "bf16", "llama3_70b_b256"): (1_218_225_152 + 20_959_488, 1_216_111_324),
+    ("b38d995c81ab74bf", "fp8_e4m3", "llama3_70b_b256"): (610_174_720 + 14_523_136, 609_141_468),
+    ("b38d995c81ab74bf", "int4", "llama3_70b_b256"): (324_636_160 + 5_971_968, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")
@@ -63,9 +64,9 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def scaled_traffic(khash: str, kv: str, alg_bytes: int):
+def scaled_traffic(khash: str, kv: str, workload: str, alg_bytes: int):
     """Captured DRAM bytes of the small case scaled to `alg_bytes`, or None."""
-    rec = TRAFFIC.get((khash, kv))
+    rec = TRAFFIC.get((khash, kv, workload))
     if rec is None:
         return None
     dram, alg = rec
@@ -328,7 +329,7 @@ def cpu_worker(args):
         n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     else:
         cfg = CONFIGS[args.config]
-        case = make_decode_case(cfg, device="cpu", seed=args.seed, num_seqs=min(cfg.num_seqs, 48))
+        case = make_decode_case(cfg, device="cpu", seed=args.seed, num_seqs=min(cfg.num_seqs, 160))
         tables, ctx_all = case.block_tables, case.context_lens
         n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     n_gen = len(ctx_all)
@@ -588,7 +589,7 @@ def gpu_arm(args):
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = ubytes / (dec_avg_ms * 1e-3) / 1e9
     khash = kernel_hash()
-    traffic = None if (multi or use_prefix) else scaled_traffic(khash, args.kv_dtype, ubytes)
+    traffic = None if (multi or use_prefix) else scaled_traffic(khash, args.kv_dtype, args.config, ubytes)
 
     if rank != 0:
         return
