@@ -231,10 +231,10 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16", q_len=1) -
     import torch
 
     from paged_kv_cache_254_gb300 import BlockManager
-    from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case
+    from workloads import CONFIGS, SAMPLINGS, make_decode_case, make_sampling_case
 
-    if name == SAMPLING.name:
-        cfg = SAMPLING
+    if name in SAMPLINGS:
+        cfg = SAMPLINGS[name]
         seed = cfg.seed if seed is None else seed
         case = make_sampling_case(cfg, device=device, seed=seed)
         B, S = cfg.block_size, cfg.samples
@@ -308,7 +308,7 @@ def make_workload(name, device, seed, num_seqs=None, kv_dtype="bf16", q_len=1) -
         "tables_h": tables, "ctx_h": ctx, "slots_h": slots, "copies_h": copies,
         "tables": to(tables), "ctx": to(ctx), "slots": to(slots), "copies": to(copies),
         "host_block_manager_ms": host_ms, "bm_stats": bm.stats(),
-        "shared": name == SAMPLING.name, "kv_dtype": kv_dtype,
+        "shared": name in SAMPLINGS, "kv_dtype": kv_dtype,
         "group_starts": to(gstarts), "group_prefix": to(gprefix), "n_groups": int(gprefix.size),
         "q_len": q_len, "q_start": to((np.arange(len(seqs) + 1) * q_len).astype(np.int32)),
     }
@@ -319,11 +319,11 @@ def cpu_worker(args):
     """Time the fp64 oracle on the first sequences of the workload (host
     cores, single-threaded BLAS) and print one JSON object."""
     from oracle.attention import decode_multi_ref, decode_ref
-    from workloads import CONFIGS, SAMPLING, make_decode_case, make_sampling_case, sampling_tables
+    from workloads import CONFIGS, SAMPLINGS, make_decode_case, make_sampling_case, sampling_tables
     import torch
 
-    if args.config == SAMPLING.name:
-        cfg = SAMPLING
+    if args.config in SAMPLINGS:
+        cfg = SAMPLINGS[args.config]
         case = make_sampling_case(cfg, device="cpu", seed=args.seed, groups=8)
         tables, ctx_all = sampling_tables(case)
         n_total, Hq, Hkv, d, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
@@ -349,7 +349,7 @@ def cpu_worker(args):
         done += 1
     dt = time.perf_counter() - t0
     ctx_done = [int(c) for c in ctx_all[:done]]
-    if args.config == SAMPLING.name:
+    if args.config in SAMPLINGS:
         nbytes = unique_decode_bytes(tables[:done], ctx_done, Hq, Hkv, d, B)
     else:
         nbytes = decode_bytes(ctx_done, Hq, Hkv, d, B, q_len=ql)
@@ -386,8 +386,8 @@ def reference_arm(args):
     world, rank, local = dist_env()
     if world > 1 and rank != 0:
         return
-    from workloads import CONFIGS, SAMPLING
-    cfg = SAMPLING if args.config == SAMPLING.name else CONFIGS[args.config]
+    from workloads import CONFIGS, SAMPLINGS
+    cfg = SAMPLINGS[args.config] if args.config in SAMPLINGS else CONFIGS[args.config]
     vals = []
     sample = None
     tok = []
@@ -451,7 +451,7 @@ def gpu_arm(args):
     _build.build()
 
     seed = None if args.seed is None and rank == 0 else (args.seed or 0) + 1000 * rank
-    if args.q_len > 1 and (args.kv_dtype != "bf16" or args.config == "parallel_sampling"):
+    if args.q_len > 1 and (args.kv_dtype != "bf16" or args.config.startswith("parallel_sampling")):
         raise SystemExit("--q-len > 1 runs the 16-bit cache on the decode workloads")
     st = make_workload(args.config, device, seed, args.num_seqs, args.kv_dtype, q_len=args.q_len)
     multi = args.q_len > 1

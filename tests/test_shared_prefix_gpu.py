@@ -9,7 +9,7 @@ import torch
 from oracle.attention import decode_ref, decode_shared_prefix_ref
 from oracle.kv_ops import append_ref, bits, copy_ref, slot_of
 from tests.gpu_util import ATOL, RTOL, assert_close, from_bits, need_gpu, plant_key
-from workloads import SAMPLING, make_sampling_case, make_values, sampling_tables
+from workloads import SAMPLINGS, make_sampling_case, make_values, sampling_tables
 
 pytestmark = pytest.mark.gpu
 
@@ -122,16 +122,16 @@ def test_malformed_description_falls_back_to_plain_attention():
     assert_close(out, decode_ref(q, kp, vp, tables, ctx, 0.088), what="malformed group")
 
 
-def test_parallel_sampling_full_size():
-    """64 prompts x 8 samples: copy-on-write, append, then prefix-aware
-    decode with the groups the host block manager finds."""
-    from paged_kv_cache_254_gb300 import BlockManager
-    case = make_sampling_case(SAMPLING, device="cuda")
+@pytest.mark.parametrize("cfg_name", ["parallel_sampling", "parallel_sampling_aligned"])
+def test_parallel_sampling_full_size(cfg_name):
+    """64 prompts x 8 samples: copy-on-write (none when the prompt fills its
+    blocks), append, then prefix-aware decode over the full shared blocks."""
+    case = make_sampling_case(SAMPLINGS[cfg_name], device="cuda")
     cfg = case.cfg
     B, S = cfg.block_size, cfg.samples
     tables, ctx = sampling_tables(case)
     pairs = np.array([[case.prompt_blocks[i // S][-1], case.private_last[i]]
-                      for i in range(len(ctx)) if case.private_last[i] >= 0], dtype=np.int32)
+                      for i in range(len(ctx)) if case.private_last[i] >= 0], dtype=np.int32).reshape(-1, 2)
     slots = np.concatenate([[slot_of(tables[i], t, B) for t in range(cfg.prompt_len, int(ctx[i]))]
                             for i in range(len(ctx))]).astype(np.int64)
     wk, wv = copy_ref(bits(case.k_pool), bits(case.v_pool), pairs)
@@ -139,7 +139,7 @@ def test_parallel_sampling_full_size():
     pa().pa_copy_blocks(torch.from_numpy(pairs).cuda(), case.k_pool, case.v_pool)
     pa().pa_append_kv(case.k_new, case.v_new, torch.from_numpy(slots).cuda(), case.k_pool, case.v_pool)
     starts = np.arange(0, len(ctx) + 1, S, dtype=np.int32)
-    prefix = np.full(cfg.groups, cfg.prompt_len // B, dtype=np.int32)          # 63 full shared blocks
+    prefix = np.full(cfg.groups, cfg.prompt_len // B, dtype=np.int32)          # the full shared blocks
     err = pa().new_error_word("cuda")
     out = run_sp(case.q, case.k_pool, case.v_pool, tables, ctx, starts, prefix, case.scale, err=err)
     assert pa().pa_read_error(err) == 0

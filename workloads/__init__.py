@@ -10,6 +10,8 @@ the other for data.
 from .synth import (  # noqa: F401
     CONFIGS,
     SAMPLING,
+    SAMPLING_ALIGNED,
+    SAMPLINGS,
     DecodeConfig,
     DecodeCase,
     SamplingConfig,

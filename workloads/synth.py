@@ -232,6 +232,17 @@ class SamplingConfig:
 
 SAMPLING = SamplingConfig()
 
+# The block-aligned reading of the same workload: a 2048-token prompt fills its
+# 64 blocks, so the samples' first writes open fresh blocks and nothing is
+# copied on write.
+SAMPLING_ALIGNED = SamplingConfig(
+    name="parallel_sampling_aligned", prompt_len=2048, seed=1006,
+    description=("parallel sampling, block-aligned prompt: 64 prompt groups x 8 samples, 2048-token "
+                 "shared prompt (64 full blocks of 32, no copy-on-write), divergent tail U[0,256] + 1 "
+                 "new token per sample, 32/8 heads, d 128"))
+
+SAMPLINGS = {c.name: c for c in (SAMPLING, SAMPLING_ALIGNED)}
+
 
 @dataclass
 class SamplingCase:
