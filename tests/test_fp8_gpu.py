@@ -127,6 +127,28 @@ def test_llama3_70b_shape_full_size_sampled():
     assert_close(out, kf_rows, rows=rows, what="fp8 llama3_70b_b256")
 
 
+def test_long_context_mha_full_size_sampled():
+    # 32 sequences x 32,768 tokens x 64 KV heads over an 8-bit pool (17.2 GB),
+    # the launch the bench times; sampled (sequence, head) rows checked
+    cfg = CONFIGS["long_mha_32k"]
+    case = make_decode_case(cfg, device="cuda", values=False)
+    g = torch.Generator(device="cuda").manual_seed(33)
+    q = make_values((cfg.num_seqs, 64, 128), "bf16", g, "cuda")
+    kv = make_codes((case.num_blocks, 64, 2, 16, 128), g, "cuda")
+    out = run(case, q, kv, 0.25, 0.25, "e4m3")
+    assert torch.isfinite(out.float()).all()
+    for s, h in ((0, 0), (13, 37), (31, 63)):
+        nb = -(-int(case.context_lens[s]) // 16)
+        ids = torch.from_numpy(case.block_tables[s, :nb].astype(np.int64)).cuda()
+        sub = kv[ids][:, h:h + 1].contiguous()                   # this head's pieces only
+        kf, vf = dequantized_pools(u8(sub), 16, 0.25, 0.25, "e4m3")
+        want = decode_ref(q[s:s + 1, h:h + 1], kf, vf, np.arange(nb)[None, :], case.context_lens[s:s + 1],
+                          case.scale)
+        assert_close(out[s:s + 1, h:h + 1], want, what=f"32K MHA sequence {s} head {h}")
+    del case, kv
+    torch.cuda.empty_cache()
+
+
 def oracle_rows(case, q, kv, rows):
     """Dequantise only the blocks the sampled rows read."""
     need = sorted({int(b) for s, _ in rows for b in case.block_tables[s][:-(-int(case.context_lens[s]) // 16)]})

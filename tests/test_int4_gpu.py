@@ -117,6 +117,29 @@ def test_full_size_batch_sampled():
         assert_close(out[s:s + 1], want, what=f"sequence {s}")
 
 
+def test_long_context_mha_full_size_sampled():
+    # 32 sequences x 32,768 tokens x 64 KV heads over a 4-bit pool (9.1 GB),
+    # the launch the bench times; sampled (sequence, head) rows checked
+    cfg = CONFIGS["long_mha_32k"]
+    case = make_decode_case(cfg, device="cuda", values=False)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    case.q = make_values((cfg.num_seqs, cfg.num_q_heads, 128), cfg.dtype, g, "cuda")
+    pool = make_int4_pool(case.num_blocks, cfg.num_kv_heads, cfg.block_size, 128, g, "cuda")
+    out = decode(case, pool)
+    assert torch.isfinite(out.float()).all()
+    B = cfg.block_size
+    for s, h in ((0, 0), (13, 37), (31, 63)):
+        nb = -(-int(case.context_lens[s]) // B)
+        ids = torch.from_numpy(case.block_tables[s, :nb].astype(np.int64)).cuda()
+        sub = pool[ids][:, h:h + 1].contiguous()                 # this head's pieces only
+        kf, vf = dequantized_pools(flat(sub), B, 128)
+        want = decode_ref(case.q[s:s + 1, h:h + 1], kf, vf, np.arange(nb)[None, :], case.context_lens[s:s + 1],
+                          case.scale)
+        assert_close(out[s:s + 1, h:h + 1], want, what=f"32K MHA sequence {s} head {h}")
+    del case, pool
+    torch.cuda.empty_cache()
+
+
 def test_dequantized_values_round_trip_through_append():
     # appended rows decode (oracle side) to code * scale of the pages' rule
     from oracle.int4 import quantize_rows
