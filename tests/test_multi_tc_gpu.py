@@ -204,18 +204,20 @@ def test_peaked_and_planted_keys_tcgen05(q_mult, max_q):
     assert_close(run(case, q, qs, max_q=max_q), oracle(case, q, qs), what=f"tcgen05 peaked x{q_mult} q{max_q}")
 
 
-def test_verify_batch_4_token_chunks_sampled():
-    # the 70B-shaped batch with 4-token chunks (three drafted tokens + one; 32
-    # rows per pair), checked on its first 6 sequences
-    cfg = CONFIGS["llama3_70b_b256"]
-    case = make_decode_case(cfg, device="cuda", seed=41)
+@pytest.mark.parametrize("config,q_len", [("llama3_70b_b256", 3), ("llama3_70b_b256", 4), ("llama3_70b_b256", 8),
+                                          ("llama3_8b_b64", 8), ("llama3_8b_b64", 16)])
+def test_verify_batch_chunks_sampled(config, q_len):
+    # the bench's multi-token batches (q_len new tokens per sequence: 24 to
+    # 64 rows per pair), checked on sequences spread over the batch
+    cfg = CONFIGS[config]
+    case = make_decode_case(cfg, device="cuda", seed=41 + q_len)
     N = len(case.context_lens)
-    qs = (np.arange(N + 1) * 4).astype(np.int32)
-    gen = torch.Generator(device="cuda").manual_seed(43)
-    q = make_values((4 * N, cfg.num_q_heads, cfg.head_dim), cfg.dtype, gen, "cuda")
-    got = run(case, q, qs, max_q=4)
-    n = 6
-    ref = decode_multi_ref(q[:4 * n], case.k_pool, case.v_pool, case.block_tables[:n], case.context_lens[:n],
-                           qs[:n + 1], case.scale)
-    assert_close(got[:4 * n], ref, what="70B batch, 4-token chunks")
+    qs = (np.arange(N + 1) * q_len).astype(np.int32)
+    gen = torch.Generator(device="cuda").manual_seed(43 + q_len)
+    q = make_values((q_len * N, cfg.num_q_heads, cfg.head_dim), cfg.dtype, gen, "cuda")
+    got = run(case, q, qs, max_q=q_len)
     assert torch.isfinite(got.float()).all()
+    for s in (0, N // 3, N - 1):
+        ref = decode_multi_ref(q[q_len * s:q_len * (s + 1)], case.k_pool, case.v_pool, case.block_tables[s:s + 1],
+                               case.context_lens[s:s + 1], np.array([0, q_len], dtype=np.int32), case.scale)
+        assert_close(got[q_len * s:q_len * (s + 1)], ref, what=f"{config} {q_len}-token chunks, sequence {s}")
