@@ -353,6 +353,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // across them; the first batch of the next sequence is fetched (tpre)
     // while the current one is in use.
     SegIter is{};             // set by open_chunk before the first issue
+    // the KV stream is read once: its L2 lines go first, so the partial
+    // states written meanwhile are still in L2 when the merge reads them
+    const uint64_t kv_pol = l2_evict_first();
     long long ihi = 0;
     int ilen = 0, ib = 0, tbase = 0;
     int tcur = 0, tnxt = 0, tpre = 0;
@@ -443,9 +446,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 for (int u = 0; u < UB; ++u)
                     if (u == lane) id = ids[u];
                 if ((unsigned)id >= (unsigned)p.NB) id = 0;   // flagged by lane 0 above
-                bulk_load(ring + st * Gm::STAGE_BYTES + Gm::poff(lane),
-                          p.kv8 + ((size_t)id * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES,
-                          full0 + 8 * st);
+                bulk_load_hint(ring + st * Gm::STAGE_BYTES + Gm::poff(lane),
+                               p.kv8 + ((size_t)id * p.Hkv + is.kvh) * Gm::PIECE_BYTES, Gm::PIECE_BYTES,
+                               full0 + 8 * st, kv_pol);
             }
         } else {
             // the block's K and V chunks, one 3-D box each ([column half][BS
@@ -454,8 +457,8 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             __syncwarp();
             if (!aborted && lane < 2) {
                 const int id = (unsigned)ids[0] < (unsigned)p.NB ? ids[0] : 0;   // a bad id is flagged above
-                tma_load_3d(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0), lane ? &tmap_v : &tmap_k, 0,
-                            (id * p.Hkv + is.kvh) * BS, 0, full0 + 8 * st);
+                tma_load_3d_hint(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0),
+                                 lane ? &tmap_v : &tmap_k, 0, (id * p.Hkv + is.kvh) * BS, 0, full0 + 8 * st, kv_pol);
             }
         }
         ++nis;

@@ -277,6 +277,7 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
     long long nis = 0;
     int ist = 0;               // nis % R, kept without a division
     bool idone = false;
+    const uint64_t kv_pol = l2_evict_first();
     auto issue_one = [&]() {   // warp 0 only; the stage's slot is known to be free
         if (idone) return;
         const int st = ist;
@@ -293,9 +294,10 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         __syncwarp();
         // one box per chunk ([column half][BS rows][128 B]): K from lane 0, V
         // from lane 1, side by side
+        // (read once: L2 evict-first)
         if (lane < 2)
-            tma_load_3d(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0), lane ? &tmap_v : &tmap_k, 0,
-                        (id * p.Hkv + is.kvh) * BS, 0, fb);
+            tma_load_3d_hint(ring + st * Gm::STAGE_BYTES + (lane ? Gm::CHUNK_BYTES : 0), lane ? &tmap_v : &tmap_k,
+                             0, (id * p.Hkv + is.kvh) * BS, 0, fb, kv_pol);
         ++nis;
         ++ib;
         if (ib == ilen) {

@@ -244,6 +244,7 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const long long lo = has_work ? sc.lo(blockIdx.x) : 0, hi = has_work ? sc.lo(blockIdx.x + 1) : 0;
 
     if (warp == Tr::COPY_WARP) {
+        const uint64_t kv_pol = l2_evict_first();
         // ================================================================ copies
         int j = 0, st = 0, nseg = 0;            // stage, its ring slot and phase
         uint32_t ph = 0;
@@ -328,10 +329,11 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             const int y = (cid * p.Hkv + it.kvh) * BS;
                             const uint32_t dst = ring + st * Tr::STAGE_BYTES + (kl ? 0 : Tr::KV_BYTES) + ci * Tr::BLK_BYTES;
                             if (ok && lane < 2 * SB && ci < nbs) {
+                                // each block is read once: L2 evict-first
                                 if (kl)
-                                    tma_load_4d(dst, &tmap_k, 0, 0, 0, y / 8, full(st));
+                                    tma_load_4d_hint(dst, &tmap_k, 0, 0, 0, y / 8, full(st), kv_pol);
                                 else
-                                    tma_load_3d(dst, &tmap_v, 0, y, 0, full(st));
+                                    tma_load_3d_hint(dst, &tmap_v, 0, y, 0, full(st), kv_pol);
                             }
                         }
                         ++j;

@@ -266,6 +266,7 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         long long issued = 0;
         bool aborted = false;
         ItemIter it = it0;
+        const uint64_t pol_once = l2_evict_first(), pol_keep = l2_evict_normal();
         while (it.gi_flat < hi && !aborted) {
             const int len = (int)min((long long)(it.pb - it.b0), hi - it.gi_flat);
             const int32_t* trow = p.block_tables + (size_t)it.s0 * p.MB + it.b0;
@@ -312,9 +313,12 @@ pa_prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                         mbar_arrive_expect_tx(fb, Gm::STAGE_BYTES);
                         const int y = (id * p.Hkv + it.kvh) * BS;
                         const uint32_t kdst = ring_u32 + st * Gm::STAGE_BYTES;
-                        // one box per chunk: [column half][BS rows][128 B]
-                        tma_load_3d(kdst, &tmap_k, 0, y, 0, fb);
-                        tma_load_3d(kdst + Gm::CHUNK_BYTES, &tmap_v, 0, y, 0, fb);
+                        // one box per chunk: [column half][BS rows][128 B];
+                        // a group of one row chunk reads its blocks once (L2
+                        // evict-first), one of several once per chunk
+                        const uint64_t pol = it.nch > 1 ? pol_keep : pol_once;
+                        tma_load_3d_hint(kdst, &tmap_k, 0, y, 0, fb, pol);
+                        tma_load_3d_hint(kdst + Gm::CHUNK_BYTES, &tmap_v, 0, y, 0, fb, pol);
                     }
                     issued += run;
                     done += run;
