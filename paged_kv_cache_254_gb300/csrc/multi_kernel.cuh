@@ -494,11 +494,18 @@ pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_
     const int c = (int)blockIdx.x + 1;            // boundary between chunks c - 1 and c
     if (c >= sc.NS) return;
     const long long x = sc.lo(c);
-    // the pair holding flattened block x: sequence s with cum[s] Hkv <= x < cum[s + 1] Hkv
+    // the pair holding flattened block x: sequence s with cum[s] Hkv <= x <
+    // cum[s + 1] Hkv, by a 32-way search (one probe per lane per round, so
+    // two rounds of dependent loads up to 1,024 sequences); every warp runs
+    // it, so the block needs no barrier
     int a = 0, b = N;
     while (b - a > 1) {
-        const int m = (a + b) >> 1;
-        if (cum[m] * Hkv <= x) a = m; else b = m;
+        const int step = (b - a + 31) / 32;
+        const int idx = a + lane * step;
+        const bool le = idx < b && cum[idx] * Hkv <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        a += (31 - __clz(m)) * step;                  // lane 0 probes a, which always holds
+        b = min(a + step, b);
     }
     const int s = a;
     const int nb = (int)(cum[s + 1] - cum[s]);
