@@ -284,6 +284,9 @@ pa_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // Everything above is CTA-local; the pre-pass's outputs (and whatever the
     // stream wrote before it) are read only after the previous kernel is done.
     griddep_wait();
+    // The merge post-pass may be scheduled now: its CTAs take SMs as this
+    // grid's CTAs retire and wait (griddepcontrol.wait) for the whole grid.
+    griddep_launch_dependents();
     const bool in_smem = p.N <= Tr::CUM_SMEM;
     if (in_smem) {
         for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) {
@@ -773,6 +776,7 @@ template <int D>
 __global__ void __launch_bounds__(256, 4)
 pa_decode_merge(const long long* __restrict__ cum, const float* __restrict__ partials, uint16_t* __restrict__ out,
                 int N, int Hkv, int G, long long nworkers, int nd, float v_scale, int bf16) {
+    griddep_wait();   // the decode grid is complete and its writes visible
     constexpr int PSTRIDE = D + 4;
     constexpr int LPH = D / 4;                     // lanes per head
     constexpr int HPW = 32 / LPH;                  // heads per warp

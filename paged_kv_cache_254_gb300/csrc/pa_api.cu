@@ -170,9 +170,19 @@ cudaError_t merge_launch(const DecodeLaunch& L, int g, long long nworkers, cudaS
     constexpr int HPW = 32 / (D / 4);
     const long long tasks = (long long)L.p.N * L.p.Hkv * ((g + HPW - 1) / HPW);
     const long long blocks = (tasks + 7) / 8;
-    pa_decode_merge<D><<<(unsigned)blocks, 256, 0, st>>>(L.p.cum, L.p.partials, L.p.out, L.p.N, L.p.Hkv, g,
-                                                         nworkers, L.p.nd, L.p.v_scale, L.bf16 ? 1 : 0);
-    return cudaGetLastError();
+    // programmatic stream serialization: the merge's CTAs are placed as the
+    // decode's retire, then wait for the decode grid (griddep_wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pa_decode_merge<D>, L.p.cum, static_cast<const float*>(L.p.partials), L.p.out,
+                              L.p.N, L.p.Hkv, g, nworkers, L.p.nd, L.p.v_scale, L.bf16 ? 1 : 0);
 }
 
 // Lay out the decode region, run the pre-pass, fill L's scheduling fields,
