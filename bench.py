@@ -48,9 +48,9 @@ FALLBACK_HBM_GBS = 6800.0
 # workload or kernel instantiation) reports null.
 #   (hash, kv dtype, workload): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("b7e06e569c4fd8cc", "bf16", "llama3_70b_b256"): (1_217_311_488 + 7_236_352, 1_216_111_324),
-    ("b7e06e569c4fd8cc", "fp8_e4m3", "llama3_70b_b256"): (609_407_488 + 6_949_376, 609_141_468),
-    ("b7e06e569c4fd8cc", "int4", "llama3_70b_b256"): (324_340_992 + 4_538_624, 324_624_348),
+    ("0abab86476c76ebf", "bf16", "llama3_70b_b256"): (1_217_307_136 + 7_269_376, 1_216_111_324),
+    ("0abab86476c76ebf", "fp8_e4m3", "llama3_70b_b256"): (609_414_144 + 6_953_728, 609_141_468),
+    ("0abab86476c76ebf", "int4", "llama3_70b_b256"): (324_374_272 + 4_313_856, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")

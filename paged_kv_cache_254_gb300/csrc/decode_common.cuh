@@ -12,6 +12,24 @@
 
 namespace pa {
 
+// Launch configuration with programmatic stream serialization: the kernel
+// may start while the stream's previous kernel runs, and waits for it with
+// griddepcontrol.wait before reading anything the stream wrote.  `attr`
+// holds the attribute the configuration points to.
+inline cudaLaunchConfig_t pdl_config(long long grid, int threads, int smem, cudaStream_t stream,
+                                     cudaLaunchAttribute (&attr)[1]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 // One (block, KV head) chunk of the 16-bit cache as it sits in a ring stage:
 // HALVES boxes of BS rows x 128 bytes, 128-byte swizzled; the K chunk, then
 // the V chunk.  One stage holds one block.

@@ -878,16 +878,8 @@ template <class Tr>
 cudaError_t decode_launch(const DecodeLaunch& L) {
     // launched with programmatic stream serialization: the CTAs' set-up
     // overlaps the pre-pass, and the kernel waits for it (griddep_wait)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)L.grid);
-    cfg.blockDim = dim3(Tr::THREADS);
-    cfg.dynamicSmemBytes = Tr::SMEM_BYTES;
-    cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const cudaLaunchConfig_t cfg = pdl_config(L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream, attr);
     return cudaLaunchKernelEx(&cfg, pa_decode_kernel<Tr>, *L.tmap_k, *L.tmap_v, L.p);
 }
 

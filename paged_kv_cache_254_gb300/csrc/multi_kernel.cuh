@@ -217,6 +217,11 @@ pa_multi_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constan
         prefetch_tmap(&tmap_v);
         *abort_flag = 0;
     }
+    // launched with programmatic stream serialization after the pre-pass:
+    // the set-up above overlaps it; nothing the stream wrote is read before
+    // it completes.  The merge post-pass may then be placed as CTAs retire.
+    griddep_wait();
+    griddep_launch_dependents();
     const bool in_smem = p.N <= Tr::CUM_SMEM;
     if (in_smem) {
         for (int i = threadIdx.x; i <= p.N; i += Tr::THREADS) {
@@ -484,6 +489,7 @@ pa_multi_merge(const long long* __restrict__ cum, const int32_t* __restrict__ q_
                const int32_t* __restrict__ context_lens, const float* __restrict__ partials,
                uint16_t* __restrict__ out, int N, int Hkv, int G, int rows_per_chunk, int nchunks_hint,
                int max_q, int total_q, int bf16) {
+    griddep_wait();   // the attention grid is complete and its writes visible
     constexpr int PSTRIDE = D + 4;
     constexpr int LPR = D / 4;                    // lanes per row
     constexpr int RPW = 32 / LPR;                 // rows per warp
@@ -607,8 +613,9 @@ struct MultiKernelInfo {
 
 template <class Tr>
 cudaError_t multi_launch(const MultiLaunch& L) {
-    pa_multi_kernel<Tr><<<L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream>>>(*L.tmap_k, *L.tmap_v, L.p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream, attr);
+    return cudaLaunchKernelEx(&cfg, pa_multi_kernel<Tr>, *L.tmap_k, *L.tmap_v, L.p);
 }
 
 template <class Tr>

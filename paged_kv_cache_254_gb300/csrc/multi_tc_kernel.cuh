@@ -212,6 +212,11 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched with programmatic stream serialization after the pre-pass:
+    // the set-up above overlaps it; nothing the stream wrote is read before
+    // it completes.  The merge post-pass may then be placed as CTAs retire.
+    griddep_wait();
+    griddep_launch_dependents();
 
     SeqTab tab;
     tab.cum = p.cum;
@@ -771,8 +776,9 @@ pa_multi_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 
 template <class Tr>
 cudaError_t multi_tc_launch(const MultiLaunch& L) {
-    pa_multi_tc_kernel<Tr><<<L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream>>>(*L.tmap_q, *L.tmap_k, *L.tmap_v, L.p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(L.grid, Tr::THREADS, Tr::SMEM_BYTES, L.stream, attr);
+    return cudaLaunchKernelEx(&cfg, pa_multi_tc_kernel<Tr>, *L.tmap_q, *L.tmap_k, *L.tmap_v, L.p);
 }
 
 template <class Tr>

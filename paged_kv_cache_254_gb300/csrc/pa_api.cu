@@ -172,15 +172,8 @@ cudaError_t merge_launch(const DecodeLaunch& L, int g, long long nworkers, cudaS
     const long long blocks = (tasks + 7) / 8;
     // programmatic stream serialization: the merge's CTAs are placed as the
     // decode's retire, then wait for the decode grid (griddep_wait)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(256);
-    cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const cudaLaunchConfig_t cfg = pdl_config(blocks, 256, 0, st, attr);
     return cudaLaunchKernelEx(&cfg, pa_decode_merge<D>, L.p.cum, static_cast<const float*>(L.p.partials), L.p.out,
                               L.p.N, L.p.Hkv, g, nworkers, L.p.nd, L.p.v_scale, L.bf16 ? 1 : 0);
 }
@@ -871,14 +864,17 @@ pa_status pa_decode_multi(const pa_shape* shape, int32_t max_q_len, int32_t tota
     if (k->launch(L) != cudaSuccess) return PA_ERR_CUDA;
     const int g = shape->num_q_heads / shape->num_kv_heads;
     if (ctas > 1) {   // one CTA per chunk boundary: the pairs cut there
-        if (shape->head_dim == 128)
-            pa_multi_merge<128><<<ctas - 1, MERGE_THREADS, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
-                                                                d.Hkv, g, k->rows, ctas, max_q_len, total_q,
-                                                                shape->dtype == PA_BF16);
-        else
-            pa_multi_merge<64><<<ctas - 1, MERGE_THREADS, 0, L.stream>>>(d.cum, q_start, context_lens, d.partials, d.out, d.N,
-                                                               d.Hkv, g, k->rows, ctas, max_q_len, total_q,
-                                                               shape->dtype == PA_BF16);
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = pdl_config(ctas - 1, MERGE_THREADS, 0, L.stream, attr);
+        const float* parts = d.partials;
+        const int bf = shape->dtype == PA_BF16;
+        const cudaError_t e =
+            shape->head_dim == 128
+                ? cudaLaunchKernelEx(&cfg, pa_multi_merge<128>, d.cum, q_start, context_lens, parts, d.out, d.N,
+                                     d.Hkv, g, k->rows, ctas, max_q_len, total_q, bf)
+                : cudaLaunchKernelEx(&cfg, pa_multi_merge<64>, d.cum, q_start, context_lens, parts, d.out, d.N, d.Hkv,
+                                     g, k->rows, ctas, max_q_len, total_q, bf);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
