@@ -258,10 +258,11 @@ pa_status pa_copy_blocks_fp8(const pa_shape* shape, const int32_t* src_dst_pairs
  * checks the claim: a member whose table or length breaks it, or a malformed
  * group description, sets PA_DEVERR_GROUP and the affected rows are NaN (a
  * malformed group is treated as having no prefix); no access leaves the
- * tables, pools or workspace.  Two launches on `stream`: the prefix pass
- * (one (group, KV head) item reads the shared blocks for up to 32 query rows)
- * and the decode over each sequence's own blocks, which folds the prefix
- * state in by the log-sum-exp rule.  Workspace: see
+ * tables, pools or workspace.  On `stream`: a memset of the workspace's
+ * counters, the prefix pass (one (group, KV head) item reads the shared
+ * blocks for up to 32 query rows), then the decode's pre-pass, attention
+ * kernel and merge over each sequence's own blocks, the attention kernel
+ * folding the prefix state in by the log-sum-exp rule.  Workspace: see
  * pa_decode_shared_prefix_workspace_bytes (no initialisation needed).
  */
 size_t pa_decode_shared_prefix_workspace_bytes(const pa_shape* shape);

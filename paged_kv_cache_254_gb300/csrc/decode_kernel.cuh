@@ -20,9 +20,10 @@
 // out SMs that get less memory bandwidth or more segment ends than others.
 // A pair that lies inside one chunk is finished by its warp; a pair cut by
 // chunk boundaries leaves a partial state (m, l, unnormalised o) per piece in
-// the workspace, and a post-pass kernel (pa_decode_merge, one warp per pair)
-// merges the pieces with the log-sum-exp rule in chunk order, so no warp ever
-// waits on another.  Chunk boundaries depend on context lengths and the grid only, never
+// the workspace, and a post-pass kernel (pa_decode_merge, one warp per pair
+// and query head, launched to wait on this grid with griddepcontrol) merges
+// the pieces with the log-sum-exp rule in chunk order, so no warp ever waits
+// on another.  Chunk boundaries depend on context lengths and the grid only, never
 // on block ids or on which warp took a chunk, so results are bitwise
 // independent of block placement and of timing.  A chunk start is found by a
 // search over per-sequence block prefix sums (written by a pre-pass kernel,
@@ -35,9 +36,10 @@
 // combination.
 //
 // Inside a warp.  Each warp owns R shared-memory stages with one mbarrier
-// each.  The copies of a stage (two-dimensional TMA loads with 128-byte
-// swizzle for the 16-bit cache, one bulk copy per block piece for the
-// quantized caches) are issued R stages ahead of the one being computed, and
+// each.  The copies of a stage (one 3-D TMA box with 128-byte swizzle per
+// block for K and one for V in the 16-bit cache, one bulk copy per block
+// piece for the quantized caches, all under an L2 evict-first policy: the
+// stream is read once) are issued R stages ahead of the one being computed, and
 // a stage is refilled as soon as it has been folded in (mma.sync scores,
 // online softmax, PV: consume_block for the 16-bit cache with the query heads
 // as MMA rows; consume_stage8t / consume_stage4t for the quantized caches
