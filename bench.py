@@ -48,9 +48,9 @@ FALLBACK_HBM_GBS = 6800.0
 # workload or kernel instantiation) reports null.
 #   (hash, kv dtype, workload): (captured dram bytes, algorithmic bytes of the captured launch)
 TRAFFIC = {
-    ("0abab86476c76ebf", "bf16", "llama3_70b_b256"): (1_217_307_136 + 7_269_376, 1_216_111_324),
-    ("0abab86476c76ebf", "fp8_e4m3", "llama3_70b_b256"): (609_414_144 + 6_953_728, 609_141_468),
-    ("0abab86476c76ebf", "int4", "llama3_70b_b256"): (324_374_272 + 4_313_856, 324_624_348),
+    ("f1214767ababa837", "bf16", "llama3_70b_b256"): (1_217_302_272 + 7_294_976, 1_216_111_324),
+    ("f1214767ababa837", "fp8_e4m3", "llama3_70b_b256"): (609_424_128 + 7_066_112, 609_141_468),
+    ("f1214767ababa837", "int4", "llama3_70b_b256"): (324_384_000 + 4_621_312, 324_624_348),
 }
 
 KERNEL_SOURCES = ("decode_kernel.cuh", "decode_common.cuh", "decode_tok.cuh", "ptx.cuh")
